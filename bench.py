@@ -1,0 +1,494 @@
+"""Benchmark of the low-precision linear-layer hot path on one GB300.
+
+Workload (the decode configuration the headline metric is quoted on): an
+8B-class decoder layer set -- q/o 4096x4096, k/v 1024x4096, gate/up
+14336x4096, down 4096x14336, bf16 weights ~N(0, 0.02) with 0.1% x20
+outliers -- in NVFP4 with LoRA r = 32 (alpha = 64), decoding 1, 8 and 64
+tokens.  One step is one pass of the whole hot path over that layer set:
+
+  requant  re-quantize all 7 bf16 weights to NVFP4 (absmax sweep + encode)
+  decode   W4A16 + LoRA linear of all 7 layers at M = 1, 8 and 64
+  prefill  the same linears at M = 4096 (activations with 1% x10 channels)
+  fp8      FP8 path at M = 4096: activation 1x128 quantize, 128x128 weight
+           re-quantize, blockwise-scaled GEMM
+
+Each phase is timed with CUDA events on the launching stream after an L2
+flush (a 512 MB write), so no phase reads its weights from L2 left by the
+previous one.  ``value`` is the decode phase's HBM throughput: its
+algorithmic bytes (packed codes, block and tensor scales, LoRA factors,
+activations in, outputs out) over its device time; the other phases are
+reported in ``breakdown`` with their own roofline fractions.
+
+``--impl reference`` times the CPU oracle instead (a bounded sample of the
+same workload per step, on the host's cores) and prints the same line with
+``"impl": "reference"``.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from quantized_rl_rollout_gb300 import configs, inputs  # noqa: E402
+
+METRIC = "NVFP4+LoRA linear: decode HBM GB/s, prefill TFLOPS; % of roofline"
+WORKLOAD = "decode, 8B-class layer set (q/o 4096x4096, k/v 1024x4096, gate/up 14336x4096, down 4096x14336), NVFP4 + LoRA r=32, M=1,8,64"
+DECODE_TOKENS = (1, 8, 64)
+PREFILL_TOKENS = 4096
+R = 32
+ALPHA = 2.0 * R
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            out = dict(FALLBACK_PEAKS)
+            for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                if key in d and isinstance(d[key], (int, float)):
+                    out[key] = float(d[key])
+            out["source"] = "measured"
+            return out
+        except (OSError, ValueError):
+            pass
+    return dict(FALLBACK_PEAKS)
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes / flops
+
+
+def decode_bytes(layers, m, r):
+    total = 0
+    for l in layers:
+        total += l.n * l.k // 2 + l.n * l.k // 16 + 4  # codes, block scales, tensor scale
+        total += 2 * r * (l.k + l.n)  # LoRA A and B
+        total += 2 * m * l.k + 2 * m * l.n  # x in, y out
+    return total
+
+
+def linear_flops(layers, m, r):
+    return sum(2 * m * l.n * l.k + 2 * m * r * (l.k + l.n) for l in layers)
+
+
+def requant_nvfp4_bytes(layers):
+    # two sweeps over the bf16 weight (the codes depend on the tensor-wide absmax)
+    return sum(2 * 2 * l.n * l.k + l.n * l.k // 2 + l.n * l.k // 16 + 4 for l in layers)
+
+
+def fp8_quant_bytes(layers, m):
+    w = sum(2 * l.n * l.k + l.n * l.k + 4 * ((l.n + 127) // 128) * (l.k // 128) for l in layers)
+    a = sum(2 * m * l.k + m * l.k + 4 * m * (l.k // 128) for l in layers)
+    return w, a
+
+
+# ---------------------------------------------------------------------------
+
+
+class Clocks:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown," \
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown," \
+             "clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+class Workload:
+    """Device tensors of one step (weights resident in HBM before timing)."""
+
+    def __init__(self, qrr, device, seed=0):
+        self.q = qrr
+        self.dev = device
+        self.layers = configs.LAYERS_8B
+        L = self.layers
+        self.W = [inputs.weight(l.n, l.k, inputs.derive_seed(seed, "8b", l.name, "W"), device=device) for l in L]
+        self.lora = [inputs.lora(R, l.k, l.n, inputs.derive_seed(seed, "8b", l.name, "lora"), device=device)[:2]
+                     for l in L]
+        self.nv = [(torch.empty(l.n, l.k // 2, dtype=torch.uint8, device=device),
+                    torch.empty(l.n, l.k // 16, dtype=torch.uint8, device=device),
+                    torch.empty(1, dtype=torch.float32, device=device)) for l in L]
+        self.xd = {m: [inputs.activations(m, l.k, inputs.derive_seed(seed, "8b", l.name, "x", m), device=device)
+                       for l in L] for m in DECODE_TOKENS}
+        self.yd = {m: [torch.empty(m, l.n, dtype=torch.bfloat16, device=device) for l in L] for m in DECODE_TOKENS}
+        self.xp = [inputs.activations(PREFILL_TOKENS, l.k, inputs.derive_seed(seed, "8b", l.name, "xp"), device=device,
+                                      channel_outlier_frac=0.01) for l in L]
+        self.yp = [torch.empty(PREFILL_TOKENS, l.n, dtype=torch.bfloat16, device=device) for l in L]
+        self.f8w = [(torch.empty(l.n, l.k, dtype=torch.uint8, device=device),
+                     torch.empty((l.n + 127) // 128, l.k // 128, dtype=torch.float32, device=device)) for l in L]
+        self.f8a = [(torch.empty(PREFILL_TOKENS, l.k, dtype=torch.uint8, device=device),
+                     torch.empty(PREFILL_TOKENS, l.k // 128, dtype=torch.float32, device=device)) for l in L]
+        self.yf = [torch.empty(PREFILL_TOKENS, l.n, dtype=torch.bfloat16, device=device) for l in L]
+        ws = max(qrr.linear_nvfp4_lora_workspace_bytes(PREFILL_TOKENS, l.n, l.k, R) for l in L)
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
+        self.rq_ws = torch.empty(4096, dtype=torch.uint8, device=device)
+        self.flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
+        self.launches = 0
+
+    # each phase returns the number of library kernels it launched
+    def requant(self):
+        self.q.requantize_weights(self.W, self.nv, self.q.FORMAT_NVFP4, workspace=self.rq_ws)
+        return 2
+
+    def decode(self, m):
+        for i, _ in enumerate(self.layers):
+            c, s, t = self.nv[i]
+            A, B = self.lora[i]
+            self.q.linear_nvfp4_lora(self.xd[m][i], c, s, t, A, B, ALPHA, y=self.yd[m][i], workspace=self.ws)
+        return 2 * len(self.layers)
+
+    def prefill(self):
+        for i, _ in enumerate(self.layers):
+            c, s, t = self.nv[i]
+            A, B = self.lora[i]
+            self.q.linear_nvfp4_lora(self.xp[i], c, s, t, A, B, ALPHA, y=self.yp[i], workspace=self.ws)
+        return 2 * len(self.layers)
+
+    def fp8_quant(self):
+        self.q.requantize_weights(self.W, self.f8w, self.q.FORMAT_FP8_W128)
+        for i, _ in enumerate(self.layers):
+            self.q.quantize_fp8_a1x128(self.xp[i], q=self.f8a[i][0], scales=self.f8a[i][1])
+        return 1 + len(self.layers)
+
+    def fp8_gemm(self):
+        for i, _ in enumerate(self.layers):
+            qa, sa = self.f8a[i]
+            qw, sw = self.f8w[i]
+            self.q.gemm_fp8_blockwise(qa, sa, qw, sw, y=self.yf[i])
+        return len(self.layers)
+
+    def do_flush(self):
+        self.flush.fill_(self.launches & 0xFF)
+
+
+PHASES = ["requant", "decode_m1", "decode_m8", "decode_m64", "prefill", "fp8_quant", "fp8_gemm"]
+
+
+def run_phase(w, name):
+    if name == "requant":
+        return w.requant()
+    if name.startswith("decode_m"):
+        return w.decode(int(name[len("decode_m"):]))
+    if name == "prefill":
+        return w.prefill()
+    if name == "fp8_quant":
+        return w.fp8_quant()
+    return w.fp8_gemm()
+
+
+def timed_steps(w, steps, phases):
+    """Per-phase device ms (lists over steps) and kernel launches in the timed region."""
+    stream = torch.cuda.current_stream()
+    times = {p: [] for p in phases}
+    launches = 0
+    for _ in range(steps):
+        for p in phases:
+            w.do_flush()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            launches += run_phase(w, p)
+            e1.record(stream)
+            times[p].append((e0, e1))
+    torch.cuda.synchronize()
+    out = {p: [a.elapsed_time(b) for a, b in times[p]] for p in phases}
+    return out, launches
+
+
+def e2e_decode(w, steps):
+    """Decode through the public API with host buffers: per step, copy every
+    layer's tokens from pinned host memory, run the 7 linears, copy y back."""
+    hx = {m: [x.cpu().pin_memory() for x in w.xd[m]] for m in DECODE_TOKENS}
+    hy = {m: [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in w.yd[m]] for m in DECODE_TOKENS}
+    dx = {m: [torch.empty_like(x) for x in w.xd[m]] for m in DECODE_TOKENS}
+    h2d = sum(x.numel() * 2 for m in DECODE_TOKENS for x in hx[m])
+    d2h = sum(y.numel() * 2 for m in DECODE_TOKENS for y in hy[m])
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for m in DECODE_TOKENS:
+            for i, _ in enumerate(w.layers):
+                dx[m][i].copy_(hx[m][i], non_blocking=True)
+                c, s, t = w.nv[i]
+                A, B = w.lora[i]
+                w.q.linear_nvfp4_lora(dx[m][i], c, s, t, A, B, ALPHA, y=w.yd[m][i], workspace=w.ws)
+                hy[m][i].copy_(w.yd[m][i], non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(steps):
+        w.do_flush()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        one()
+        e1.record(stream)
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    return statistics.median(ms), h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing
+
+
+def oracle_decode_sample(seconds_target):
+    """Time the oracle on a bounded sample of the decode workload: NVFP4
+    quantize of the q layer (4096 x 4096) once, then the float64 W4A16 +
+    LoRA linear for 1, 8 and 64 tokens, repeated until ~seconds_target.
+    Returns (GB/s of decode bytes handled, seconds, sample description)."""
+    import oracle
+
+    layer = configs.LAYERS_8B[0]
+    g = np.random.default_rng(0)
+    w = g.standard_normal((layer.n, layer.k)).astype(np.float32) * np.float32(0.02)
+    w = oracle.formats.bf16_rne(w)
+    a = oracle.formats.bf16_rne(g.standard_normal((R, layer.k)) * 0.01)
+    b = oracle.formats.bf16_rne(g.standard_normal((layer.n, R)) * 0.01)
+    t0 = time.perf_counter()
+    codes, scales, s_t = oracle.nvfp4.quantize(w)
+    bytes_done = 0
+    reps = 0
+    while True:
+        for m in DECODE_TOKENS:
+            x = oracle.formats.bf16_rne(g.standard_normal((m, layer.k)))
+            oracle.linear.linear_nvfp4_lora(x, codes, scales, s_t, a, b, ALPHA)
+            bytes_done += decode_bytes([layer], m, R)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds_target:
+            break
+    secs = time.perf_counter() - t0
+    desc = (f"oracle NVFP4 quantize of one 4096x4096 layer + float64 W4A16+LoRA linear at M=1,8,64, "
+            f"{reps} repetitions, decode bytes of that layer per repetition")
+    return bytes_done / secs / 1e9, secs, desc
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ---------------------------------------------------------------------------
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        return rank, world, local, dist
+    return 0, 1, 0, None
+
+
+def max_over_ranks(dist, value):
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--phases", default=",".join(PHASES))
+    args = ap.parse_args()
+    warmup = max(3, args.warmup)
+    rank, world, local, dist = dist_setup(args.gpus)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        vals = []
+        total_s = 0.0
+        desc = ""
+        for i in range(warmup + args.steps):
+            v, s, desc = oracle_decode_sample(seconds_target=2.0)
+            if i >= warmup:
+                vals.append(v)
+                total_s += s
+        value = statistics.median(vals)
+        cores = cpu_cores()
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+                "steps": args.steps, "warmup": warmup, "ms_per_step": 1000.0 * total_s / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "sample": desc},
+                "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc},
+                "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    from quantized_rl_rollout_gb300 import qrr
+
+    qrr.lib()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    phases = [p for p in args.phases.split(",") if p]
+    w = Workload(qrr, device)
+    # warm-up (untimed)
+    for _ in range(warmup):
+        for p in phases:
+            run_phase(w, p)
+    torch.cuda.synchronize()
+
+    clocks = Clocks(local)
+    clocks.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    per_phase, launches = timed_steps(w, args.steps, phases)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+
+    med = {p: statistics.median(v) for p, v in per_phase.items()}
+    L = configs.LAYERS_8B
+    peaks = load_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops"]  # nominal FP8:BF16 dense ratio of 2
+    breakdown = {}
+    dec_bytes = 0
+    dec_ms = 0.0
+    for p in phases:
+        ms = med[p]
+        if p.startswith("decode_m"):
+            m = int(p[len("decode_m"):])
+            b = decode_bytes(L, m, R)
+            dec_bytes += b
+            dec_ms += ms
+            breakdown[p] = {"ms": ms, "GB/s": b / ms / 1e6, "frac_hbm": b / ms / 1e6 / peaks["hbm_gbs"],
+                            "bytes": b}
+        elif p == "requant":
+            b = requant_nvfp4_bytes(L)
+            breakdown[p] = {"ms": ms, "GB/s": b / ms / 1e6, "frac_hbm": b / ms / 1e6 / peaks["hbm_gbs"], "bytes": b}
+        elif p == "prefill":
+            f = linear_flops(L, PREFILL_TOKENS, R)
+            breakdown[p] = {"ms": ms, "TFLOP/s": f / ms / 1e9, "frac_bf16": f / ms / 1e9 / peaks["bf16_tflops"],
+                            "flops": f}
+        elif p == "fp8_quant":
+            bw, ba = fp8_quant_bytes(L, PREFILL_TOKENS)
+            breakdown[p] = {"ms": ms, "GB/s": (bw + ba) / ms / 1e6, "frac_hbm": (bw + ba) / ms / 1e6 / peaks["hbm_gbs"],
+                            "bytes": bw + ba}
+        elif p == "fp8_gemm":
+            f = sum(2 * PREFILL_TOKENS * l.n * l.k for l in L)
+            breakdown[p] = {"ms": ms, "TFLOP/s": f / ms / 1e9, "frac_fp8_nominal": f / ms / 1e9 / fp8_peak, "flops": f}
+
+    step_ms = sum(med.values())
+    step_ms = max_over_ranks(dist, step_ms)
+    dec_ms_all = max_over_ranks(dist, dec_ms) if dec_ms else 0.0
+    value = world * dec_bytes / dec_ms_all / 1e6 if dec_ms_all else None
+
+    # dominant phase -> roofline object
+    dom = max(phases, key=lambda p: med[p])
+    d = breakdown[dom]
+    if "GB/s" in d:
+        roof = {"bound": "hbm", "achieved": d["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": d["GB/s"] / peaks["hbm_gbs"], "traffic": None, "kernel_phase": dom}
+    elif dom == "fp8_gemm":
+        roof = {"bound": "tensor", "achieved": d["TFLOP/s"], "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": d["TFLOP/s"] / fp8_peak, "traffic": None, "kernel_phase": dom}
+    else:
+        roof = {"bound": "tensor", "achieved": d["TFLOP/s"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": d["TFLOP/s"] / peaks["bf16_tflops"], "traffic": None, "kernel_phase": dom}
+    roof["peak_source"] = peaks["source"]
+
+    e2e = None
+    cpu = None
+    if rank == 0 and any(p.startswith("decode_m") for p in phases):
+        e_ms, h2d, d2h = e2e_decode(w, max(3, args.steps))
+        e_bytes = sum(decode_bytes(L, m, R) for m in DECODE_TOKENS)
+        e2e = {"value": e_bytes / e_ms / 1e6, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_ms}
+        v, s, desc = oracle_decode_sample(seconds_target=12.0)
+        cpu = {"value": v, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc, "seconds": s}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "nvfp4-w/bf16-act/fp32-acc", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "phases": phases, "l2": "flushed (512 MB write) before every phase",
+                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                "roofline": roof, "breakdown": breakdown, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches, "clocks": clk, "wall_s_timed": wall,
+                "peaks": peaks}
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

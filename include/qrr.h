@@ -1,0 +1,192 @@
+/*
+ * qrr.h -- C ABI of the GB300 (sm_103a) low-precision linear-layer library
+ * for RL rollout: NVFP4 W4A16 + BF16 LoRA linear, blockwise FP8 quantize +
+ * GEMM, and re-quantization of all weights after a training step.
+ *
+ * Sources (page title, section):
+ *  - "QeRL: Beyond Efficiency -- Quantization-enhanced Reinforcement Learning
+ *    for LLMs", abstract: NVFP4 weights combined with LoRA speed up rollout.
+ *  - "NVIDIA and MIT Collaborate on QeRL", Key Features and the paragraph
+ *    after them: the policy's weight path moves to NVFP4 while logits and
+ *    gradients stay in higher precision; prefill and decode both speed up.
+ *  - "NVIDIA NeMo RL behaalt 48% snelheidswinst met end-to-end
+ *    FP8-precisietraining", section "De technische doorbraak": blockwise E4M3
+ *    with 128x128 weight tiles and 1x128 activation blocks, FP8 linear
+ *    layers; section "Praktische prestatiewinsten": scales recalibrated after
+ *    every training step; last paragraph before "Waarom dit belangrijk is":
+ *    optional power-of-two scale factors.
+ *
+ * Formats.  The pages name NVFP4 but do not spell it out; this library uses
+ * the standard layout: element code E2M1 (magnitudes 0, .5, 1, 1.5, 2, 3, 4,
+ * 6; bit 3 = sign), two codes per byte with the even K index in the low
+ * nibble; one E4M3 (FN) block scale per 16 consecutive elements of a row; one
+ * FP32 tensor scale.  Element (n, k) decodes to
+ * e2m1(code) * e4m3(scale[n][k/16]) * tensor_scale.  Quantization:
+ *   s_t = amax(W) / 2688            (fp32, correctly rounded)
+ *   s_b = e4m3_rne(amax_b / (6 * s_t))
+ *   d_b = e4m3(s_b) * s_t
+ *   code = e2m1_rne(x / d_b)        (x / d_b a correctly rounded fp32 quotient)
+ * with round-to-nearest-even, saturation to the largest finite value, the
+ * input's sign kept, all-zero codes where d_b == 0 and s_t == 0 for an
+ * all-zero tensor.
+ *
+ * Conventions shared by every call.
+ *  - All pointers except `descs` of qrr_requantize_weights are DEVICE
+ *    pointers on the current CUDA device, owned by the caller.  The library
+ *    allocates no memory; calls that need scratch take a caller-owned
+ *    `workspace` whose size the matching *_workspace_bytes() query returns.
+ *  - Matrices are row-major and contiguous.  Weights use nn.Linear
+ *    orientation W[N = out][K = in], y = x . W^T; LoRA uses A[r][K], B[N][r].
+ *  - bf16 / fp32 / byte pointers must be 16-byte aligned.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) and never synchronizes with the host.  The tensor
+ *    scale stays on the device, so quantize -> linear never round-trips.
+ *  - Return value: QRR_OK, or an error detected on the host before anything
+ *    is launched (invalid argument, unsupported shape, misalignment, small
+ *    workspace), or QRR_ERR_CUDA when a launch fails.
+ *  - `dev_status` (nullable, device int32): conditions found on the device are
+ *    OR-ed into it (QRR_DEV_NONFINITE: a non-finite input was seen; the
+ *    outputs are then unspecified).  The library never clears it; the caller
+ *    zeroes it and reads it when it chooses.
+ */
+#ifndef QRR_H_
+#define QRR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum qrr_status {
+  QRR_OK = 0,
+  QRR_ERR_INVALID_ARG = 1,       /* null pointer, negative size, unknown enum value */
+  QRR_ERR_UNSUPPORTED_SHAPE = 2, /* a size constraint of the call is not met */
+  QRR_ERR_MISALIGNED = 3,        /* a pointer is not 16-byte aligned */
+  QRR_ERR_WORKSPACE = 4,         /* workspace missing or smaller than the query says */
+  QRR_ERR_CUDA = 5               /* a CUDA runtime call or a kernel launch failed */
+} qrr_status;
+
+/* Bits OR-ed into the optional device status word. */
+#define QRR_DEV_NONFINITE 0x1
+
+typedef enum qrr_scale_mode {
+  QRR_SCALE_FP32 = 0, /* s = fp32(amax / 448); codes e4m3_rne(x / s) */
+  QRR_SCALE_POW2 = 1  /* s = smallest power of two >= fp32(amax / 448); codes e4m3_rne(x * 2^-e) */
+} qrr_scale_mode;
+
+typedef enum qrr_format {
+  QRR_FORMAT_NVFP4 = 0,   /* codes [N][K/2], E4M3 scales [N][K/16], fp32 tensor scale */
+  QRR_FORMAT_FP8_W128 = 1 /* E4M3 codes [N][K], fp32 scales [ceil(N/128)][K/128] */
+} qrr_format;
+
+/* Human-readable name of a qrr_status value (static storage). */
+const char* qrr_status_string(int status);
+
+/* ABI version of this header (bumped on any signature change). */
+int qrr_abi_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* NVFP4 quantization of one bf16 weight ("QeRL: Beyond Efficiency",
+ * abstract; layout and formula above).
+ *   W            bf16 [N][K], K a multiple of 32, N >= 0
+ *   codes        uint8 [N][K/2]  (out)
+ *   scales       uint8 [N][K/16] (out, E4M3 bytes)
+ *   tensor_scale fp32 [1]        (out, device)
+ *   workspace    qrr_quantize_nvfp4_workspace_bytes() bytes of scratch
+ * Two kernels on `stream`: a tensor-wide absmax sweep, then the encode sweep
+ * (which reads the absmax from the workspace, no host round trip). */
+size_t qrr_quantize_nvfp4_workspace_bytes(void);
+qrr_status qrr_quantize_nvfp4(const void* W, int64_t N, int64_t K, uint8_t* codes, uint8_t* scales,
+                              float* tensor_scale, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* W4A16 + LoRA linear ("NVIDIA and MIT Collaborate on QeRL", paragraph after
+ * Key Features: NVFP4 weight path, activations/logits in higher precision;
+ * "QeRL: Beyond Efficiency", abstract: NVFP4 with LoRA):
+ *   y = x . W_hat^T + (alpha / r) . (x . A^T) . B^T,  y in bf16
+ *   x            bf16 [M][K], M >= 0, K a multiple of 256
+ *   codes/scales/tensor_scale: an NVFP4 weight [N][K] as qrr_quantize_nvfp4 writes it
+ *   lora_A       bf16 [r][K] or NULL;  lora_B bf16 [N][r] or NULL
+ *   r            LoRA rank, 0..256 and a multiple of 8 when the adapter is on;
+ *                the adapter is off when r == 0 or A or B is NULL
+ *   y            bf16 [M][N] (out); N a multiple of 128
+ *   workspace    qrr_linear_nvfp4_lora_workspace_bytes(M, N, K, r) bytes
+ * Products are formed exactly and summed in fp32; the dequantized weight
+ * e2m1 * e4m3 is exact in bf16.  A decode variant (split-K GEMV) is chosen
+ * for small M and a tensor-core GEMM for large M; both give the same
+ * contract. */
+size_t qrr_linear_nvfp4_lora_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r);
+qrr_status qrr_linear_nvfp4_lora(const void* x, int64_t M, int64_t K, const uint8_t* codes,
+                                 const uint8_t* scales, const float* tensor_scale, int64_t N,
+                                 const void* lora_A, const void* lora_B, int32_t r, float alpha,
+                                 void* y, void* workspace, size_t workspace_bytes,
+                                 int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Blockwise FP8 quantization ("NVIDIA NeMo RL behaalt 48% ...", section "De
+ * technische doorbraak": E4M3, 128x128 tiles for weights, 1x128 for
+ * activations; power-of-two scales optional).
+ * Weights:     W bf16 [N][K] -> q uint8 [N][K], scales fp32 [ceil(N/128)][K/128];
+ *              K a multiple of 128, any N >= 0 (the last tile row may be short).
+ * Activations: x bf16 [M][K] -> q uint8 [M][K], scales fp32 [M][K/128]; K % 128 == 0.
+ * A block whose absmax is 0 gets scale 0 and all-zero codes. */
+qrr_status qrr_quantize_fp8_w128x128(const void* W, int64_t N, int64_t K, uint8_t* q, float* scales,
+                                     int32_t scale_mode, int32_t* dev_status, void* stream);
+qrr_status qrr_quantize_fp8_a1x128(const void* x, int64_t M, int64_t K, uint8_t* q, float* scales,
+                                   int32_t scale_mode, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Blockwise-scaled FP8 GEMM (same section: FP8 linear layers):
+ *   y[m][n] = sum_kb sa[m][kb] * sw[n/128][kb] * sum_{k in kb} qa[m][k] * qw[n][k]
+ *   qa uint8 [M][K], sa fp32 [M][K/128], qw uint8 [N][K], sw fp32 [ceil(N/128)][K/128]
+ *   y  bf16 [M][N] (out); K a multiple of 128, N a multiple of 128.
+ *   scale_mode  QRR_SCALE_POW2 promises that every scale is a power of two
+ *               (or zero); the result is the same either way.
+ * The E4M3 products are exact; each 128-wide block sum is fp32 before the
+ * scales are applied. */
+qrr_status qrr_gemm_fp8_blockwise(const uint8_t* qa, const float* sa, const uint8_t* qw,
+                                  const float* sw, int64_t M, int64_t N, int64_t K, void* y,
+                                  int32_t scale_mode, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Re-quantize every weight after a training step ("NVIDIA NeMo RL behaalt
+ * 48% ...", section "Praktische prestatiewinsten": scales recalibrated after
+ * every step).  Each descriptor is quantized from scratch (current absmax, no
+ * scale history), exactly as the single-tensor calls above would.
+ *   descs   HOST array of `count` descriptors (read during the call only)
+ *   format  QRR_FORMAT_NVFP4: codes/scales/tensor_scale as qrr_quantize_nvfp4
+ *           QRR_FORMAT_FP8_W128: codes = q, scales = fp32 tile scales,
+ *           tensor_scale unused (may be NULL); scale_mode as for FP8
+ *   workspace qrr_requantize_workspace_bytes(count) bytes (NVFP4 only; FP8 needs none)
+ * All descriptors are processed by grouped launches (one absmax sweep and one
+ * encode sweep for NVFP4, one sweep for FP8), not one launch per tensor. */
+typedef struct qrr_weight_desc {
+  const void* W;       /* bf16 [N][K] */
+  int64_t N;
+  int64_t K;
+  uint8_t* codes;      /* NVFP4 codes [N][K/2] or FP8 codes [N][K] */
+  void* scales;        /* NVFP4 uint8 [N][K/16] or FP8 fp32 [ceil(N/128)][K/128] */
+  float* tensor_scale; /* NVFP4 only */
+} qrr_weight_desc;
+
+size_t qrr_requantize_workspace_bytes(int32_t count);
+qrr_status qrr_requantize_weights(const qrr_weight_desc* descs, int32_t count, int32_t format,
+                                  int32_t scale_mode, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Conformance probe: the library's own float32 -> E2M1 / E4M3 rounding
+ * primitive applied to n values (fmt 0 = E2M1 code in the low 4 bits,
+ * fmt 1 = E4M3 byte).  in fp32 [n], out uint8 [n]; n >= 0.  The quantizers
+ * take every rounding decision through this primitive, so a test can compare
+ * it with the format definition value by value. */
+qrr_status qrr_round_probe(const float* in, int64_t n, int32_t fmt, uint8_t* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QRR_H_ */

@@ -1,0 +1,96 @@
+// Device helpers shared by the sm_103a kernels: rounding onto the E2M1 / E4M3
+// grids, exact E4M3 decode, bf16 absmax, and the power-of-two scale rule.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qrr.h"
+
+namespace qrr {
+
+constexpr int kSMs = 152;  // GB300: 2 dies x 76 SMs (grids are sized from the live device count)
+
+// ---- rounding primitives (hardware cvt: round-to-nearest-even, satfinite,
+//      sign kept) ------------------------------------------------------------
+
+// Two fp32 -> one byte of two E2M1 codes; `lo` lands in bits 3..0.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two fp32 -> two E4M3 bytes; `lo` lands in bits 7..0.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Exact value of an E4M3 (FN) byte, from its bit fields.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  float mag = e ? __uint_as_float(((e + 120u) << 23) | (m << 20))  // (1 + m/8) 2^(e-7)
+                : static_cast<float>(m) * 0.001953125f;            // m 2^-9
+  return __uint_as_float(__float_as_uint(mag) | ((b & 0x80u) << 24));
+}
+
+// bf16 bits -> fp32 (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Largest |bf16| bit pattern (sign cleared) of the 8 values in a uint4, as a
+// 15-bit integer: non-negative bf16 order like their bit patterns, so an
+// integer max is the absmax, and >= 0x7F80 means inf/NaN.
+__device__ __forceinline__ uint32_t absmax_bits8(uint4 v) {
+  uint32_t m = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
+  m = __vmaxu2(m, v.z & 0x7FFF7FFFu);
+  m = __vmaxu2(m, v.w & 0x7FFF7FFFu);
+  return max(m & 0xFFFFu, m >> 16);
+}
+
+__device__ __forceinline__ float bf16bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+// ---- FP8 scale rules --------------------------------------------------------
+
+// Power-of-two scale: the smallest 2^e with 2^e >= v (v > 0, finite).
+// Returns e; the scale itself is pow2_from_exp(e).
+__device__ __forceinline__ int pow2_ceil_exp(float v) {
+  const uint32_t bits = __float_as_uint(v);
+  if (bits >= 0x00800000u) {  // normal
+    const int ex = static_cast<int>(bits >> 23) - 127;
+    return ex + ((bits & 0x7FFFFFu) != 0u);
+  }
+  // subnormal: v = m 2^-149, ceil(log2 m) = 32 - clz(m - 1)
+  return -149 + (32 - __clz(static_cast<int>(bits - 1u)));
+}
+
+__device__ __forceinline__ float pow2_from_exp(int e) {  // e in [-149, 127]
+  return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23)
+                   : __uint_as_float(1u << (e + 149));
+}
+
+// x * 2^-e, exact for the magnitudes that reach the E4M3 grid.
+struct Pow2Scaler {
+  float f1, f2;
+  __device__ __forceinline__ explicit Pow2Scaler(int e) {
+    const int ne = -e;  // in [-127, 149]
+    if (ne <= 127) {
+      f1 = __uint_as_float(static_cast<uint32_t>(ne + 127) << 23);
+      f2 = 1.0f;
+    } else {
+      f1 = __uint_as_float(254u << 23);  // 2^127
+      f2 = __uint_as_float(static_cast<uint32_t>(ne - 127 + 127) << 23);
+    }
+  }
+  __device__ __forceinline__ float operator()(float x) const { return __fmul_rn(__fmul_rn(x, f1), f2); }
+};
+
+__device__ __forceinline__ void flag(int32_t* status, int32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+}  // namespace qrr

@@ -1,0 +1,270 @@
+// Quantizers: NVFP4 (tensor absmax sweep + encode sweep), blockwise FP8 for
+// 1x128 activation blocks and 128x128 weight tiles, and the rounding probe.
+//
+// All of them are HBM-streaming kernels.  Each thread moves 16-byte vectors,
+// consecutive threads touch consecutive vectors (coalesced), and grids are a
+// multiple of the SM count with grid-stride loops.  NVFP4 and FP8-weight
+// kernels take a batch of tensors ("jobs") so re-quantizing a whole layer set
+// is two (NVFP4) or one (FP8) launch.
+//
+// NVFP4 layout and rule ("QeRL: Beyond Efficiency", abstract; standard NVFP4
+// layout): s_t = amax/2688, s_b = e4m3(amax_b / (6 s_t)), d_b = e4m3(s_b) s_t,
+// code = e2m1(x / d_b); every step one correctly-rounded fp32 operation.
+// FP8 ("NVIDIA NeMo RL behaalt 48% ...", "De technische doorbraak"): E4M3
+// codes with one scale per 1x128 activation block / 128x128 weight tile,
+// s = amax/448 or the next power of two.
+#include "quant.cuh"
+
+namespace qrr {
+
+// ---------------------------------------------------------------------------
+// NVFP4 pass 1: tensor absmax.  A block's absmax is the max of |bf16| bit
+// patterns; `amax_bits[j]` must be zero before the launch.
+
+__global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __grid_constant__ Nvfp4Batch batch) {
+  const int64_t chunks = batch.total_amax_chunks;
+  for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x) {
+    int j = 0;
+    while (j + 1 < batch.count && batch.job[j + 1].first_amax_chunk <= c) ++j;
+    const Nvfp4Job& job = batch.job[j];
+    const int64_t nvec = job.N * job.K / 8;  // uint4 of 8 bf16
+    const int64_t base = (c - job.first_amax_chunk) * kAmaxChunkVecs;
+    const uint4* src = reinterpret_cast<const uint4*>(job.W);
+    uint32_t m = 0;
+#pragma unroll
+    for (int u = 0; u < kAmaxChunkVecs / 256; ++u) {
+      const int64_t i = base + u * 256 + threadIdx.x;
+      if (i < nvec) m = max(m, absmax_bits8(__ldg(src + i)));
+    }
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((threadIdx.x & 31) == 0 && m) {
+      atomicMax(batch.amax_bits + j, m);
+      if (m >= 0x7F80u) flag(batch.status, QRR_DEV_NONFINITE);
+    }
+  }
+}
+
+// NVFP4 pass 2: encode.  One thread per 16-element block; block b of a tensor
+// is elements [16b, 16b+16) of the flat row-major matrix (K % 16 == 0), its
+// codes are bytes [8b, 8b+8) and its scale is byte b.
+__global__ void __launch_bounds__(256) nvfp4_encode_kernel(const __grid_constant__ Nvfp4Batch batch) {
+  const int64_t chunks = batch.total_encode_chunks;
+  for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x) {
+    int j = 0;
+    while (j + 1 < batch.count && batch.job[j + 1].first_encode_chunk <= c) ++j;
+    const Nvfp4Job& job = batch.job[j];
+    const int64_t nblocks = job.N * job.K / 16;
+    const int64_t b = (c - job.first_encode_chunk) * 256 + threadIdx.x;
+    const float amax_t = bf16bits_to_f32(batch.amax_bits[j]);
+    const float s_t = __fdiv_rn(amax_t, 2688.0f);
+    if (b == 0) *job.tensor_scale = s_t;
+    if (b >= nblocks) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(job.W) + 2 * b;
+    const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+    uint32_t sb = 0;
+    uint2 packed = make_uint2(0u, 0u);
+    if (s_t > 0.0f) {
+      const float amax_b = bf16bits_to_f32(max(absmax_bits8(v0), absmax_bits8(v1)));
+      const float six_st = __fmul_rn(6.0f, s_t);
+      sb = cvt_e4m3x2(__fdiv_rn(amax_b, six_st), 0.0f) & 0xFFu;
+      const float d = __fmul_rn(e4m3_to_f32(sb), s_t);
+      if (d > 0.0f) {
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint32_t out[2] = {0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float q0 = __fdiv_rn(bf16_lo(w[i]), d);
+          const float q1 = __fdiv_rn(bf16_hi(w[i]), d);
+          out[i >> 2] |= cvt_e2m1x2(q0, q1) << (8 * (i & 3));
+        }
+        packed = make_uint2(out[0], out[1]);
+      }
+    }
+    reinterpret_cast<uint2*>(job.codes)[b] = packed;
+    job.scales[b] = static_cast<uint8_t>(sb);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// FP8 activations, 1x128 blocks.  Thread i handles elements [8i, 8i+8) of the
+// flat [M, K] matrix; 16 consecutive threads (a half warp) form one 128-block,
+// whose flat index is also the index of its scale in [M, K/128].
+
+__global__ void __launch_bounds__(256) fp8_a1x128_kernel(const uint16_t* __restrict__ x, int64_t nvec,
+                                                        uint8_t* __restrict__ q, float* __restrict__ scales,
+                                                        int mode, int32_t* status) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  // the loop test is uniform across the warp (its first element), so every
+  // shuffle below has all 32 lanes; nvec is a multiple of 16, so a half warp is
+  // wholly live or wholly past the end
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i - (threadIdx.x & 31) < nvec;
+       i += stride) {
+    const bool live = i < nvec;
+    const uint4 v = live ? __ldg(reinterpret_cast<const uint4*>(x) + i) : make_uint4(0, 0, 0, 0);
+    uint32_t m = absmax_bits8(v);
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (!live) continue;
+    if (m >= 0x7F80u && (threadIdx.x & 15) == 0) flag(status, QRR_DEV_NONFINITE);
+    const float amax = bf16bits_to_f32(m);
+    const float v448 = __fdiv_rn(amax, 448.0f);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[2] = {0u, 0u};
+    float s = 0.0f;
+    if (v448 > 0.0f) {
+      if (mode == QRR_SCALE_FP32) {
+        s = v448;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          out[k >> 1] |= cvt_e4m3x2(__fdiv_rn(bf16_lo(w[k]), s), __fdiv_rn(bf16_hi(w[k]), s)) << (16 * (k & 1));
+      } else {
+        const int e = pow2_ceil_exp(v448);
+        s = pow2_from_exp(e);
+        const Pow2Scaler sc(e);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          out[k >> 1] |= cvt_e4m3x2(sc(bf16_lo(w[k])), sc(bf16_hi(w[k]))) << (16 * (k & 1));
+      }
+    }
+    reinterpret_cast<uint2*>(q)[i] = make_uint2(out[0], out[1]);
+    if ((threadIdx.x & 15) == 0) scales[i >> 4] = s;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// FP8 weights, 128x128 tiles.  One CTA (256 threads) per tile: thread t holds
+// row (u * 16 + t / 16), 16-byte column chunk t % 16, for u = 0..7 (a warp
+// reads two full 256-byte tile rows), so the tile's absmax is reduced in
+// registers, then encoded without re-reading HBM.
+
+__global__ void __launch_bounds__(256) fp8_w128_kernel(const __grid_constant__ Fp8WBatch batch) {
+  __shared__ uint32_t warp_max[8];
+  for (int64_t t = blockIdx.x; t < batch.total_tiles; t += gridDim.x) {
+    int j = 0;
+    while (j + 1 < batch.count && batch.job[j + 1].first_tile <= t) ++j;
+    const Fp8WJob& job = batch.job[j];
+    const int64_t local = t - job.first_tile;
+    const int64_t kt = job.K / 128;
+    const int64_t tr = local / kt, tc = local % kt;
+    const int64_t row0 = tr * 128;
+    const int cchunk = threadIdx.x & 15;
+    uint4 v[8];
+    uint32_t m = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t row = row0 + u * 16 + (threadIdx.x >> 4);
+      if (row < job.N) {
+        v[u] = __ldg(reinterpret_cast<const uint4*>(job.W + row * job.K + tc * 128) + cchunk);
+        m = max(m, absmax_bits8(v[u]));
+      } else {
+        v[u] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = warp_max[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) m = max(m, warp_max[w]);
+    __syncthreads();  // warp_max is reused by the next tile
+    if (m >= 0x7F80u && threadIdx.x == 0) flag(batch.status, QRR_DEV_NONFINITE);
+    const float v448 = __fdiv_rn(bf16bits_to_f32(m), 448.0f);
+    float s = 0.0f;
+    int e = 0;
+    if (v448 > 0.0f) {
+      if (batch.mode == QRR_SCALE_FP32) {
+        s = v448;
+      } else {
+        e = pow2_ceil_exp(v448);
+        s = pow2_from_exp(e);
+      }
+    }
+    if (threadIdx.x == 0) job.scales[tr * kt + tc] = s;
+    const Pow2Scaler sc(e);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t row = row0 + u * 16 + (threadIdx.x >> 4);
+      if (row >= job.N) continue;
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      uint32_t out[2] = {0u, 0u};
+      if (s > 0.0f) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float a = batch.mode == QRR_SCALE_FP32 ? __fdiv_rn(bf16_lo(w[k]), s) : sc(bf16_lo(w[k]));
+          const float b = batch.mode == QRR_SCALE_FP32 ? __fdiv_rn(bf16_hi(w[k]), s) : sc(bf16_hi(w[k]));
+          out[k >> 1] |= cvt_e4m3x2(a, b) << (16 * (k & 1));
+        }
+      }
+      reinterpret_cast<uint2*>(job.q + row * job.K + tc * 128)[cchunk] = make_uint2(out[0], out[1]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Rounding probe: the same cvt primitives the quantizers use.
+__global__ void round_probe_kernel(const float* __restrict__ in, int64_t n, int fmt, uint8_t* __restrict__ out) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float v = in[i];
+    out[i] = static_cast<uint8_t>(fmt == 0 ? (cvt_e2m1x2(v, 0.0f) & 0xFu) : (cvt_e4m3x2(v, 0.0f) & 0xFFu));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers.
+
+int grid_for(int64_t work_units, int per_sm) {
+  int dev = 0, sms = kSMs;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+  return static_cast<int>(work_units < cap ? (work_units > 0 ? work_units : 1) : cap);
+}
+
+cudaError_t launch_nvfp4(Nvfp4Batch& batch, cudaStream_t stream) {
+  int64_t amax_chunks = 0, enc_chunks = 0;
+  for (int j = 0; j < batch.count; ++j) {
+    Nvfp4Job& job = batch.job[j];
+    job.first_amax_chunk = amax_chunks;
+    job.first_encode_chunk = enc_chunks;
+    const int64_t nvec = job.N * job.K / 8;
+    amax_chunks += (nvec + kAmaxChunkVecs - 1) / kAmaxChunkVecs;
+    // every tensor gets at least one encode chunk: block 0's thread writes s_t
+    enc_chunks += std::max<int64_t>(1, (job.N * job.K / 16 + 255) / 256);
+  }
+  batch.total_amax_chunks = amax_chunks;
+  batch.total_encode_chunks = enc_chunks;
+  cudaError_t err = cudaMemsetAsync(batch.amax_bits, 0, sizeof(uint32_t) * batch.count, stream);
+  if (err != cudaSuccess) return err;
+  if (amax_chunks > 0) nvfp4_amax_kernel<<<grid_for(amax_chunks, 8), 256, 0, stream>>>(batch);
+  nvfp4_encode_kernel<<<grid_for(enc_chunks, 8), 256, 0, stream>>>(batch);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_a1x128(const void* x, int64_t M, int64_t K, uint8_t* q, float* scales, int mode,
+                              int32_t* status, cudaStream_t stream) {
+  const int64_t nvec = M * K / 8;
+  if (nvec == 0) return cudaSuccess;
+  fp8_a1x128_kernel<<<grid_for((nvec + 255) / 256, 8), 256, 0, stream>>>(static_cast<const uint16_t*>(x), nvec, q,
+                                                                           scales, mode, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_w128(Fp8WBatch& batch, cudaStream_t stream) {
+  int64_t tiles = 0;
+  for (int j = 0; j < batch.count; ++j) {
+    batch.job[j].first_tile = tiles;
+    tiles += ((batch.job[j].N + 127) / 128) * (batch.job[j].K / 128);
+  }
+  batch.total_tiles = tiles;
+  if (tiles == 0) return cudaSuccess;
+  fp8_w128_kernel<<<grid_for(tiles, 6), 256, 0, stream>>>(batch);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_round_probe(const float* in, int64_t n, int fmt, uint8_t* out, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  round_probe_kernel<<<grid_for((n + 255) / 256, 8), 256, 0, stream>>>(in, n, fmt, out);
+  return cudaGetLastError();
+}
+
+}  // namespace qrr

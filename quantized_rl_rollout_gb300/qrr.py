@@ -1,0 +1,207 @@
+"""Thin ctypes binding of the C ABI in ``include/qrr.h``.
+
+Each Python function has the name of the C entry point without its ``qrr_``
+prefix and only marshals arguments: it checks dtypes and contiguity, allocates
+outputs and workspace with torch when the caller passes none, and hands raw
+device pointers and the current CUDA stream to the library.  Every step of the
+computation runs in the library's kernels; there is no other code path, and a
+missing library is an error.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_qrr.so")
+
+SCALE_FP32 = 0
+SCALE_POW2 = 1
+FORMAT_NVFP4 = 0
+FORMAT_FP8_W128 = 1
+DEV_NONFINITE = 0x1
+
+_c_i64 = ctypes.c_int64
+_c_i32 = ctypes.c_int32
+_c_p = ctypes.c_void_p
+_c_sz = ctypes.c_size_t
+
+
+class WeightDesc(ctypes.Structure):
+    """Mirror of ``qrr_weight_desc``."""
+
+    _fields_ = [("W", _c_p), ("N", _c_i64), ("K", _c_i64), ("codes", _c_p), ("scales", _c_p),
+                ("tensor_scale", _c_p)]
+
+
+# symbol -> (restype, argtypes)
+SIGNATURES = {
+    "qrr_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "qrr_abi_version": (ctypes.c_int, []),
+    "qrr_quantize_nvfp4_workspace_bytes": (_c_sz, []),
+    "qrr_quantize_nvfp4": (ctypes.c_int, [_c_p, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p, _c_p]),
+    "qrr_linear_nvfp4_lora_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_i64, _c_i32]),
+    "qrr_linear_nvfp4_lora": (ctypes.c_int, [_c_p, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_p, _c_i32,
+                                             ctypes.c_float, _c_p, _c_p, _c_sz, _c_p, _c_p]),
+    "qrr_quantize_fp8_w128x128": (ctypes.c_int, [_c_p, _c_i64, _c_i64, _c_p, _c_p, _c_i32, _c_p, _c_p]),
+    "qrr_quantize_fp8_a1x128": (ctypes.c_int, [_c_p, _c_i64, _c_i64, _c_p, _c_p, _c_i32, _c_p, _c_p]),
+    "qrr_gemm_fp8_blockwise": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_i32, _c_p,
+                                              _c_p]),
+    "qrr_requantize_workspace_bytes": (_c_sz, [_c_i32]),
+    "qrr_requantize_weights": (ctypes.c_int, [ctypes.POINTER(WeightDesc), _c_i32, _c_i32, _c_i32, _c_p, _c_sz, _c_p,
+                                              _c_p]),
+    "qrr_round_probe": (ctypes.c_int, [_c_p, _c_i64, _c_i32, _c_p, _c_p]),
+}
+
+_lib = None
+
+
+class QrrError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_name(status)}")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (loaded on first use); raises if it is not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"the CUDA library {LIB_PATH} is not built; run __graft_entry__.build() "
+                               "(there is no CPU fallback)")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def status_name(status: int) -> str:
+    return lib().qrr_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise QrrError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t, dtype, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _workspace(nbytes: int, device):
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------------------
+
+def quantize_nvfp4(W, codes=None, scales=None, tensor_scale=None, workspace=None, dev_status=None, stream=None):
+    """NVFP4 quantization of a bf16 [N, K] weight -> (codes, scales, tensor_scale)."""
+    _need(W, torch.bfloat16, "W")
+    n, k = W.shape
+    dev = W.device
+    codes = torch.empty(n, k // 2, dtype=torch.uint8, device=dev) if codes is None else codes
+    scales = torch.empty(n, k // 16, dtype=torch.uint8, device=dev) if scales is None else scales
+    tensor_scale = torch.empty(1, dtype=torch.float32, device=dev) if tensor_scale is None else tensor_scale
+    ws_bytes = lib().qrr_quantize_nvfp4_workspace_bytes()
+    workspace = _workspace(ws_bytes, dev) if workspace is None else workspace
+    _check(lib().qrr_quantize_nvfp4(_ptr(W), n, k, _ptr(codes), _ptr(scales), _ptr(tensor_scale), _ptr(workspace),
+                                    workspace.numel(), _ptr(dev_status), _stream(stream)), "qrr_quantize_nvfp4")
+    return codes, scales, tensor_scale
+
+
+def linear_nvfp4_lora_workspace_bytes(M, N, K, r) -> int:
+    return int(lib().qrr_linear_nvfp4_lora_workspace_bytes(M, N, K, r))
+
+
+def linear_nvfp4_lora(x, codes, scales, tensor_scale, lora_A=None, lora_B=None, alpha=0.0, y=None, workspace=None,
+                      dev_status=None, stream=None):
+    """y = x . dequant(W)^T + (alpha/r) (x . A^T) . B^T in bf16."""
+    _need(x, torch.bfloat16, "x")
+    m, k = x.shape
+    n = codes.shape[0]
+    r = 0 if lora_A is None or lora_B is None else int(lora_A.shape[0])
+    y = torch.empty(m, n, dtype=torch.bfloat16, device=x.device) if y is None else y
+    if workspace is None:
+        workspace = _workspace(linear_nvfp4_lora_workspace_bytes(m, n, k, r), x.device)
+    _check(lib().qrr_linear_nvfp4_lora(_ptr(x), m, k, _ptr(codes), _ptr(scales), _ptr(tensor_scale), n,
+                                       _ptr(lora_A), _ptr(lora_B), r, float(alpha), _ptr(y), _ptr(workspace),
+                                       workspace.numel(), _ptr(dev_status), _stream(stream)),
+           "qrr_linear_nvfp4_lora")
+    return y
+
+
+def quantize_fp8_w128x128(W, mode=SCALE_FP32, q=None, scales=None, dev_status=None, stream=None):
+    _need(W, torch.bfloat16, "W")
+    n, k = W.shape
+    q = torch.empty(n, k, dtype=torch.uint8, device=W.device) if q is None else q
+    scales = torch.empty((n + 127) // 128, k // 128, dtype=torch.float32, device=W.device) if scales is None else scales
+    _check(lib().qrr_quantize_fp8_w128x128(_ptr(W), n, k, _ptr(q), _ptr(scales), int(mode), _ptr(dev_status),
+                                           _stream(stream)), "qrr_quantize_fp8_w128x128")
+    return q, scales
+
+
+def quantize_fp8_a1x128(x, mode=SCALE_FP32, q=None, scales=None, dev_status=None, stream=None):
+    _need(x, torch.bfloat16, "x")
+    m, k = x.shape
+    q = torch.empty(m, k, dtype=torch.uint8, device=x.device) if q is None else q
+    scales = torch.empty(m, k // 128, dtype=torch.float32, device=x.device) if scales is None else scales
+    _check(lib().qrr_quantize_fp8_a1x128(_ptr(x), m, k, _ptr(q), _ptr(scales), int(mode), _ptr(dev_status),
+                                         _stream(stream)), "qrr_quantize_fp8_a1x128")
+    return q, scales
+
+
+def gemm_fp8_blockwise(qa, sa, qw, sw, mode=SCALE_FP32, y=None, dev_status=None, stream=None):
+    m, k = qa.shape
+    n = qw.shape[0]
+    y = torch.empty(m, n, dtype=torch.bfloat16, device=qa.device) if y is None else y
+    _check(lib().qrr_gemm_fp8_blockwise(_ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), m, n, k, _ptr(y), int(mode),
+                                        _ptr(dev_status), _stream(stream)), "qrr_gemm_fp8_blockwise")
+    return y
+
+
+def requantize_weights(weights, outputs, fmt=FORMAT_NVFP4, mode=SCALE_FP32, workspace=None, dev_status=None,
+                       stream=None):
+    """Re-quantize every bf16 weight of ``weights`` into ``outputs``.
+
+    ``outputs[i]`` is ``(codes, scales, tensor_scale)`` for NVFP4 or
+    ``(q, scales)`` for FP8 128x128.
+    """
+    count = len(weights)
+    descs = (WeightDesc * max(count, 1))()
+    for i, (w, out) in enumerate(zip(weights, outputs)):
+        _need(w, torch.bfloat16, f"weights[{i}]")
+        ts = out[2] if fmt == FORMAT_NVFP4 else None
+        descs[i] = WeightDesc(_ptr(w), w.shape[0], w.shape[1], _ptr(out[0]), _ptr(out[1]), _ptr(ts))
+    dev = weights[0].device if count else torch.device("cuda")
+    if workspace is None:
+        workspace = _workspace(lib().qrr_requantize_workspace_bytes(count), dev)
+    _check(lib().qrr_requantize_weights(descs, count, int(fmt), int(mode), _ptr(workspace), workspace.numel(),
+                                        _ptr(dev_status), _stream(stream)), "qrr_requantize_weights")
+    return outputs
+
+
+def round_probe(values, fmt, out=None, stream=None):
+    _need(values, torch.float32, "values")
+    out = torch.empty(values.numel(), dtype=torch.uint8, device=values.device) if out is None else out
+    _check(lib().qrr_round_probe(_ptr(values), values.numel(), int(fmt), _ptr(out), _stream(stream)),
+           "qrr_round_probe")
+    return out

@@ -1,0 +1,208 @@
+"""GPU parity of the W4A16 + LoRA linear and the blockwise FP8 GEMM against the
+float64 oracle, within the acceptance tolerance (normwise <= 5e-3, per
+element <= 1e-2 (|y| + rms(y))), plus re-quantization of a layer set."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_rl_rollout_gb300 import configs, inputs
+
+from .conftest import to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def q():
+    from quantized_rl_rollout_gb300 import build, qrr
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build.build()
+    qrr.lib()
+    return qrr
+
+
+def _layer(q, n, k, r, tag, outliers=True):
+    W = inputs.weight(n, k, inputs.derive_seed(0, tag, "W"), device=DEV, outlier_frac=1e-3 if outliers else 0.0)
+    codes, scales, ts = q.quantize_nvfp4(W)
+    A, B, alpha = inputs.lora(r, k, n, inputs.derive_seed(0, tag, "lora"), device=DEV) if r else (None, None, 0.0)
+    return W, codes, scales, ts, A, B, alpha
+
+
+def _ref(x, codes, scales, ts, A, B, alpha, rows=None):
+    c = codes.cpu().numpy()
+    s = scales.cpu().numpy()
+    t = np.float32(ts.item())
+    a = None if A is None else to_np(A)
+    b = None if B is None else to_np(B)
+    if rows is None:
+        return oracle.linear.linear_nvfp4_lora(to_np(x), c, s, t, a, b, alpha)
+    w_hat = oracle.nvfp4.dequantize(c[rows], s[rows], t)
+    return oracle.linear.linear_rows(to_np(x), w_hat, a, None if b is None else b[rows], alpha)
+
+
+def _assert_close(y, y_ref, what):
+    ok, nerr, worst = oracle.linear.within_tolerance(to_np(y), y_ref)
+    assert ok, f"{what}: normwise {nerr:.3e}, worst element ratio {worst:.3f}"
+
+
+def test_tiny_config(q):
+    c = configs.TINY
+    W = inputs.weight(c["n"], c["k"], inputs.derive_seed(0, "tiny", "W"), device=DEV)
+    x = inputs.activations(c["m"], c["k"], inputs.derive_seed(0, "tiny", "x"), device=DEV)
+    A, B, _ = inputs.lora(c["r"], c["k"], c["n"], inputs.derive_seed(0, "tiny", "lora"), device=DEV)
+    codes, scales, ts = q.quantize_nvfp4(W)
+    y = q.linear_nvfp4_lora(x, codes, scales, ts, A, B, c["alpha"])
+    torch.cuda.synchronize()
+    _assert_close(y, _ref(x, codes, scales, ts, A, B, c["alpha"]), "tiny")
+
+
+@pytest.mark.parametrize("m", [1, 3, 8, 17, 64, 65, 256])
+@pytest.mark.parametrize("r", [0, 8, 32])
+def test_token_counts_and_ranks(q, m, r):
+    n, k = 384, 1024
+    W, codes, scales, ts, A, B, alpha = _layer(q, n, k, r, f"mr{r}")
+    x = inputs.activations(m, k, inputs.derive_seed(0, "x", m, r), device=DEV)
+    y = q.linear_nvfp4_lora(x, codes, scales, ts, A, B, alpha)
+    torch.cuda.synchronize()
+    _assert_close(y, _ref(x, codes, scales, ts, A, B, alpha), f"m={m} r={r}")
+
+
+def test_closed_forms(q):
+    n, k, r = 256, 512, 16
+    W, codes, scales, ts, A, B, alpha = _layer(q, n, k, r, "closed")
+    x = torch.zeros(5, k, dtype=torch.bfloat16, device=DEV)
+    y = q.linear_nvfp4_lora(x, codes, scales, ts, A, B, alpha)
+    torch.cuda.synchronize()
+    assert not y.float().abs().max().item()
+    # one-hot token -> column k0 of W_hat plus the adapter column
+    k0 = 301
+    x[2, k0] = 1.0
+    y = q.linear_nvfp4_lora(x, codes, scales, ts, A, B, alpha)
+    torch.cuda.synchronize()
+    _assert_close(y, _ref(x, codes, scales, ts, A, B, alpha), "one-hot")
+    # alpha = 0 equals no adapter
+    xr = inputs.activations(9, k, 5, device=DEV)
+    y0 = q.linear_nvfp4_lora(xr, codes, scales, ts, A, B, 0.0)
+    y1 = q.linear_nvfp4_lora(xr, codes, scales, ts, None, None, 0.0)
+    torch.cuda.synchronize()
+    _assert_close(y0, _ref(xr, codes, scales, ts, None, None, 0.0), "alpha=0")
+    _assert_close(y1, _ref(xr, codes, scales, ts, None, None, 0.0), "no adapter")
+    # W = 0 -> adapter term only
+    Z = torch.zeros(n, k, dtype=torch.bfloat16, device=DEV)
+    zc, zs, zt = q.quantize_nvfp4(Z)
+    y = q.linear_nvfp4_lora(xr, zc, zs, zt, A, B, alpha)
+    torch.cuda.synchronize()
+    _assert_close(y, _ref(xr, zc, zs, zt, A, B, alpha), "W=0")
+
+
+def test_empty_tokens(q):
+    W, codes, scales, ts, A, B, alpha = _layer(q, 128, 256, 8, "empty")
+    x = torch.zeros(0, 256, dtype=torch.bfloat16, device=DEV)
+    y = q.linear_nvfp4_lora(x, codes, scales, ts, A, B, alpha)
+    torch.cuda.synchronize()
+    assert y.shape == (0, 128)
+
+
+@pytest.mark.parametrize("m", [1, 8, 64])
+def test_decode_8b_layer_set_sampled(q, m):
+    """Every layer of the 8B-class set at decode sizes; 256 sampled output
+    columns per layer (all tokens) against the oracle."""
+    g = np.random.default_rng(m)
+    r = configs.DECODE_8B["r"]
+    for layer in configs.LAYERS_8B:
+        tag = f"dec8b/{layer.name}"
+        W, codes, scales, ts, A, B, alpha = _layer(q, layer.n, layer.k, r, tag)
+        x = inputs.activations(m, layer.k, inputs.derive_seed(0, tag, "x", m), device=DEV)
+        y = q.linear_nvfp4_lora(x, codes, scales, ts, A, B, alpha)
+        torch.cuda.synchronize()
+        rows = np.unique(np.concatenate([[0, layer.n - 1], g.integers(0, layer.n, 254)]))
+        y_ref = _ref(x, codes, scales, ts, A, B, alpha, rows=rows)
+        _assert_close(y[:, torch.from_numpy(rows).to(DEV)], y_ref, f"{layer.name} m={m}")
+        del W, codes, scales
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_fp8_gemm_small(q, mode):
+    m, n, k = 96, 384, 512
+    x = inputs.activations(m, k, 11, device=DEV, channel_outlier_frac=0.01)
+    W = inputs.weight(n, k, 12, device=DEV)
+    qa, sa = q.quantize_fp8_a1x128(x, mode)
+    qw, sw = q.quantize_fp8_w128x128(W, mode)
+    y = q.gemm_fp8_blockwise(qa, sa, qw, sw, mode)
+    torch.cuda.synchronize()
+    y_ref = oracle.fp8.gemm_blockwise(qa.cpu().numpy(), sa.cpu().numpy(), qw.cpu().numpy(), sw.cpu().numpy())
+    _assert_close(y, y_ref, f"fp8 mode {mode}")
+
+
+def test_fp8_gemm_exact_integers(q):
+    """Small integers with power-of-two scales: the exact result is
+    representable, so the bf16 output must equal its rounding."""
+    m, n, k = 32, 256, 256
+    a = ((torch.arange(m * k, device=DEV).reshape(m, k) % 7) - 3).to(torch.bfloat16)
+    w = ((torch.arange(n * k, device=DEV).reshape(n, k) % 5) - 2).to(torch.bfloat16)
+    qa, sa = q.quantize_fp8_a1x128(a, 1)
+    qw, sw = q.quantize_fp8_w128x128(w, 1)
+    y = q.gemm_fp8_blockwise(qa, sa, qw, sw, 1)
+    torch.cuda.synchronize()
+    y_ref = oracle.fp8.gemm_blockwise(qa.cpu().numpy(), sa.cpu().numpy(), qw.cpu().numpy(), sw.cpu().numpy())
+    assert np.array_equal(to_np(y), oracle.formats.bf16_rne(y_ref))
+
+
+def test_fp8_gemm_8b_sampled(q):
+    """FP8 path on an 8B-class layer at 4096 tokens; 64 sampled token rows."""
+    g = np.random.default_rng(5)
+    layer = configs.LAYERS_8B[4]  # gate 14336 x 4096
+    x = inputs.activations(4096, layer.k, 21, device=DEV, channel_outlier_frac=0.01)
+    W = inputs.weight(layer.n, layer.k, 22, device=DEV)
+    qa, sa = q.quantize_fp8_a1x128(x)
+    qw, sw = q.quantize_fp8_w128x128(W)
+    y = q.gemm_fp8_blockwise(qa, sa, qw, sw)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([[0, 4095], g.integers(0, 4096, 62)]))
+    rt = torch.from_numpy(rows).to(DEV)
+    y_ref = oracle.fp8.gemm_blockwise(qa[rt].cpu().numpy(), sa[rt].cpu().numpy(), qw.cpu().numpy(), sw.cpu().numpy())
+    _assert_close(y[rt], y_ref, "fp8 8B gate")
+
+
+def test_requantize_nvfp4_matches_single_calls(q):
+    shapes = [(512, 256), (1024, 4096), (96, 1024), (128, 32), (0, 64)]
+    Ws = [inputs.weight(n, k, inputs.derive_seed(0, "rq", i), device=DEV) for i, (n, k) in enumerate(shapes)]
+    Wu = [inputs.updated(w, inputs.derive_seed(0, "rq-upd", i)) for i, w in enumerate(Ws)]
+    outs = [(torch.empty(n, k // 2, dtype=torch.uint8, device=DEV), torch.empty(n, k // 16, dtype=torch.uint8, device=DEV),
+             torch.empty(1, dtype=torch.float32, device=DEV)) for n, k in shapes]
+    q.requantize_weights(Wu, outs, q.FORMAT_NVFP4)
+    torch.cuda.synchronize()
+    for w, (c, s, t) in zip(Wu, outs):
+        rc, rs, rt = oracle.nvfp4.quantize(to_np(w))
+        assert t.item() == float(rt)
+        assert np.array_equal(c.cpu().numpy(), rc) and np.array_equal(s.cpu().numpy(), rs)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_requantize_fp8(q, mode):
+    shapes = [(512, 256), (200, 1024), (1024, 128)]
+    Ws = [inputs.updated(inputs.weight(n, k, i, device=DEV), 100 + i) for i, (n, k) in enumerate(shapes)]
+    outs = [(torch.empty(n, k, dtype=torch.uint8, device=DEV),
+             torch.empty((n + 127) // 128, k // 128, dtype=torch.float32, device=DEV)) for n, k in shapes]
+    q.requantize_weights(Ws, outs, q.FORMAT_FP8_W128, mode)
+    torch.cuda.synchronize()
+    for w, (c, s) in zip(Ws, outs):
+        rc, rs = oracle.fp8.quantize_w128x128(to_np(w), mode)
+        assert np.array_equal(s.cpu().numpy(), rs) and np.array_equal(c.cpu().numpy(), rc)
+
+
+def test_requantize_many_tensors_grouping(q):
+    """More descriptors than one grouped launch holds (the library splits them)."""
+    Ws = [inputs.weight(32 + i, 64, 500 + i, device=DEV) for i in range(60)]
+    outs = [(torch.empty(w.shape[0], 32, dtype=torch.uint8, device=DEV),
+             torch.empty(w.shape[0], 4, dtype=torch.uint8, device=DEV),
+             torch.empty(1, dtype=torch.float32, device=DEV)) for w in Ws]
+    q.requantize_weights(Ws, outs, q.FORMAT_NVFP4)
+    torch.cuda.synchronize()
+    for w, (c, s, t) in zip(Ws, outs):
+        rc, rs, rt = oracle.nvfp4.quantize(to_np(w))
+        assert t.item() == float(rt) and np.array_equal(c.cpu().numpy(), rc) and np.array_equal(s.cpu().numpy(), rs)
