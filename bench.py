@@ -364,6 +364,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--phases", default=",".join(PHASES))
+    ap.add_argument("--skip-extras", action="store_true", help="no e2e or CPU-oracle legs (for profiler runs)")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
     rank, world, local, dist = dist_setup(args.gpus)
@@ -468,7 +469,7 @@ def main():
 
     e2e = None
     cpu = None
-    if rank == 0 and any(p.startswith("decode_m") for p in phases):
+    if rank == 0 and not args.skip_extras and any(p.startswith("decode_m") for p in phases):
         e_ms, h2d, d2h = e2e_decode(w, max(3, args.steps))
         e_bytes = sum(decode_bytes(L, m, R) for m in DECODE_TOKENS)
         e2e = {"value": e_bytes / e_ms / 1e6, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -479,7 +480,7 @@ def main():
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
                 "warmup": warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "nvfp4-w/bf16-act/fp32-acc", "data": "synthetic",
+                "vs_baseline": None, "dtype": "nvfp4xbf16", "data": "synthetic",
                 "config": {"workload": WORKLOAD, "phases": phases, "l2": "flushed (512 MB write) before every phase",
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
                 "roofline": roof, "breakdown": breakdown, "cpu_baseline": cpu, "e2e": e2e,

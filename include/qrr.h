@@ -46,7 +46,9 @@
  *    workspace), or QRR_ERR_CUDA when a launch fails.
  *  - `dev_status` (nullable, device int32): conditions found on the device are
  *    OR-ed into it (QRR_DEV_NONFINITE: a non-finite input was seen; the
- *    outputs are then unspecified).  The library never clears it; the caller
+ *    outputs are then unspecified; QRR_DEV_TIMEOUT: a tensor-core pipeline
+ *    wait gave up after its bounded time and the kernel ended early).  The
+ *    library never clears it; the caller
  *    zeroes it and reads it when it chooses.
  */
 #ifndef QRR_H_
@@ -69,7 +71,8 @@ typedef enum qrr_status {
 } qrr_status;
 
 /* Bits OR-ed into the optional device status word. */
-#define QRR_DEV_NONFINITE 0x1
+#define QRR_DEV_NONFINITE 0x1 /* a non-finite input value was seen */
+#define QRR_DEV_TIMEOUT 0x2   /* a pipeline wait gave up after its time limit; outputs unspecified */
 
 typedef enum qrr_scale_mode {
   QRR_SCALE_FP32 = 0, /* s = fp32(amax / 448); codes e4m3_rne(x / s) */

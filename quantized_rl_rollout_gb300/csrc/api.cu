@@ -163,8 +163,8 @@ qrr_status qrr_quantize_fp8_a1x128(const void* x, int64_t M, int64_t K, uint8_t*
 qrr_status qrr_gemm_fp8_blockwise(const uint8_t* qa, const float* sa, const uint8_t* qw, const float* sw, int64_t M,
                                   int64_t N, int64_t K, void* y, int32_t scale_mode, int32_t* dev_status,
                                   void* stream) {
-  (void)dev_status;
   if (M < 0 || N < 0 || K < 0 || !is_fp8_mode(scale_mode)) return QRR_ERR_INVALID_ARG;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return QRR_ERR_UNSUPPORTED_SHAPE;
   if (M * N > 0 && !y) return QRR_ERR_INVALID_ARG;
   if (M * K > 0 && (!qa || !sa)) return QRR_ERR_INVALID_ARG;
   if (N * K > 0 && (!qw || !sw)) return QRR_ERR_INVALID_ARG;
@@ -176,7 +176,7 @@ qrr_status qrr_gemm_fp8_blockwise(const uint8_t* qa, const float* sa, const uint
   cudaStream_t s = as_stream(stream);
   if (K == 0) return from_cuda(cudaMemsetAsync(y, 0, static_cast<size_t>(M * N) * 2, s));
   Fp8GemmArgs a{qa, sa, qw, sw, y, M, N, K};
-  return from_cuda(launch_fp8_gemm_simt(a, s));
+  return from_cuda(launch_fp8_gemm_tc(a, dev_status, s));
 }
 
 qrr_status qrr_requantize_weights(const qrr_weight_desc* descs, int32_t count, int32_t format, int32_t scale_mode,

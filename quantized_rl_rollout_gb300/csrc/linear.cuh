@@ -36,6 +36,6 @@ struct Fp8GemmArgs {
   int64_t M, N, K;
 };
 
-cudaError_t launch_fp8_gemm_simt(const Fp8GemmArgs& a, cudaStream_t stream);
+cudaError_t launch_fp8_gemm_tc(const Fp8GemmArgs& a, int32_t* status, cudaStream_t stream);
 
 }  // namespace qrr
