@@ -180,7 +180,7 @@ class Workload:
         self.f8a = [(torch.empty(PREFILL_TOKENS, l.k, dtype=torch.uint8, device=device),
                      torch.empty(PREFILL_TOKENS, l.k // 128, dtype=torch.float32, device=device)) for l in L]
         self.yf = [torch.empty(PREFILL_TOKENS, l.n, dtype=torch.bfloat16, device=device) for l in L]
-        ws = max(qrr.linear_nvfp4_lora_workspace_bytes(PREFILL_TOKENS, l.n, l.k, R) for l in L)
+        ws = max(qrr.linear_nvfp4_lora_workspace_bytes(m, l.n, l.k, R) for l in L for m in DECODE_TOKENS + (PREFILL_TOKENS,))
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
         self.rq_ws = torch.empty(4096, dtype=torch.uint8, device=device)
         self.flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)

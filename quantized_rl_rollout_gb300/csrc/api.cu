@@ -4,8 +4,11 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "linear.cuh"
 #include "quant.cuh"
+#include "tc.cuh"
 
 using namespace qrr;
 
@@ -29,10 +32,52 @@ inline qrr_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QRR_OK : 
 
 inline bool is_fp8_mode(int32_t m) { return m == QRR_SCALE_FP32 || m == QRR_SCALE_POW2; }
 
-// Linear workspace: t fp32 [M, r] (LoRA down projection).
-size_t linear_ws_bytes(int64_t M, int64_t /*N*/, int64_t /*K*/, int32_t r) {
-  if (M < 0 || r < 0) return 0;
-  return round_up(static_cast<size_t>(M) * static_cast<size_t>(r) * sizeof(float)) + kAlign;
+// How one linear call runs: operand type, token tile, split-K, workspace.
+struct LinPlan {
+  bool f16;
+  int bn, m_tiles, n_tiles, splits, kcps, lora_chunks;
+  size_t t_off, x16_off, p_off, part_off, cnt_off, total;
+};
+
+// Decode (<= 64 tokens) takes the f16 operand path and splits K until there
+// are about two work units per SM, as long as the fp32 partials stay under a
+// few percent of the weight bytes; prefill runs one unit per output tile.
+LinPlan plan_linear(int64_t M, int64_t N, int64_t K, int32_t r) {
+  LinPlan p{};
+  const bool decode = M <= 64;
+  p.f16 = decode;
+  p.bn = w4_bn_for(M);
+  p.n_tiles = static_cast<int>(N / 128);
+  p.m_tiles = static_cast<int>((M + p.bn - 1) / p.bn);
+  p.lora_chunks = r > 0 ? static_cast<int>((2 * r + 63) / 64) : 0;
+  const int kc = static_cast<int>(K / 64);
+  int splits = 1;
+  if (decode && kc >= 8) {
+    const int base = std::max(1, p.n_tiles * p.m_tiles);
+    const int target = (2 * kSMs + base - 1) / base;
+    const int cap = std::max<int>(1, static_cast<int>(0.035 * static_cast<double>(K) / static_cast<double>(std::max<int64_t>(M, 1))));
+    splits = std::max(1, std::min(std::min(target, cap), kc / 4));
+  }
+  p.kcps = ((kc + splits - 1) / splits + 3) / 4 * 4;
+  p.splits = std::max(1, (kc + p.kcps - 1) / std::max(1, p.kcps));
+  size_t off = 0;
+  p.t_off = off;
+  off += round_up(static_cast<size_t>(M) * 64 * p.lora_chunks * 2);
+  p.x16_off = off;
+  if (p.f16) off += round_up(static_cast<size_t>(M) * static_cast<size_t>(K) * 2);
+  p.p_off = off;
+  if (p.f16) off += round_up(static_cast<size_t>(M) * 4);
+  p.part_off = off;
+  if (p.splits > 1) off += round_up(static_cast<size_t>(p.splits) * M * N * 4);
+  p.cnt_off = off;
+  off += round_up(static_cast<size_t>(p.m_tiles) * p.n_tiles * 4);
+  p.total = off + kAlign;
+  return p;
+}
+
+size_t linear_ws_bytes(int64_t M, int64_t N, int64_t K, int32_t r) {
+  if (M < 0 || N < 0 || K < 0 || r < 0) return 0;
+  return plan_linear(M, N, K, r).total;
 }
 
 }  // namespace
@@ -112,27 +157,67 @@ qrr_status qrr_linear_nvfp4_lora(const void* x, int64_t M, int64_t K, const uint
   if (injected_cuda_fault()) return QRR_ERR_CUDA;
   if (M == 0 || N == 0) return QRR_OK;
   cudaStream_t s = as_stream(stream);
-  float* t = static_cast<float*>(workspace);
   if (K == 0) return from_cuda(cudaMemsetAsync(y, 0, static_cast<size_t>(M * N) * 2, s));
-  if (rr > 0) {
-    cudaError_t e = launch_lora_down_simt(x, lora_A, M, K, rr, t, s);
-    if (e != cudaSuccess) return QRR_ERR_CUDA;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return QRR_ERR_UNSUPPORTED_SHAPE;
+  const LinPlan pl = plan_linear(M, N, K, rr);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  __nv_bfloat16* tbuf = reinterpret_cast<__nv_bfloat16*>(ws + pl.t_off);
+  __half* x16 = reinterpret_cast<__half*>(ws + pl.x16_off);
+  int* pexp = reinterpret_cast<int*>(ws + pl.p_off);
+  uint32_t* counters = reinterpret_cast<uint32_t*>(ws + pl.cnt_off);
+  cudaError_t e = cudaSuccess;
+  if (pl.splits > 1) e = cudaMemsetAsync(counters, 0, static_cast<size_t>(pl.m_tiles) * pl.n_tiles * 4, s);
+  if (e != cudaSuccess) return QRR_ERR_CUDA;
+  if (pl.f16 || rr > 0) {
+    PrepArgs pa{};
+    pa.x = static_cast<const uint16_t*>(x);
+    pa.A = static_cast<const uint16_t*>(lora_A);
+    pa.tensor_scale = tensor_scale;
+    pa.x16 = x16;
+    pa.pexp = pexp;
+    pa.t = tbuf;
+    pa.M = M;
+    pa.K = K;
+    pa.r = rr;
+    pa.t_cols = 64 * pl.lora_chunks;
+    pa.lora_scale = rr > 0 ? alpha / static_cast<float>(rr) : 0.0f;
+    pa.status = dev_status;
+    if (launch_lora_prep(pa, pl.f16, s) != cudaSuccess) return QRR_ERR_CUDA;
   }
-  LinearArgs a{};
-  a.x = static_cast<const uint16_t*>(x);
-  a.codes = codes;
-  a.scales = scales;
-  a.tensor_scale = tensor_scale;
-  a.A = static_cast<const uint16_t*>(lora_A);
-  a.B = static_cast<const uint16_t*>(lora_B);
-  a.t = t;
-  a.y = y;
-  a.M = M;
-  a.N = N;
-  a.K = K;
-  a.r = rr;
-  a.lora_scale = rr > 0 ? alpha / static_cast<float>(rr) : 0.0f;
-  return from_cuda(launch_linear_simt(a, s));
+  W4Params p{};
+  p.count = 1;
+  p.status = dev_status;
+  W4Layer& L = p.layer[0];
+  const void* xsrc = pl.f16 ? static_cast<const void*>(x16) : x;
+  const CUtensorMapDataType xt = pl.f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_tmap_2d(&L.tx, xsrc, xt, M, K, K * 2, pl.bn, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&L.tcodes, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, N, K / 2, K / 2, 128, 32,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+    return QRR_ERR_CUDA;
+  if (rr > 0) {
+    if (!make_tmap_2d(&L.tt, tbuf, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, M, 64 * pl.lora_chunks,
+                      64 * pl.lora_chunks * 2, pl.bn, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+      return QRR_ERR_CUDA;
+  } else {
+    L.tt = L.tx;  // never read without an adapter
+  }
+  L.scales = scales;
+  L.tensor_scale = tensor_scale;
+  L.B = static_cast<const uint16_t*>(lora_B);
+  L.pexp = pl.f16 ? pexp : nullptr;
+  L.y = static_cast<__nv_bfloat16*>(y);
+  L.partial = reinterpret_cast<float*>(ws + pl.part_off);
+  L.counters = counters;
+  L.M = static_cast<int>(M);
+  L.N = static_cast<int>(N);
+  L.K = static_cast<int>(K);
+  L.r = rr;
+  L.lora_chunks = pl.lora_chunks;
+  L.n_tiles = pl.n_tiles;
+  L.m_tiles = pl.m_tiles;
+  L.splits = pl.splits;
+  L.kcps = pl.kcps;
+  return from_cuda(launch_w4a16_tc(p, pl.bn, pl.f16, s));
 }
 
 qrr_status qrr_quantize_fp8_w128x128(const void* W, int64_t N, int64_t K, uint8_t* q, float* scales,

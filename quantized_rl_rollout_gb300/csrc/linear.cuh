@@ -2,8 +2,11 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <cuda.h>
 
 #include "common.cuh"
 
@@ -26,6 +29,50 @@ struct LinearArgs {
 cudaError_t launch_lora_down_simt(const void* x, const void* A, int64_t M, int64_t K, int r, float* t,
                                   cudaStream_t stream);
 cudaError_t launch_linear_simt(const LinearArgs& a, cudaStream_t stream);
+
+// ---- tensor-core W4A16 linear (linear_tc.cu) ----
+
+constexpr int kMaxW4Layers = 8;
+
+struct W4Layer {
+  CUtensorMap tx;      // x (bf16) or its f16 image [M, K], box [BN, 64], 128 B swizzle
+  CUtensorMap tcodes;  // packed codes u8 [N, K/2], box [128, 32]
+  CUtensorMap tt;      // LoRA t' bf16 [M, 64 * lora_chunks], box [BN, 64], 128 B swizzle
+  const uint8_t* scales;
+  const float* tensor_scale;
+  const uint16_t* B;  // LoRA B [N, r]
+  const int* pexp;    // per-token power-of-two pre-scale (f16 path) or null
+  __nv_bfloat16* y;
+  float* partial;      // [splits, M, N] when splits > 1
+  uint32_t* counters;  // [m_tiles * n_tiles], zero before the launch
+  int M, N, K, r, lora_chunks;
+  int n_tiles, m_tiles, splits, kcps;  // kcps: 64-wide K chunks per split (multiple of 4)
+  int first_unit;
+};
+
+struct W4Params {
+  W4Layer layer[kMaxW4Layers];
+  int count;
+  int total_units;
+  int32_t* status;
+};
+
+struct PrepArgs {
+  const uint16_t* x;  // bf16 [M, K]
+  const uint16_t* A;  // bf16 [r, K]
+  const float* tensor_scale;
+  __half* x16;          // f16 [M, K] (f16 path)
+  int* pexp;            // [M] (f16 path)
+  __nv_bfloat16* t;     // [M, t_cols]
+  int64_t M, K;
+  int r, t_cols;
+  float lora_scale;
+  int32_t* status;
+};
+
+int w4_bn_for(int64_t M);
+cudaError_t launch_lora_prep(const PrepArgs& a, bool f16, cudaStream_t stream);
+cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, cudaStream_t stream);
 
 struct Fp8GemmArgs {
   const uint8_t* qa;  // [M, K]
