@@ -7,7 +7,8 @@ outliers -- in NVFP4 with LoRA r = 32 (alpha = 64), decoding 1, 8 and 64
 tokens.  One step is one pass of the whole hot path over that layer set:
 
   requant  re-quantize all 7 bf16 weights to NVFP4 (absmax sweep + encode)
-  decode   W4A16 + LoRA linear of all 7 layers at M = 1, 8 and 64
+  decode   W4A16 + LoRA linear of all 7 layers at M = 1, 8 and 64 (one
+           grouped call per token count)
   prefill  the same linears at M = 4096 (activations with 1% x10 channels)
   fp8      FP8 path at M = 4096: activation 1x128 quantize, 128x128 weight
            re-quantize, blockwise-scaled GEMM
@@ -180,7 +181,10 @@ class Workload:
         self.f8a = [(torch.empty(PREFILL_TOKENS, l.k, dtype=torch.uint8, device=device),
                      torch.empty(PREFILL_TOKENS, l.k // 128, dtype=torch.float32, device=device)) for l in L]
         self.yf = [torch.empty(PREFILL_TOKENS, l.n, dtype=torch.bfloat16, device=device) for l in L]
-        ws = max(qrr.linear_nvfp4_lora_workspace_bytes(m, l.n, l.k, R) for l in L for m in DECODE_TOKENS + (PREFILL_TOKENS,))
+        self.gd = {m: self._group(self.xd[m], self.yd[m]) for m in DECODE_TOKENS}
+        self.gp = self._group(self.xp, self.yp)
+        ws = max([qrr.linear_nvfp4_lora_grouped_workspace_bytes(self.gd[m]) for m in DECODE_TOKENS] +
+                 [qrr.linear_nvfp4_lora_grouped_workspace_bytes(self.gp)])
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
         self.rq_ws = torch.empty(4096, dtype=torch.uint8, device=device)
         self.flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
@@ -191,19 +195,22 @@ class Workload:
         self.q.requantize_weights(self.W, self.nv, self.q.FORMAT_NVFP4, workspace=self.rq_ws)
         return 2
 
-    def decode(self, m):
+    def _group(self, xs, ys):
+        out = []
         for i, _ in enumerate(self.layers):
             c, s, t = self.nv[i]
             A, B = self.lora[i]
-            self.q.linear_nvfp4_lora(self.xd[m][i], c, s, t, A, B, ALPHA, y=self.yd[m][i], workspace=self.ws)
-        return 2 * len(self.layers)
+            out.append(dict(x=xs[i], codes=c, scales=s, tensor_scale=t, lora_A=A, lora_B=B, alpha=ALPHA, y=ys[i]))
+        return out
+
+    def decode(self, m):
+        # the whole layer set in one grouped call: LoRA/f16 prologue + one GEMM launch
+        self.q.linear_nvfp4_lora_grouped(self.gd[m], workspace=self.ws)
+        return 2
 
     def prefill(self):
-        for i, _ in enumerate(self.layers):
-            c, s, t = self.nv[i]
-            A, B = self.lora[i]
-            self.q.linear_nvfp4_lora(self.xp[i], c, s, t, A, B, ALPHA, y=self.yp[i], workspace=self.ws)
-        return 2 * len(self.layers)
+        self.q.linear_nvfp4_lora_grouped(self.gp, workspace=self.ws)
+        return 2
 
     def fp8_quant(self):
         self.q.requantize_weights(self.W, self.f8w, self.q.FORMAT_FP8_W128)
@@ -266,13 +273,14 @@ def e2e_decode(w, steps):
     d2h = sum(y.numel() * 2 for m in DECODE_TOKENS for y in hy[m])
     stream = torch.cuda.current_stream()
 
+    groups = {m: w._group(dx[m], w.yd[m]) for m in DECODE_TOKENS}
+
     def one():
         for m in DECODE_TOKENS:
             for i, _ in enumerate(w.layers):
                 dx[m][i].copy_(hx[m][i], non_blocking=True)
-                c, s, t = w.nv[i]
-                A, B = w.lora[i]
-                w.q.linear_nvfp4_lora(dx[m][i], c, s, t, A, B, ALPHA, y=w.yd[m][i], workspace=w.ws)
+            w.q.linear_nvfp4_lora_grouped(groups[m], workspace=w.ws)
+            for i, _ in enumerate(w.layers):
                 hy[m][i].copy_(w.yd[m][i], non_blocking=True)
 
     for _ in range(3):

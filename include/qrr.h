@@ -113,7 +113,7 @@ qrr_status qrr_quantize_nvfp4(const void* W, int64_t N, int64_t K, uint8_t* code
  *   x            bf16 [M][K], M >= 0, K a multiple of 256
  *   codes/scales/tensor_scale: an NVFP4 weight [N][K] as qrr_quantize_nvfp4 writes it
  *   lora_A       bf16 [r][K] or NULL;  lora_B bf16 [N][r] or NULL
- *   r            LoRA rank, 0..256 and a multiple of 8 when the adapter is on;
+ *   r            LoRA rank, 0..64 and a multiple of 8 when the adapter is on;
  *                the adapter is off when r == 0 or A or B is NULL
  *   y            bf16 [M][N] (out); N a multiple of 128
  *   workspace    qrr_linear_nvfp4_lora_workspace_bytes(M, N, K, r) bytes
@@ -127,6 +127,35 @@ qrr_status qrr_linear_nvfp4_lora(const void* x, int64_t M, int64_t K, const uint
                                  const void* lora_A, const void* lora_B, int32_t r, float alpha,
                                  void* y, void* workspace, size_t workspace_bytes,
                                  int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Grouped W4A16 + LoRA linear: up to 8 independent layers that share the
+ * token count M (a decoder layer's q/k/v/o/gate/up/down at one decode step),
+ * run as one prologue launch and one persistent tensor-core launch whose work
+ * units cover every layer, so small layers do not pay their own launch and
+ * pipeline fill.  Each descriptor follows qrr_linear_nvfp4_lora's contract
+ * (x [M][K], y [M][N], same alignment and shape rules); the result is the
+ * same as calling it once per layer.
+ *   descs      HOST array of `count` (1..8) descriptors, read during the call
+ *   workspace  qrr_linear_nvfp4_lora_grouped_workspace_bytes(descs, count, M)
+ * Returns QRR_ERR_UNSUPPORTED_SHAPE when count > 8. */
+typedef struct qrr_linear_desc {
+  const void* x;              /* bf16 [M][K] */
+  int64_t N, K;
+  const uint8_t* codes;       /* [N][K/2] */
+  const uint8_t* scales;      /* [N][K/16] */
+  const float* tensor_scale;  /* device scalar */
+  const void* lora_A;         /* bf16 [r][K] or NULL */
+  const void* lora_B;         /* bf16 [N][r] or NULL */
+  int32_t r;
+  float alpha;
+  void* y;                    /* bf16 [M][N] */
+} qrr_linear_desc;
+
+size_t qrr_linear_nvfp4_lora_grouped_workspace_bytes(const qrr_linear_desc* descs, int32_t count, int64_t M);
+qrr_status qrr_linear_nvfp4_lora_grouped(const qrr_linear_desc* descs, int32_t count, int64_t M,
+                                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                         void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Blockwise FP8 quantization ("NVIDIA NeMo RL behaalt 48% ...", section "De

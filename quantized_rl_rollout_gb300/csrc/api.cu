@@ -10,6 +10,8 @@
 #include "quant.cuh"
 #include "tc.cuh"
 
+#include <cuda_fp16.h>
+
 using namespace qrr;
 
 namespace {
@@ -32,52 +34,211 @@ inline qrr_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QRR_OK : 
 
 inline bool is_fp8_mode(int32_t m) { return m == QRR_SCALE_FP32 || m == QRR_SCALE_POW2; }
 
-// How one linear call runs: operand type, token tile, split-K, workspace.
-struct LinPlan {
-  bool f16;
-  int bn, m_tiles, n_tiles, splits, kcps, lora_chunks;
-  size_t t_off, x16_off, p_off, part_off, cnt_off, total;
+// One layer of a (grouped) linear call, as the caller describes it.
+struct LinIn {
+  const void* x;
+  int64_t N, K;
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const float* tensor_scale;
+  const void* A;
+  const void* B;
+  int32_t r;  // effective rank (0 = no adapter)
+  float alpha;
+  void* y;
 };
 
-// Decode (<= 64 tokens) takes the f16 operand path and splits K until there
-// are about two work units per SM, as long as the fp32 partials stay under a
-// few percent of the weight bytes; prefill runs one unit per output tile.
-LinPlan plan_linear(int64_t M, int64_t N, int64_t K, int32_t r) {
+// How a linear call runs: operand type, token tile, per-layer split-K and the
+// workspace carve-up.  Every layer of a call shares the token count M.
+struct LinPlan {
+  bool f16;
+  int bn, bk, m_tiles, count;
+  struct Layer {
+    int n_tiles, splits, kcps, lora_chunks;
+    size_t t_off, x16_off, p_off, part_off, cnt_off;
+  } l[kMaxW4Layers];
+  size_t cnt_begin, cnt_bytes, total;
+};
+
+// Decode (<= 64 tokens) takes the f16 operand path and splits K; the split
+// length (in pipeline stages) is the one that best fills whole waves of the
+// SMs across all layers of the call, with each layer's fp32 partials capped
+// at about a quarter of its weight bytes.  Prefill runs one unit per tile.
+LinPlan plan_linear(int64_t M, const LinIn* in, int count) {
   LinPlan p{};
   const bool decode = M <= 64;
   p.f16 = decode;
   p.bn = w4_bn_for(M);
-  p.n_tiles = static_cast<int>(N / 128);
+  p.bk = w4_bk_for(M);
   p.m_tiles = static_cast<int>((M + p.bn - 1) / p.bn);
-  p.lora_chunks = r > 0 ? static_cast<int>((2 * r + 63) / 64) : 0;
-  const int kc = static_cast<int>(K / 64);
-  int splits = 1;
-  if (decode && kc >= 8) {
-    const int base = std::max(1, p.n_tiles * p.m_tiles);
-    const int target = (2 * kSMs + base - 1) / base;
-    const int cap = std::max<int>(1, static_cast<int>(0.035 * static_cast<double>(K) / static_cast<double>(std::max<int64_t>(M, 1))));
-    splits = std::max(1, std::min(std::min(target, cap), kc / 4));
+  p.count = count;
+  int kc[kMaxW4Layers], cap[kMaxW4Layers], maxkc = 1;
+  for (int j = 0; j < count; ++j) {
+    p.l[j].n_tiles = static_cast<int>(in[j].N / 128);
+    p.l[j].lora_chunks = in[j].r > 0 ? static_cast<int>((2 * in[j].r + 63) / 64) : 0;
+    kc[j] = std::max(1, static_cast<int>(in[j].K / p.bk));
+    cap[j] = decode ? std::max<int>(1, static_cast<int>(0.035 * static_cast<double>(in[j].K) /
+                                                        static_cast<double>(std::max<int64_t>(M, 1))))
+                    : 1;
+    maxkc = std::max(maxkc, kc[j]);
+    p.l[j].splits = 1;
+    p.l[j].kcps = kc[j];
   }
-  p.kcps = ((kc + splits - 1) / splits + 3) / 4 * 4;
-  p.splits = std::max(1, (kc + p.kcps - 1) / std::max(1, p.kcps));
+  if (decode) {
+    double best = -1.0;
+    for (int ul = maxkc; ul >= 1; --ul) {
+      double work = 0.0;
+      int units = 0, longest = 1;
+      int sp[kMaxW4Layers];
+      for (int j = 0; j < count; ++j) {
+        int s = std::min((kc[j] + ul - 1) / ul, std::min(cap[j], kc[j]));
+        const int kcps = (kc[j] + s - 1) / s;
+        s = (kc[j] + kcps - 1) / kcps;
+        sp[j] = s;
+        const int base = p.l[j].n_tiles * p.m_tiles;
+        units += base * s;
+        work += static_cast<double>(base) * kc[j];
+        longest = std::max(longest, kcps);
+      }
+      const int waves = (units + kSMs - 1) / kSMs;
+      const double eff = work / (static_cast<double>(waves) * kSMs * longest);
+      if (eff > best + 1e-9) {
+        best = eff;
+        for (int j = 0; j < count; ++j) {
+          p.l[j].splits = sp[j];
+          p.l[j].kcps = (kc[j] + sp[j] - 1) / sp[j];
+        }
+      }
+    }
+  }
   size_t off = 0;
-  p.t_off = off;
-  off += round_up(static_cast<size_t>(M) * 64 * p.lora_chunks * 2);
-  p.x16_off = off;
-  if (p.f16) off += round_up(static_cast<size_t>(M) * static_cast<size_t>(K) * 2);
-  p.p_off = off;
-  if (p.f16) off += round_up(static_cast<size_t>(M) * 4);
-  p.part_off = off;
-  if (p.splits > 1) off += round_up(static_cast<size_t>(p.splits) * M * N * 4);
-  p.cnt_off = off;
-  off += round_up(static_cast<size_t>(p.m_tiles) * p.n_tiles * 4);
-  p.total = off + kAlign;
+  for (int j = 0; j < count; ++j) {
+    LinPlan::Layer& L = p.l[j];
+    L.t_off = off;
+    off += round_up(static_cast<size_t>(M) * 64 * L.lora_chunks * 2);
+    L.x16_off = off;
+    if (p.f16) off += round_up(static_cast<size_t>(M) * static_cast<size_t>(in[j].K) * 2);
+    L.p_off = off;
+    if (p.f16) off += round_up(static_cast<size_t>(M) * 4);
+    L.part_off = off;
+    if (L.splits > 1) off += round_up(static_cast<size_t>(L.splits) * M * in[j].N * 4);
+  }
+  p.cnt_begin = off;
+  for (int j = 0; j < count; ++j) {
+    p.l[j].cnt_off = off;
+    off += static_cast<size_t>(p.m_tiles) * p.l[j].n_tiles * 4;
+  }
+  p.cnt_bytes = off - p.cnt_begin;
+  p.total = round_up(off) + kAlign;
   return p;
+}
+
+// Host-side checks shared by the single and grouped linear calls.
+qrr_status check_linear(const LinIn& a, int64_t M, const void* A_in, const void* B_in, int32_t r_in) {
+  if (a.N < 0 || a.K < 0 || r_in < 0) return QRR_ERR_INVALID_ARG;
+  if (!a.tensor_scale) return QRR_ERR_INVALID_ARG;
+  if (M * a.N > 0 && !a.y) return QRR_ERR_INVALID_ARG;
+  if (M * a.K > 0 && !a.x) return QRR_ERR_INVALID_ARG;
+  if (a.N * a.K > 0 && (!a.codes || !a.scales)) return QRR_ERR_INVALID_ARG;
+  if (a.K % 256 != 0 || a.N % 128 != 0) return QRR_ERR_UNSUPPORTED_SHAPE;
+  if (a.N > INT32_MAX || a.K > INT32_MAX) return QRR_ERR_UNSUPPORTED_SHAPE;
+  if (a.r > 0 && (a.r > 64 || a.r % 8 != 0)) return QRR_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(a.x) || !aligned16(a.codes) || !aligned16(a.scales) ||
+      (reinterpret_cast<uintptr_t>(a.tensor_scale) & 3u) || !aligned16(a.y) ||
+      (a.r > 0 && (!aligned16(A_in) || !aligned16(B_in))))
+    return QRR_ERR_MISALIGNED;
+  return QRR_OK;
+}
+
+qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, size_t workspace_bytes,
+                      int32_t* dev_status, cudaStream_t s) {
+  const LinPlan pl = plan_linear(M, in, count);
+  if (!workspace || workspace_bytes < pl.total) return QRR_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return QRR_ERR_MISALIGNED;
+  if (injected_cuda_fault()) return QRR_ERR_CUDA;
+  if (M == 0) return QRR_OK;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // layers with K == 0 produce zeros; layers with N == 0 produce nothing
+  W4Params p{};
+  PrepBatch pb{};
+  p.status = dev_status;
+  bool any_split = false;
+  for (int j = 0; j < count; ++j) {
+    const LinIn& a = in[j];
+    const LinPlan::Layer& pj = pl.l[j];
+    if (a.N == 0) continue;
+    if (a.K == 0) {
+      if (cudaMemsetAsync(a.y, 0, static_cast<size_t>(M * a.N) * 2, s) != cudaSuccess) return QRR_ERR_CUDA;
+      continue;
+    }
+    __nv_bfloat16* tbuf = reinterpret_cast<__nv_bfloat16*>(ws + pj.t_off);
+    __half* x16 = reinterpret_cast<__half*>(ws + pj.x16_off);
+    int* pexp = reinterpret_cast<int*>(ws + pj.p_off);
+    if (pl.f16 || a.r > 0) {
+      PrepArgs& pa = pb.a[pb.count++];
+      pa.x = static_cast<const uint16_t*>(a.x);
+      pa.A = static_cast<const uint16_t*>(a.A);
+      pa.tensor_scale = a.tensor_scale;
+      pa.x16 = x16;
+      pa.pexp = pexp;
+      pa.t = tbuf;
+      pa.M = M;
+      pa.K = a.K;
+      pa.r = a.r;
+      pa.t_cols = 64 * pj.lora_chunks;
+      pa.lora_scale = a.r > 0 ? a.alpha / static_cast<float>(a.r) : 0.0f;
+      pa.status = dev_status;
+    }
+    W4Layer& L = p.layer[p.count++];
+    const void* xsrc = pl.f16 ? static_cast<const void*>(x16) : a.x;
+    const CUtensorMapDataType xt = pl.f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!make_tmap_2d(&L.tx, xsrc, xt, M, a.K, a.K * 2, pl.bn, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d(&L.tcodes, a.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.N, a.K / 2, a.K / 2, 128, pl.bk / 2,
+                      pl.bk == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make_tmap_2d(&L.tscales, a.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.N, a.K / 16, a.K / 16, 128, 16,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+      return QRR_ERR_CUDA;
+    if (a.r > 0) {
+      if (!make_tmap_2d(&L.tt, tbuf, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, M, 64 * pj.lora_chunks,
+                        64 * pj.lora_chunks * 2, pl.bn, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return QRR_ERR_CUDA;
+    } else {
+      L.tt = L.tx;  // never read without an adapter
+    }
+    L.scales = a.scales;
+    L.tensor_scale = a.tensor_scale;
+    L.B = static_cast<const uint16_t*>(a.B);
+    L.pexp = pl.f16 ? pexp : nullptr;
+    L.y = static_cast<__nv_bfloat16*>(a.y);
+    L.partial = reinterpret_cast<float*>(ws + pj.part_off);
+    L.counters = reinterpret_cast<uint32_t*>(ws + pj.cnt_off);
+    L.M = static_cast<int>(M);
+    L.N = static_cast<int>(a.N);
+    L.K = static_cast<int>(a.K);
+    L.r = a.r;
+    L.lora_chunks = pj.lora_chunks;
+    L.n_tiles = pj.n_tiles;
+    L.m_tiles = pl.m_tiles;
+    L.splits = pj.splits;
+    L.kcps = pj.kcps;
+    any_split = any_split || pj.splits > 1;
+  }
+  if (p.count == 0) return QRR_OK;
+  if (any_split && cudaMemsetAsync(ws + pl.cnt_begin, 0, pl.cnt_bytes, s) != cudaSuccess) return QRR_ERR_CUDA;
+  if (pb.count > 0 && launch_lora_prep(pb, pl.f16, s) != cudaSuccess) return QRR_ERR_CUDA;
+  return from_cuda(launch_w4a16_tc(p, pl.bn, pl.f16, s));
+}
+
+LinIn make_in(const void* x, int64_t N, int64_t K, const uint8_t* codes, const uint8_t* scales, const float* ts,
+              const void* A, const void* B, int32_t r, float alpha, void* y) {
+  const bool lora = r > 0 && A && B;
+  return LinIn{x, N, K, codes, scales, ts, A, B, lora ? r : 0, alpha, y};
 }
 
 size_t linear_ws_bytes(int64_t M, int64_t N, int64_t K, int32_t r) {
   if (M < 0 || N < 0 || K < 0 || r < 0) return 0;
-  return plan_linear(M, N, K, r).total;
+  const LinIn in{nullptr, N, K, nullptr, nullptr, nullptr, nullptr, nullptr, r, 0.0f, nullptr};
+  return plan_linear(M, &in, 1).total;
 }
 
 }  // namespace
@@ -139,85 +300,35 @@ qrr_status qrr_linear_nvfp4_lora(const void* x, int64_t M, int64_t K, const uint
                                  const float* tensor_scale, int64_t N, const void* lora_A, const void* lora_B,
                                  int32_t r, float alpha, void* y, void* workspace, size_t workspace_bytes,
                                  int32_t* dev_status, void* stream) {
-  (void)dev_status;
-  if (M < 0 || N < 0 || K < 0 || r < 0) return QRR_ERR_INVALID_ARG;
-  const bool lora = r > 0 && lora_A && lora_B;
-  if (!tensor_scale) return QRR_ERR_INVALID_ARG;
-  if (M * N > 0 && !y) return QRR_ERR_INVALID_ARG;
-  if (M * K > 0 && !x) return QRR_ERR_INVALID_ARG;
-  if (N * K > 0 && (!codes || !scales)) return QRR_ERR_INVALID_ARG;
-  if (K % 256 != 0 || N % 128 != 0) return QRR_ERR_UNSUPPORTED_SHAPE;
-  if (lora && (r > 256 || r % 8 != 0)) return QRR_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned16(x) || !aligned16(codes) || !aligned16(scales) || (reinterpret_cast<uintptr_t>(tensor_scale) & 3u) || !aligned16(y) ||
-      (lora && (!aligned16(lora_A) || !aligned16(lora_B))))
-    return QRR_ERR_MISALIGNED;
-  const int32_t rr = lora ? r : 0;
-  if (!workspace || workspace_bytes < linear_ws_bytes(M, N, K, rr)) return QRR_ERR_WORKSPACE;
-  if (!aligned16(workspace)) return QRR_ERR_MISALIGNED;
-  if (injected_cuda_fault()) return QRR_ERR_CUDA;
-  if (M == 0 || N == 0) return QRR_OK;
-  cudaStream_t s = as_stream(stream);
-  if (K == 0) return from_cuda(cudaMemsetAsync(y, 0, static_cast<size_t>(M * N) * 2, s));
-  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return QRR_ERR_UNSUPPORTED_SHAPE;
-  const LinPlan pl = plan_linear(M, N, K, rr);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  __nv_bfloat16* tbuf = reinterpret_cast<__nv_bfloat16*>(ws + pl.t_off);
-  __half* x16 = reinterpret_cast<__half*>(ws + pl.x16_off);
-  int* pexp = reinterpret_cast<int*>(ws + pl.p_off);
-  uint32_t* counters = reinterpret_cast<uint32_t*>(ws + pl.cnt_off);
-  cudaError_t e = cudaSuccess;
-  if (pl.splits > 1) e = cudaMemsetAsync(counters, 0, static_cast<size_t>(pl.m_tiles) * pl.n_tiles * 4, s);
-  if (e != cudaSuccess) return QRR_ERR_CUDA;
-  if (pl.f16 || rr > 0) {
-    PrepArgs pa{};
-    pa.x = static_cast<const uint16_t*>(x);
-    pa.A = static_cast<const uint16_t*>(lora_A);
-    pa.tensor_scale = tensor_scale;
-    pa.x16 = x16;
-    pa.pexp = pexp;
-    pa.t = tbuf;
-    pa.M = M;
-    pa.K = K;
-    pa.r = rr;
-    pa.t_cols = 64 * pl.lora_chunks;
-    pa.lora_scale = rr > 0 ? alpha / static_cast<float>(rr) : 0.0f;
-    pa.status = dev_status;
-    if (launch_lora_prep(pa, pl.f16, s) != cudaSuccess) return QRR_ERR_CUDA;
+  if (M < 0 || M > INT32_MAX) return M < 0 ? QRR_ERR_INVALID_ARG : QRR_ERR_UNSUPPORTED_SHAPE;
+  const LinIn in = make_in(x, N, K, codes, scales, tensor_scale, lora_A, lora_B, r, alpha, y);
+  qrr_status st = check_linear(in, M, lora_A, lora_B, r);
+  if (st != QRR_OK) return st;
+  return run_linear(&in, 1, M, workspace, workspace_bytes, dev_status, as_stream(stream));
+}
+
+size_t qrr_linear_nvfp4_lora_grouped_workspace_bytes(const qrr_linear_desc* descs, int32_t count, int64_t M) {
+  if (!descs || count <= 0 || count > kMaxW4Layers || M < 0) return 0;
+  LinIn in[kMaxW4Layers];
+  for (int j = 0; j < count; ++j)
+    in[j] = make_in(descs[j].x, descs[j].N, descs[j].K, descs[j].codes, descs[j].scales, descs[j].tensor_scale,
+                    descs[j].lora_A, descs[j].lora_B, descs[j].r, descs[j].alpha, descs[j].y);
+  return plan_linear(M, in, count).total;
+}
+
+qrr_status qrr_linear_nvfp4_lora_grouped(const qrr_linear_desc* descs, int32_t count, int64_t M, void* workspace,
+                                         size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (count < 0 || (count > 0 && !descs) || M < 0) return QRR_ERR_INVALID_ARG;
+  if (count > kMaxW4Layers || M > INT32_MAX) return QRR_ERR_UNSUPPORTED_SHAPE;
+  if (count == 0) return QRR_OK;
+  LinIn in[kMaxW4Layers];
+  for (int j = 0; j < count; ++j) {
+    const qrr_linear_desc& d = descs[j];
+    in[j] = make_in(d.x, d.N, d.K, d.codes, d.scales, d.tensor_scale, d.lora_A, d.lora_B, d.r, d.alpha, d.y);
+    qrr_status st = check_linear(in[j], M, d.lora_A, d.lora_B, d.r);
+    if (st != QRR_OK) return st;
   }
-  W4Params p{};
-  p.count = 1;
-  p.status = dev_status;
-  W4Layer& L = p.layer[0];
-  const void* xsrc = pl.f16 ? static_cast<const void*>(x16) : x;
-  const CUtensorMapDataType xt = pl.f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!make_tmap_2d(&L.tx, xsrc, xt, M, K, K * 2, pl.bn, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_2d(&L.tcodes, codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, N, K / 2, K / 2, 128, 32,
-                    CU_TENSOR_MAP_SWIZZLE_NONE))
-    return QRR_ERR_CUDA;
-  if (rr > 0) {
-    if (!make_tmap_2d(&L.tt, tbuf, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, M, 64 * pl.lora_chunks,
-                      64 * pl.lora_chunks * 2, pl.bn, 64, CU_TENSOR_MAP_SWIZZLE_128B))
-      return QRR_ERR_CUDA;
-  } else {
-    L.tt = L.tx;  // never read without an adapter
-  }
-  L.scales = scales;
-  L.tensor_scale = tensor_scale;
-  L.B = static_cast<const uint16_t*>(lora_B);
-  L.pexp = pl.f16 ? pexp : nullptr;
-  L.y = static_cast<__nv_bfloat16*>(y);
-  L.partial = reinterpret_cast<float*>(ws + pl.part_off);
-  L.counters = counters;
-  L.M = static_cast<int>(M);
-  L.N = static_cast<int>(N);
-  L.K = static_cast<int>(K);
-  L.r = rr;
-  L.lora_chunks = pl.lora_chunks;
-  L.n_tiles = pl.n_tiles;
-  L.m_tiles = pl.m_tiles;
-  L.splits = pl.splits;
-  L.kcps = pl.kcps;
-  return from_cuda(launch_w4a16_tc(p, pl.bn, pl.f16, s));
+  return run_linear(in, count, M, workspace, workspace_bytes, dev_status, as_stream(stream));
 }
 
 qrr_status qrr_quantize_fp8_w128x128(const void* W, int64_t N, int64_t K, uint8_t* q, float* scales,

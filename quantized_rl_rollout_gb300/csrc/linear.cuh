@@ -38,15 +38,16 @@ struct W4Layer {
   CUtensorMap tx;      // x (bf16) or its f16 image [M, K], box [BN, 64], 128 B swizzle
   CUtensorMap tcodes;  // packed codes u8 [N, K/2], box [128, 32]
   CUtensorMap tt;      // LoRA t' bf16 [M, 64 * lora_chunks], box [BN, 64], 128 B swizzle
+  CUtensorMap tscales;  // block scales u8 [N, K/16], box [128, 16] (256-wide K stages)
   const uint8_t* scales;
   const float* tensor_scale;
-  const uint16_t* B;  // LoRA B [N, r]
+  const uint16_t* B;  // LoRA B [N, r], r <= 64
   const int* pexp;    // per-token power-of-two pre-scale (f16 path) or null
   __nv_bfloat16* y;
   float* partial;      // [splits, M, N] when splits > 1
   uint32_t* counters;  // [m_tiles * n_tiles], zero before the launch
   int M, N, K, r, lora_chunks;
-  int n_tiles, m_tiles, splits, kcps;  // kcps: 64-wide K chunks per split (multiple of 4)
+  int n_tiles, m_tiles, splits, kcps;  // kcps: pipeline stages (BK-wide K slices) per split
   int first_unit;
 };
 
@@ -70,8 +71,14 @@ struct PrepArgs {
   int32_t* status;
 };
 
+struct PrepBatch {
+  PrepArgs a[kMaxW4Layers];
+  int count;
+};
+
 int w4_bn_for(int64_t M);
-cudaError_t launch_lora_prep(const PrepArgs& a, bool f16, cudaStream_t stream);
+int w4_bk_for(int64_t M);
+cudaError_t launch_lora_prep(const PrepBatch& b, bool f16, cudaStream_t stream);
 cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, cudaStream_t stream);
 
 struct Fp8GemmArgs {

@@ -14,32 +14,38 @@
 // bf16 and in f16, so the tensor core forms every product exactly and sums in
 // fp32; s_t is applied once in the epilogue.
 //
-//   warp 0      TMA: per 64-wide K chunk, x [BN x 64] (128 B swizzle) and the
-//               packed codes [128 x 32 B] into an S-stage ring
-//   warp 1      MMA: 4 x tcgen05.mma (M128 x BN x K16) per chunk, A from TMEM
-//   warps 2..5  dequant: thread = weight row (its TMEM lane); codes from
-//               shared memory, E4M3 block scales from global, 64 values per
-//               chunk stored to a 4-stage TMEM ring; then the epilogue
+//   warp 0      TMA: per BK-wide K stage, x [BN x BK] (128 B swizzle, in
+//               64-wide sub-tiles), the packed codes [128 x BK/2 B] and, for
+//               BK = 256, the block scales [128 x 16 B] into an S-stage ring
+//   warp 1      MMA: BK/16 x tcgen05.mma (M128 x BN x K16) per stage, A from TMEM
+//   warps 2..5  epilogue: D out of TMEM (double-buffered when it fits), scale,
+//               store y or a split-K partial
+//   warps 6..   G dequant warpgroups taking the stages in turn: thread = weight
+//               row (its TMEM lane); codes and scales from shared memory, BK
+//               values per stage stored to a TMEM ring of A stages
 //
 // LoRA is folded into the same accumulator as extra K columns: the prologue
 // writes t' = (alpha/r) t / (g 2^p) (t = x . A^T, g = s_t or 1, 2^p the
-// per-token pre-scale below) split into a bf16 high part and a bf16 low part;
-// the extra A columns hold [B | B].  So y = g 2^p D with no separate pass.
+// per-token pre-scale below) as interleaved bf16 (high, low) pairs; the
+// matching A columns hold (B_j, B_j).  So y = g 2^p D with no separate pass.
 //
 // Operand type.  Prefill (many tokens) feeds bf16 x directly and dequantizes
 // to bf16.  Decode (<= 64 tokens, HBM-bound) feeds f16: the prologue rescales
 // each token row by a power of two 2^-p (max |x| into [2^14, 2^15)) and
 // rounds it to f16, which is exact for every element within 2^-29 of the
-// row's largest magnitude; the weight dequantizes to f16 with one hardware
-// conversion and one packed multiply per two values, half the cost of the
-// bf16 route.  The LoRA chunks stay bf16 (their own instruction descriptor).
+// row's largest magnitude; the weight then dequantizes with one hardware
+// E2M1->f16x2 conversion and one packed multiply per two values.  The LoRA
+// stages stay bf16 (their own instruction descriptor).
 //
 // Split-K (decode): units of (layer, 128-row tile, token tile, K range); each
 // split writes an fp32 partial, and the last split to finish (a counter per
 // tile) sums the partials in split order and writes y, so the result does not
 // depend on timing.
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "linear.cuh"
 #include "tc.cuh"
@@ -48,25 +54,37 @@ namespace qrr {
 
 namespace {
 
-constexpr int kBK = 64;     // K per chunk (one 128-byte bf16/f16 row of x)
-constexpr int kAStages = 4;  // TMEM A ring
-constexpr int kThreads = 192;
-
-template <int BN>
+template <int BN, int BK, int G>
 struct Cfg {
-  static constexpr int X_BYTES = BN * 128;
-  static constexpr int C_BYTES = 128 * 32;
-  static constexpr int STAGE = X_BYTES + C_BYTES;
-  static constexpr int STAGES = (200 * 1024) / STAGE > 16 ? 16 : (200 * 1024) / STAGE;
-  static constexpr int A_COL = BN < 32 ? 32 : BN;
-  static constexpr uint32_t TMEM_COLS = (A_COL + 32 * kAStages) <= 256 ? 256 : 512;
-  static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE + 512;
+  static constexpr int KSUB = BK / 64;     // 64-wide sub-chunks per stage
+  static constexpr int X_SUB = BN * 128;   // one [BN x 64] 128-byte-swizzled sub-tile
+  static constexpr int X_BYTES = KSUB * X_SUB;
+  static constexpr int C_ROW = BK / 2;     // packed code bytes per weight row per stage
+  static constexpr int C_BYTES = 128 * C_ROW;
+  static constexpr bool SC_TMA = BK >= 256;  // block scales staged by TMA (16 B per row)
+  static constexpr int S_BYTES = SC_TMA ? 128 * (BK / 16) : 0;
+  static constexpr int STAGE = X_BYTES + C_BYTES + S_BYTES;
+  static constexpr int STAGES_RAW = (200 * 1024) / STAGE;
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int DBUF = BN <= 128 ? 2 : 1;  // accumulator buffers in TMEM
+  static constexpr int D_COLS = BN < 32 ? 32 : BN;
+  static constexpr int A_COL = DBUF * D_COLS;
+  static constexpr int A_STAGE_COLS = BK / 2;
+  static constexpr int AST_RAW = (512 - A_COL) / A_STAGE_COLS;
+  static constexpr int AST = (AST_RAW > 8 ? 8 : AST_RAW) / G * G;
+  static constexpr int THREADS = 32 * (2 + 4 + 4 * G);
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE + 1024;
+  static_assert(STAGES >= 2, "shared memory ring too small");
+  static_assert(AST >= G, "TMEM ring too small");
+  static_assert(A_COL + AST * A_STAGE_COLS <= 512, "TMEM overflow");
 };
 
 struct SharedCtl {
-  uint64_t full[16], empty[16];
-  uint64_t a_full[kAStages], a_empty[kAStages];
-  uint64_t d_full, d_empty, done;
+  uint64_t full[8], empty[8];
+  uint64_t a_full[8], a_empty[8];
+  uint64_t d_full[2], d_empty[2];
+  uint64_t done;
   uint32_t tmem;
   int abort;
   int last;
@@ -75,6 +93,13 @@ struct SharedCtl {
 __device__ __forceinline__ uint32_t f16x2_from_e2m1x2(uint32_t byte) {
   uint32_t r;
   asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(r) : "r"(byte));
+  return r;
+}
+
+// Two E4M3 bytes (low 16 bits) -> f16x2, exactly (every E4M3 value is an f16).
+__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t two) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 b;\n\tcvt.u16.u32 b, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, b;\n\t}" : "=r"(r) : "r"(two));
   return r;
 }
 
@@ -93,57 +118,73 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float f16_lo_to_f32(uint32_t h2) { return __half2float(__ushort_as_half(h2 & 0xFFFFu)); }
 __device__ __forceinline__ float f16_hi_to_f32(uint32_t h2) { return __half2float(__ushort_as_half(h2 >> 16)); }
 
-// 64 codes (8 words) + 4 block scales -> 32 words of the MMA A operand.
+// 64 codes (8 words) + their 4 block scales (one word) -> 32 words of A.
 template <bool F16>
-__device__ __forceinline__ void dequant64(const uint32_t (&w)[8], uint32_t scales4, uint32_t (&out)[32]) {
+__device__ __forceinline__ void dequant64(const uint32_t* w, uint32_t scales4, uint32_t* out) {
+  if constexpr (F16) {
+    const uint32_t s01 = f16x2_from_e4m3x2(scales4 & 0xFFFFu), s23 = f16x2_from_e4m3x2(scales4 >> 16);
+    const uint32_t sg[4] = {__byte_perm(s01, 0, 0x1010), __byte_perm(s01, 0, 0x3232), __byte_perm(s23, 0, 0x1010),
+                            __byte_perm(s23, 0, 0x3232)};
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    const float sv = e4m3_to_f32((scales4 >> (8 * g)) & 0xFFu);
-    if constexpr (F16) {
-      const uint32_t s16 = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(sv)));  // exact
-      const uint32_t s2 = s16 | (s16 << 16);
+    for (int g = 0; g < 4; ++g)
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const uint32_t word = w[2 * g + q];
+      for (int q = 0; q < 2; ++q)
 #pragma unroll
-        for (int b = 0; b < 4; ++b) out[8 * g + 4 * q + b] = hmul2(f16x2_from_e2m1x2(word >> (8 * b)), s2);
-      }
-    } else {
+        for (int b = 0; b < 4; ++b)
+          out[8 * g + 4 * q + b] = hmul2(f16x2_from_e2m1x2(w[2 * g + q] >> (8 * b)), sg[g]);
+  } else {
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const uint32_t word = w[2 * g + q];
+    for (int g = 0; g < 4; ++g) {
+      const float sv = e4m3_to_f32((scales4 >> (8 * g)) & 0xFFu);
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          const uint32_t h2 = f16x2_from_e2m1x2(word >> (8 * b));
+          const uint32_t h2 = f16x2_from_e2m1x2(w[2 * g + q] >> (8 * b));
           out[8 * g + 4 * q + b] = pack_bf16x2(f16_lo_to_f32(h2) * sv, f16_hi_to_f32(h2) * sv);
         }
-      }
     }
   }
 }
 
+// ring position: index in [0, R) and the number of completed wraps
+struct Ring {
+  int idx = 0;
+  uint32_t use = 0;
+  template <int R>
+  __device__ __forceinline__ void next() {
+    if (++idx == R) {
+      idx = 0;
+      ++use;
+    }
+  }
+};
+
 }  // namespace
 
-template <int BN, bool F16>
-__global__ void __launch_bounds__(kThreads, 1) w4a16_tc_kernel(const __grid_constant__ W4Params p) {
-  using C = Cfg<BN>;
+template <int BN, int BK, bool F16, int G>
+__global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(const __grid_constant__ W4Params p) {
+  using C = Cfg<BN, BK, G>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   SharedCtl& sh = *reinterpret_cast<SharedCtl*>(tiles + C::STAGES * C::STAGE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &sh.abort;
+  constexpr int KSUB = C::KSUB;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], 5);  // MMA commit + 4 dequant warps
+      mbar_init(&sh.empty[s], 5);  // MMA commit + the 4 warps of one dequant group
     }
-    for (int s = 0; s < kAStages; ++s) {
+    for (int s = 0; s < C::AST; ++s) {
       mbar_init(&sh.a_full[s], 4);
       mbar_init(&sh.a_empty[s], 1);
     }
-    mbar_init(&sh.d_full, 1);
-    mbar_init(&sh.d_empty, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh.d_full[b], 1);
+      mbar_init(&sh.d_empty[b], 4);
+    }
     mbar_init(&sh.done, 1);
     sh.abort = 0;
     fence_barrier_init();
@@ -154,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_tc_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = sh.tmem;
 
-  // unit -> (layer, n tile, m tile, split, chunk range)
+  // unit -> (layer, n tile, m tile, split, stage range, LoRA stages)
   auto locate = [&](int u, int& j, int& nt, int& mt, int& sp, int& c0, int& nk, int& nl) {
     j = 0;
     while (j + 1 < p.count && p.layer[j + 1].first_unit <= u) ++j;
@@ -165,167 +206,122 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_tc_kernel(const __grid_cons
     mt = rest % L.m_tiles;
     sp = rest / L.m_tiles;
     c0 = sp * L.kcps;
-    const int kc = L.K / kBK;
+    const int kc = L.K / BK;
     nk = min(c0 + L.kcps, kc) - c0;
-    nl = (L.r > 0 && sp == L.splits - 1) ? L.lora_chunks : 0;
+    nl = (L.r > 0 && sp == L.splits - 1) ? (L.lora_chunks + KSUB - 1) / KSUB : 0;
   };
 
   if (warp == 0) {
     // ------------------------------ TMA ------------------------------
     if (elect_one()) {
-      uint32_t it = 0;
+      Ring st;
+      uint32_t issued = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
         int j, nt, mt, sp, c0, nk, nl;
         locate(u, j, nt, mt, sp, c0, nk, nl);
         const W4Layer& L = p.layer[j];
-        for (int c = 0; c < nk + nl; ++c, ++it) {
-          const int s = it % C::STAGES;
-          const uint32_t use = it / C::STAGES;
-          if (use > 0 && !mbar_wait(&sh.empty[s], (use - 1) & 1, abort, p.status)) {
+        for (int c = 0; c < nk + nl; ++c, st.next<C::STAGES>(), ++issued) {
+          if (st.use > 0 && !mbar_wait(&sh.empty[st.idx], (st.use - 1) & 1, abort, p.status)) {
             ok = false;
             break;
           }
-          uint8_t* xs = tiles + s * C::STAGE;
+          uint8_t* xs = tiles + st.idx * C::STAGE;
+          uint64_t* fb = &sh.full[st.idx];
           if (c < nk) {
-            mbar_arrive_expect_tx(&sh.full[s], C::X_BYTES + C::C_BYTES);
-            tma_load_2d(&L.tx, &sh.full[s], xs, (c0 + c) * kBK, mt * BN);
-            tma_load_2d(&L.tcodes, &sh.full[s], xs + C::X_BYTES, (c0 + c) * (kBK / 2), nt * 128);
+            const int kb = (c0 + c) * BK;
+            mbar_arrive_expect_tx(fb, C::STAGE);
+#pragma unroll
+            for (int q = 0; q < KSUB; ++q) tma_load_2d(&L.tx, fb, xs + q * C::X_SUB, kb + 64 * q, mt * BN);
+            tma_load_2d(&L.tcodes, fb, xs + C::X_BYTES, kb / 2, nt * 128);
+            if constexpr (C::SC_TMA) tma_load_2d(&L.tscales, fb, xs + C::X_BYTES + C::C_BYTES, kb / 16, nt * 128);
           } else {
-            mbar_arrive_expect_tx(&sh.full[s], C::X_BYTES);
-            tma_load_2d(&L.tt, &sh.full[s], xs, (c - nk) * kBK, mt * BN);
+            // LoRA stage: t' sub-tiles past the tensor's width read as zeros
+            const int lsub = (c - nk) * KSUB;
+            mbar_arrive_expect_tx(fb, C::X_BYTES);
+#pragma unroll
+            for (int q = 0; q < KSUB; ++q) tma_load_2d(&L.tt, fb, xs + q * C::X_SUB, (lsub + q) * 64, mt * BN);
           }
         }
       }
-      // drain: the last load of every stage has landed
+      // drain: the last load of every stage has landed before the CTA exits
       volatile int no_abort = 0;
-      for (uint32_t k = 0; k < static_cast<uint32_t>(C::STAGES) && k < it; ++k) {
-        const uint32_t i = it - 1 - k;
+      for (uint32_t k = 0; k < static_cast<uint32_t>(C::STAGES) && k < issued; ++k) {
+        const uint32_t i = issued - 1 - k;
         mbar_wait(&sh.full[i % C::STAGES], (i / C::STAGES) & 1, &no_abort, p.status);
       }
     }
   } else if (warp == 1) {
     // ------------------------------ MMA ------------------------------
+    // A stage sa is ready only after its dequant group saw the stage's TMA
+    // data land (it waits on `full` first), so this thread waits on a_full alone.
     if (elect_one()) {
       constexpr uint32_t id_main = make_idesc(F16 ? kFmtF16 : kFmtBF16, F16 ? kFmtF16 : kFmtBF16, 128, BN);
       constexpr uint32_t id_lora = make_idesc(kFmtBF16, kFmtBF16, 128, BN);
-      uint32_t it = 0, units = 0;
+      Ring st, at;
+      uint32_t units = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x, ++units) {
         int j, nt, mt, sp, c0, nk, nl;
         locate(u, j, nt, mt, sp, c0, nk, nl);
-        if (units > 0 && !mbar_wait(&sh.d_empty, (units - 1) & 1, abort, p.status)) break;
-        for (int c = 0; c < nk + nl; ++c, ++it) {
-          const int s = it % C::STAGES;
-          const int sa = it % kAStages;
-          if (!mbar_wait(&sh.full[s], (it / C::STAGES) & 1, abort, p.status) ||
-              !mbar_wait(&sh.a_full[sa], (it / kAStages) & 1, abort, p.status)) {
+        const int db = units % C::DBUF;
+        const uint32_t duse = units / C::DBUF;
+        if (duse > 0 && !mbar_wait(&sh.d_empty[db], (duse - 1) & 1, abort, p.status)) break;
+        const uint32_t dcol = tmem + db * C::D_COLS;
+        for (int c = 0; c < nk + nl; ++c, st.next<C::STAGES>(), at.next<C::AST>()) {
+          if (!mbar_wait(&sh.a_full[at.idx], at.use & 1, abort, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t xb = smem_u32(tiles + s * C::STAGE);
-          const uint32_t a0 = tmem + C::A_COL + 32 * sa;
+          const uint32_t xb = smem_u32(tiles + st.idx * C::STAGE);
+          const uint32_t a0 = tmem + C::A_COL + C::A_STAGE_COLS * at.idx;
           const uint32_t idesc = c < nk ? id_main : id_lora;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            mma_bf16_ts(tmem, a0 + 8 * k, sw128_desc(xb + 32 * k), idesc, (c > 0 || k > 0) ? 1u : 0u);
-          mma_commit(&sh.empty[s]);
-          mma_commit(&sh.a_empty[sa]);
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16_ts(dcol, a0 + 8 * k, sw128_desc(xb + (k >> 2) * C::X_SUB + 32 * (k & 3)), idesc,
+                        (c > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&sh.empty[st.idx]);
+          mma_commit(&sh.a_empty[at.idx]);
         }
         if (!ok) break;
-        mma_commit(&sh.d_full);
+        mma_commit(&sh.d_full[db]);
       }
       mma_commit(&sh.done);
       volatile int no_abort = 0;
       mbar_wait(&sh.done, 0, &no_abort, p.status);
     }
-  } else {
-    // ------------------------- dequant + epilogue -------------------------
+  } else if (warp < 6) {
+    // ------------------------------ epilogue ------------------------------
     const int q = warp & 3;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
-    uint32_t it = 0, units = 0;
+    uint32_t units = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x, ++units) {
       int j, nt, mt, sp, c0, nk, nl;
       locate(u, j, nt, mt, sp, c0, nk, nl);
       const W4Layer& L = p.layer[j];
       const int n = nt * 128 + 32 * q + lane;
-      const uint8_t* srow = L.scales + static_cast<int64_t>(n) * (L.K / 16);
-      uint4 sc = make_uint4(0, 0, 0, 0);
-      bool ok = true;
-      for (int c = 0; c < nk + nl; ++c, ++it) {
-        const int s = it % C::STAGES;
-        const int sa = it % kAStages;
-        uint32_t out[32];
-        if (c < nk) {
-          const int kc = c0 + c;
-          if ((c & 3) == 0 || c == 0) sc = __ldg(reinterpret_cast<const uint4*>(srow + (kc & ~3) * 4));
-          if (!mbar_wait(&sh.full[s], (it / C::STAGES) & 1, abort, p.status)) {
-            ok = false;
-            break;
-          }
-          const uint4* crow = reinterpret_cast<const uint4*>(tiles + s * C::STAGE + C::X_BYTES + (32 * q + lane) * 32);
-          // the two 16-byte halves are read in lane-dependent order to spread banks
-          const int h = (lane >> 2) & 1;
-          const uint4 c0v = crow[h], c1v = crow[h ^ 1];
-          const uint4 lo = h ? c1v : c0v, hi = h ? c0v : c1v;
-          const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-          const uint32_t sw[4] = {sc.x, sc.y, sc.z, sc.w};
-          dequant64<F16>(w, sw[kc & 3], out);
-        } else {
-          // LoRA chunk: A columns hold [B | B] (bf16), zero past 2r.  The wait
-          // on the stage keeps this warp's arrivals on `empty` in phase order.
-          if (!mbar_wait(&sh.full[s], (it / C::STAGES) & 1, abort, p.status)) {
-            ok = false;
-            break;
-          }
-          const int lc = c - nk;
-          const uint16_t* brow = L.B + static_cast<int64_t>(n) * L.r;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int j0 = lc * kBK + 2 * i;
-            const uint32_t b0 = j0 < 2 * L.r ? __ldg(brow + (j0 % L.r)) : 0u;
-            const uint32_t b1 = j0 + 1 < 2 * L.r ? __ldg(brow + ((j0 + 1) % L.r)) : 0u;
-            out[i] = b0 | (b1 << 16);
-          }
-        }
-        if (it >= kAStages && !mbar_wait(&sh.a_empty[sa], ((it / kAStages) - 1) & 1, abort, p.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        tmem_st32(tmem + lane_addr + C::A_COL + 32 * sa, out);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&sh.a_full[sa]);
-          mbar_arrive(&sh.empty[s]);
-        }
-      }
-      if (!ok) break;
-      // ------------------------------ epilogue ------------------------------
-      if (!mbar_wait(&sh.d_full, units & 1, abort, p.status)) break;
+      const int db = units % C::DBUF;
+      if (!mbar_wait(&sh.d_full[db], (units / C::DBUF) & 1, abort, p.status)) break;
       tc_fence_after();
       const float st = *L.tensor_scale;
       const float g = st > 0.0f ? st : 1.0f;
       const int m0 = mt * BN;
       float* part = L.splits > 1 ? L.partial + static_cast<int64_t>(sp) * L.M * L.N : nullptr;
-      // stream D out of TMEM 16 or 32 columns (tokens) at a time
       constexpr int CW = BN == 16 ? 16 : 32;
 #pragma unroll 1
       for (int cc = 0; cc < BN / CW; ++cc) {
         uint32_t r[CW];
         if constexpr (CW == 16)
-          tmem_ld16(tmem + lane_addr, r);
+          tmem_ld16(tmem + lane_addr + db * C::D_COLS, r);
         else
-          tmem_ld32(tmem + lane_addr + 32 * cc, r);
+          tmem_ld32(tmem + lane_addr + db * C::D_COLS + 32 * cc, r);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < CW; ++i) {
           const int m = m0 + CW * cc + i;
           if (m < L.M) {
-            const float sc2 = L.pexp ? __fmul_rn(g, ldexpf(1.0f, L.pexp[m])) : g;
+            const float sc2 = L.pexp ? __fmul_rn(g, pow2_from_exp(L.pexp[m])) : g;
             const float v = __uint_as_float(r[i]) * sc2;
             if (part)
               part[static_cast<int64_t>(m) * L.N + n] = v;
@@ -336,8 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_tc_kernel(const __grid_cons
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.d_empty);
-
+      if (lane == 0) mbar_arrive(&sh.d_empty[db]);
       if (part) {
         __threadfence();
         named_bar(1, 128);
@@ -350,16 +345,119 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_tc_kernel(const __grid_cons
         named_bar(1, 128);
         if (sh.last) {
           __threadfence();
-          for (int i = 0; i < BN; ++i) {
-            const int m = m0 + i;
-            if (m >= L.M) break;
-            float sum = 0.0f;
-            for (int s2 = 0; s2 < L.splits; ++s2)
-              sum += __ldcg(L.partial + (static_cast<int64_t>(s2) * L.M + m) * L.N + n);
-            L.y[static_cast<int64_t>(m) * L.N + n] = __float2bfloat16_rn(sum);
+          // sum the splits in fixed order, 16 tokens at a time
+          for (int i0 = 0; i0 < BN; i0 += 16) {
+            float sum[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sum[i] = 0.0f;
+            for (int s2 = 0; s2 < L.splits; ++s2) {
+              const float* src = L.partial + (static_cast<int64_t>(s2) * L.M + m0 + i0) * L.N + n;
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (m0 + i0 + i < L.M) sum[i] += __ldcg(src + static_cast<int64_t>(i) * L.N);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (m0 + i0 + i < L.M) L.y[static_cast<int64_t>(m0 + i0 + i) * L.N + n] = __float2bfloat16_rn(sum[i]);
           }
         }
         named_bar(1, 128);
+      }
+    }
+  } else {
+    // ------------------------------ dequant ------------------------------
+    const int grp = (warp - 6) >> 2;
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+    // TMA swizzle of the code tile: 16-byte piece p of row r sits at
+    // p ^ (r & 7) for 128-byte rows and p ^ ((r >> 2) & 1) for 32-byte rows,
+    // which keeps every 8-thread phase of a 16-byte shared load on distinct banks
+    const int rot = BK == 256 ? (row & 7) : ((row >> 2) & 1);
+    Ring st, at;
+    int turn = 0;  // stage counter modulo G
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
+      int j, nt, mt, sp, c0, nk, nl;
+      locate(u, j, nt, mt, sp, c0, nk, nl);
+      const W4Layer& L = p.layer[j];
+      const int n = nt * 128 + row;
+      const uint8_t* srow = L.scales + static_cast<int64_t>(n) * (L.K / 16);
+      for (int c = 0; c < nk + nl; ++c, st.next<C::STAGES>(), at.next<C::AST>(), turn = turn + 1 == G ? 0 : turn + 1) {
+        if (turn != grp) continue;
+        uint32_t scw[KSUB];
+        if constexpr (!C::SC_TMA) {
+          if (c < nk) scw[0] = __ldg(reinterpret_cast<const uint32_t*>(srow + (c0 + c) * (BK / 16)));
+        }
+        if (!mbar_wait(&sh.full[st.idx], st.use & 1, abort, p.status)) {
+          ok = false;
+          break;
+        }
+        // the TMEM slot of this stage was released by the MMAs issued
+        // AST stages ago (short latency), so take it before converting
+        if (at.use > 0 && !mbar_wait(&sh.a_empty[at.idx], (at.use - 1) & 1, abort, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t* stage = tiles + st.idx * C::STAGE;
+        const uint32_t a_addr = tmem + lane_addr + C::A_COL + C::A_STAGE_COLS * at.idx;
+        if (c < nk) {
+          if constexpr (C::SC_TMA) {
+            const uint4 sv = *reinterpret_cast<const uint4*>(stage + C::X_BYTES + C::C_BYTES + row * (BK / 16));
+            scw[0] = sv.x;
+            scw[1] = sv.y;
+            scw[2] = sv.z;
+            scw[3] = sv.w;
+          }
+          const uint4* crow = reinterpret_cast<const uint4*>(stage + C::X_BYTES + row * C::C_ROW);
+          // 64 values at a time: convert, then store (the store runs async
+          // while the next sub-chunk converts)
+#pragma unroll
+          for (int h = 0; h < KSUB; ++h) {
+            uint32_t w[8];
+#pragma unroll
+            for (int pc = 0; pc < 2; ++pc) {
+              const uint4 v = crow[(2 * h + pc) ^ rot];
+              w[4 * pc] = v.x;
+              w[4 * pc + 1] = v.y;
+              w[4 * pc + 2] = v.z;
+              w[4 * pc + 3] = v.w;
+            }
+            uint32_t out[32];
+            dequant64<F16>(w, scw[h], out);
+            tmem_st32(a_addr + 32 * h, out);
+          }
+        } else {
+          // LoRA stage: A word i holds (B[n, rb+i], B[n, rb+i]) against the
+          // (high, low) halves of t'; zero past rank r
+          const int rb = (c - nk) * (BK / 2);
+          const uint16_t* brow = L.B + static_cast<int64_t>(n) * L.r + rb;
+#pragma unroll
+          for (int h = 0; h < KSUB; ++h) {
+            uint32_t out[32];
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              const int v8 = 4 * h + v4;
+              uint4 bv = make_uint4(0, 0, 0, 0);
+              if (rb + 8 * v8 < L.r) bv = __ldg(reinterpret_cast<const uint4*>(brow) + v8);
+              const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                out[8 * v4 + 2 * e] = (bw[e] & 0xFFFFu) * 0x10001u;
+                out[8 * v4 + 2 * e + 1] = (bw[e] >> 16) * 0x10001u;
+              }
+            }
+            tmem_st32(a_addr + 32 * h, out);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sh.a_full[at.idx]);
+          mbar_arrive(&sh.empty[st.idx]);
+        }
       }
     }
   }
@@ -372,15 +470,18 @@ __global__ void __launch_bounds__(kThreads, 1) w4a16_tc_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------------------
-// Prologue: one CTA per token row m.
+// Prologue: one CTA per (token row m, group of 8 LoRA ranks).
 //   F16: p_m so that max|x_m| 2^-p_m is in [2^14, 2^15); x16 = f16(x 2^-p_m)
+//        (written by the rank-group-0 CTA; every CTA derives p_m itself)
 //   LoRA: t_j = sum_k x[m,k] A[j,k] (fp32); v = (alpha/r) t_j / (g 2^p_m);
-//         t'[m, j] = bf16(v), t'[m, r + j] = bf16(v - bf16(v)); zero to 64 lc.
+//         t'[m, 2j] = bf16(v), t'[m, 2j + 1] = bf16(v - bf16(v)); zero to t_cols.
 template <bool F16>
-__global__ void __launch_bounds__(256) lora_prep_kernel(PrepArgs a) {
-  __shared__ float red[8][16];
+__global__ void __launch_bounds__(256) lora_prep_kernel(const __grid_constant__ PrepBatch batch) {
+  __shared__ float red[8][8];
   __shared__ uint32_t amax_s[8];
-  const int m = blockIdx.x;
+  const PrepArgs& a = batch.a[blockIdx.z];
+  const int m = blockIdx.x, rg = blockIdx.y;
+  if (rg > 0 && 8 * rg >= a.r) return;  // this layer has fewer rank groups
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint4* xr = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(m) * a.K);
   const int nvec = static_cast<int>(a.K / 8);
@@ -392,96 +493,97 @@ __global__ void __launch_bounds__(256) lora_prep_kernel(PrepArgs a) {
     if (lane == 0) amax_s[warp] = mx;
     __syncthreads();
     mx = amax_s[0];
-    for (int i = 1; i < 8; ++i) mx = max(mx, amax_s[i]);
-    if (mx >= 0x7F80u && threadIdx.x == 0) flag(a.status, QRR_DEV_NONFINITE);
-    if (mx != 0u) {
-      const float amax = bf16bits_to_f32(mx);
-      int e;
-      frexpf(amax, &e);  // amax = f 2^e, 0.5 <= f < 1
-      pexp = e - 15;     // amax 2^-p in [2^14, 2^15)
-    }
-    if (threadIdx.x == 0) a.pexp[m] = pexp;
-    const Pow2Scaler sc(pexp);
-    uint4* x16 = reinterpret_cast<uint4*>(a.x16 + static_cast<int64_t>(m) * a.K);
-    for (int v = threadIdx.x; v < nvec; v += 256) {
-      const uint4 xv = __ldg(xr + v);
-      const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
-      uint32_t o[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __half2 h = __floats2half2_rn(sc(bf16_lo(w[i])), sc(bf16_hi(w[i])));
-        o[i] = *reinterpret_cast<const uint32_t*>(&h);
+    for (int i = 1; i < 8; ++i) mx = max(mx, amax_s[i]);
+    if (mx != 0u) {
+      int e;
+      frexpf(bf16bits_to_f32(mx), &e);  // amax = f 2^e, 0.5 <= f < 1
+      pexp = e - 15;                    // amax 2^-p in [2^14, 2^15)
+    }
+    if (rg == 0) {
+      if (mx >= 0x7F80u && threadIdx.x == 0) flag(a.status, QRR_DEV_NONFINITE);
+      if (threadIdx.x == 0) a.pexp[m] = pexp;
+      const Pow2Scaler sc(pexp);
+      uint4* x16 = reinterpret_cast<uint4*>(a.x16 + static_cast<int64_t>(m) * a.K);
+      for (int v = threadIdx.x; v < nvec; v += 256) {
+        const uint4 xv = __ldg(xr + v);
+        const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __half2 h = __floats2half2_rn(sc(bf16_lo(w[i])), sc(bf16_hi(w[i])));
+          o[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        x16[v] = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      x16[v] = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
   if (a.r == 0) return;
-  const float st = *a.tensor_scale;
-  const float g = st > 0.0f ? st : 1.0f;
-  // (alpha/r) / (g 2^p): divide by g first, then scale by the power of two
-  const Pow2Scaler unp(pexp);
-  for (int j0 = 0; j0 < a.r; j0 += 16) {
-    float part[16];
+  const int j0 = rg * 8;
+  const int nj = min(8, a.r - j0);
+  float part[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) part[i] = 0.0f;
-    for (int v = threadIdx.x; v < nvec; v += 256) {
-      const uint4 xv = __ldg(xr + v);
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+  for (int i = 0; i < 8; ++i) part[i] = 0.0f;
+  for (int v = threadIdx.x; v < nvec; v += 256) {
+    const uint4 xv = __ldg(xr + v);
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if (j0 + i >= a.r) break;
-        const uint4 av = __ldg(reinterpret_cast<const uint4*>(a.A + static_cast<int64_t>(j0 + i) * a.K) + v);
-        const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
-        float s = part[i];
+    for (int i = 0; i < 8; ++i) {
+      if (i >= nj) break;
+      const uint4 av = __ldg(reinterpret_cast<const uint4*>(a.A + static_cast<int64_t>(j0 + i) * a.K) + v);
+      const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
+      float s = part[i];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          s = fmaf(bf16_lo(xw[q]), bf16_lo(aw[q]), s);
-          s = fmaf(bf16_hi(xw[q]), bf16_hi(aw[q]), s);
-        }
-        part[i] = s;
+      for (int q = 0; q < 4; ++q) {
+        s = fmaf(bf16_lo(xw[q]), bf16_lo(aw[q]), s);
+        s = fmaf(bf16_hi(xw[q]), bf16_hi(aw[q]), s);
       }
+      part[i] = s;
     }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) part[i] += __shfl_xor_sync(0xFFFFFFFFu, part[i], o);
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) red[warp][i] = part[i];
-    }
-    __syncthreads();
-    if (threadIdx.x < 16 && j0 + static_cast<int>(threadIdx.x) < a.r) {
-      float t = 0.0f;
-      for (int w2 = 0; w2 < 8; ++w2) t += red[w2][threadIdx.x];
-      const float v = unp(__fdiv_rn(a.lora_scale * t, g));
-      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-      const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-      __nv_bfloat16* trow = a.t + static_cast<int64_t>(m) * a.t_cols;
-      trow[j0 + threadIdx.x] = hi;
-      trow[a.r + j0 + threadIdx.x] = lo;
-    }
-    __syncthreads();
   }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) part[i] += __shfl_xor_sync(0xFFFFFFFFu, part[i], o);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) red[warp][i] = part[i];
+  }
+  __syncthreads();
   __nv_bfloat16* trow = a.t + static_cast<int64_t>(m) * a.t_cols;
-  for (int j = 2 * a.r + threadIdx.x; j < a.t_cols; j += 256) trow[j] = __float2bfloat16_rn(0.0f);
+  if (threadIdx.x < nj) {
+    float t = 0.0f;
+#pragma unroll
+    for (int w2 = 0; w2 < 8; ++w2) t += red[w2][threadIdx.x];
+    const float st = *a.tensor_scale;
+    const float g = st > 0.0f ? st : 1.0f;
+    // (alpha/r) t / (g 2^p): divide by g, then scale by the power of two
+    const float v = Pow2Scaler(pexp)(__fdiv_rn(a.lora_scale * t, g));
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+    trow[2 * (j0 + threadIdx.x)] = hi;
+    trow[2 * (j0 + threadIdx.x) + 1] = lo;
+  }
+  if (rg == 0)
+    for (int j = 2 * a.r + threadIdx.x; j < a.t_cols; j += 256) trow[j] = __float2bfloat16_rn(0.0f);
 }
 
 // ---------------------------------------------------------------------------
 
 namespace {
 
-template <int BN, bool F16>
+template <int BN, int BK, bool F16, int G>
 cudaError_t launch_bn(const W4Params& p, int grid, cudaStream_t stream) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, BK, G>;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(w4a16_tc_kernel<BN, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(C::SMEM));
+    cudaError_t e = cudaFuncSetAttribute(w4a16_tc_kernel<BN, BK, F16, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  w4a16_tc_kernel<BN, F16><<<grid, kThreads, C::SMEM, stream>>>(p);
+  w4a16_tc_kernel<BN, BK, F16, G><<<grid, C::THREADS, C::SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -495,12 +597,19 @@ int w4_bn_for(int64_t M) {
   return 256;
 }
 
-cudaError_t launch_lora_prep(const PrepArgs& a, bool f16, cudaStream_t stream) {
-  if (a.M == 0) return cudaSuccess;
+// Decode tiles (<= 64 tokens) stream the weight in 256-wide K stages (block
+// scales staged by TMA); prefill tiles use 64-wide stages.
+int w4_bk_for(int64_t M) { return M <= 64 ? 256 : 64; }
+
+cudaError_t launch_lora_prep(const PrepBatch& b, bool f16, cudaStream_t stream) {
+  if (b.count == 0 || b.a[0].M == 0) return cudaSuccess;
+  int groups = 1;
+  for (int j = 0; j < b.count; ++j) groups = max(groups, (b.a[j].r + 7) / 8);
+  const dim3 grid(static_cast<unsigned>(b.a[0].M), static_cast<unsigned>(groups), static_cast<unsigned>(b.count));
   if (f16)
-    lora_prep_kernel<true><<<static_cast<unsigned>(a.M), 256, 0, stream>>>(a);
+    lora_prep_kernel<true><<<grid, 256, 0, stream>>>(b);
   else
-    lora_prep_kernel<false><<<static_cast<unsigned>(a.M), 256, 0, stream>>>(a);
+    lora_prep_kernel<false><<<grid, 256, 0, stream>>>(b);
   return cudaGetLastError();
 }
 
@@ -515,13 +624,14 @@ cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, cudaStream_t stream) 
   int dev = 0, sms = kSMs;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = units < sms ? units : sms;
-  switch (bn) {
-    case 16: return f16 ? launch_bn<16, true>(p, grid, stream) : launch_bn<16, false>(p, grid, stream);
-    case 32: return f16 ? launch_bn<32, true>(p, grid, stream) : launch_bn<32, false>(p, grid, stream);
-    case 64: return f16 ? launch_bn<64, true>(p, grid, stream) : launch_bn<64, false>(p, grid, stream);
-    case 128: return launch_bn<128, false>(p, grid, stream);
-    default: return launch_bn<256, false>(p, grid, stream);
+  if (f16) {
+    switch (bn) {
+      case 16: return launch_bn<16, 256, true, 3>(p, grid, stream);
+      case 32: return launch_bn<32, 256, true, 3>(p, grid, stream);
+      default: return launch_bn<64, 256, true, 3>(p, grid, stream);
+    }
   }
+  return bn == 128 ? launch_bn<128, 64, false, 2>(p, grid, stream) : launch_bn<256, 64, false, 2>(p, grid, stream);
 }
 
 }  // namespace qrr

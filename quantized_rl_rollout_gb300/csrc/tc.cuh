@@ -4,7 +4,7 @@
 // descriptors the MMA reads.
 //
 // Every wait here is bounded: a wait that does not complete within
-// kWaitLimitNs sets `*abort` (a per-CTA shared flag) and the kernel's
+// kWaitLimitCycles sets `*abort` (a per-CTA shared flag) and the kernel's
 // QRR_DEV_TIMEOUT status bit, and all later waits of the CTA return at once,
 // so a broken pipeline ends the kernel instead of hanging the GPU.
 #pragma once
@@ -17,18 +17,13 @@
 
 namespace qrr {
 
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr long long kWaitLimitCycles = 4000000000ll;  // about 2 s at the GB300's 2 GHz SM clock
 constexpr int32_t kDevTimeout = 0x2;                         // status bit of a timed-out wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 
 // ---- mbarrier -------------------------------------------------------------
 
@@ -67,11 +62,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // CTA already timed out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
+  // the SM cycle counter is cheap to read (a global timer read costs about a
+  // microsecond, which would add that much latency to every hand-off)
+  const long long t0 = clock64();
   while (true) {
-    if (*abort) return false;
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
       *abort = 1;
       flag(status, kDevTimeout);
       return false;

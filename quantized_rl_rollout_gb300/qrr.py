@@ -35,6 +35,14 @@ class WeightDesc(ctypes.Structure):
                 ("tensor_scale", _c_p)]
 
 
+class LinearDesc(ctypes.Structure):
+    """Mirror of ``qrr_linear_desc``."""
+
+    _fields_ = [("x", _c_p), ("N", _c_i64), ("K", _c_i64), ("codes", _c_p), ("scales", _c_p),
+                ("tensor_scale", _c_p), ("lora_A", _c_p), ("lora_B", _c_p), ("r", _c_i32), ("alpha", ctypes.c_float),
+                ("y", _c_p)]
+
+
 # symbol -> (restype, argtypes)
 SIGNATURES = {
     "qrr_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -44,6 +52,9 @@ SIGNATURES = {
     "qrr_linear_nvfp4_lora_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_i64, _c_i32]),
     "qrr_linear_nvfp4_lora": (ctypes.c_int, [_c_p, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_p, _c_i32,
                                              ctypes.c_float, _c_p, _c_p, _c_sz, _c_p, _c_p]),
+    "qrr_linear_nvfp4_lora_grouped_workspace_bytes": (_c_sz, [ctypes.POINTER(LinearDesc), _c_i32, _c_i64]),
+    "qrr_linear_nvfp4_lora_grouped": (ctypes.c_int, [ctypes.POINTER(LinearDesc), _c_i32, _c_i64, _c_p, _c_sz, _c_p,
+                                                     _c_p]),
     "qrr_quantize_fp8_w128x128": (ctypes.c_int, [_c_p, _c_i64, _c_i64, _c_p, _c_p, _c_i32, _c_p, _c_p]),
     "qrr_quantize_fp8_a1x128": (ctypes.c_int, [_c_p, _c_i64, _c_i64, _c_p, _c_p, _c_i32, _c_p, _c_p]),
     "qrr_gemm_fp8_blockwise": (ctypes.c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_p, _c_i32, _c_p,
@@ -147,6 +158,46 @@ def linear_nvfp4_lora(x, codes, scales, tensor_scale, lora_A=None, lora_B=None, 
                                        workspace.numel(), _ptr(dev_status), _stream(stream)),
            "qrr_linear_nvfp4_lora")
     return y
+
+
+def _linear_descs(layers):
+    descs = (LinearDesc * len(layers))()
+    m = None
+    for i, d in enumerate(layers):
+        x, codes, scales, ts = d["x"], d["codes"], d["scales"], d["tensor_scale"]
+        _need(x, torch.bfloat16, f"layers[{i}].x")
+        a, b = d.get("lora_A"), d.get("lora_B")
+        r = 0 if a is None or b is None else int(a.shape[0])
+        if m is None:
+            m = x.shape[0]
+        elif x.shape[0] != m:
+            raise ValueError("every layer of a grouped call has the same token count")
+        if d.get("y") is None:
+            d["y"] = torch.empty(m, codes.shape[0], dtype=torch.bfloat16, device=x.device)
+        descs[i] = LinearDesc(_ptr(x), codes.shape[0], x.shape[1], _ptr(codes), _ptr(scales), _ptr(ts), _ptr(a),
+                              _ptr(b), r, float(d.get("alpha", 0.0)), _ptr(d["y"]))
+    return descs, (m or 0)
+
+
+def linear_nvfp4_lora_grouped_workspace_bytes(layers) -> int:
+    descs, m = _linear_descs(layers)
+    return int(lib().qrr_linear_nvfp4_lora_grouped_workspace_bytes(descs, len(layers), m))
+
+
+def linear_nvfp4_lora_grouped(layers, workspace=None, dev_status=None, stream=None):
+    """Run up to 8 layers sharing the token count in one grouped call.
+
+    ``layers`` is a list of dicts with keys x, codes, scales, tensor_scale and
+    optionally lora_A, lora_B, alpha, y (allocated when absent).  Returns the
+    list of outputs.
+    """
+    descs, m = _linear_descs(layers)
+    if workspace is None:
+        nbytes = lib().qrr_linear_nvfp4_lora_grouped_workspace_bytes(descs, len(layers), m)
+        workspace = _workspace(nbytes, layers[0]["x"].device)
+    _check(lib().qrr_linear_nvfp4_lora_grouped(descs, len(layers), m, _ptr(workspace), workspace.numel(),
+                                               _ptr(dev_status), _stream(stream)), "qrr_linear_nvfp4_lora_grouped")
+    return [d["y"] for d in layers]
 
 
 def quantize_fp8_w128x128(W, mode=SCALE_FP32, q=None, scales=None, dev_status=None, stream=None):

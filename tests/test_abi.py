@@ -72,6 +72,23 @@ def test_argument_validation(lib):
     assert lib.qrr_quantize_fp8_w128x128(FAKE, 4, 128, FAKE + 4, FAKE, 0, None, None) == 3
     assert lib.qrr_gemm_fp8_blockwise(FAKE, FAKE, FAKE, FAKE, 4, 100, 128, FAKE, 0, None, None) == 2
     assert lib.qrr_round_probe(FAKE, 4, 5, FAKE, None) == 1
+    # adapter rank above 64 is outside the linear's contract
+    lws = lib.qrr_linear_nvfp4_lora_workspace_bytes(16, 128, 256, 72)
+    assert lin(FAKE, 16, 256, FAKE, FAKE, FAKE, 128, FAKE, FAKE, 72, 16.0, FAKE, FAKE, lws, None, None) == 2
+
+
+def test_grouped_linear_validation(lib):
+    from quantized_rl_rollout_gb300 import qrr
+
+    descs = (qrr.LinearDesc * 9)()
+    for i in range(9):
+        descs[i] = qrr.LinearDesc(FAKE, 128, 256, FAKE, FAKE, FAKE, None, None, 0, 0.0, FAKE)
+    assert lib.qrr_linear_nvfp4_lora_grouped(descs, 9, 16, FAKE, 1 << 20, None, None) == 2  # > 8 layers
+    ws = lib.qrr_linear_nvfp4_lora_grouped_workspace_bytes(descs, 3, 16)
+    assert ws > 0
+    assert lib.qrr_linear_nvfp4_lora_grouped(descs, 3, 16, FAKE, ws - 1, None, None) == 4
+    descs[1] = qrr.LinearDesc(FAKE, 100, 256, FAKE, FAKE, FAKE, None, None, 0, 0.0, FAKE)  # N % 128
+    assert lib.qrr_linear_nvfp4_lora_grouped(descs, 3, 16, FAKE, ws, None, None) == 2
 
 
 def test_requant_descriptor_validation(lib):

@@ -61,7 +61,7 @@ def test_tiny_config(q):
 
 
 @pytest.mark.parametrize("m", [1, 3, 8, 17, 64, 65, 256])
-@pytest.mark.parametrize("r", [0, 8, 32])
+@pytest.mark.parametrize("r", [0, 8, 32, 64])
 def test_token_counts_and_ranks(q, m, r):
     n, k = 384, 1024
     W, codes, scales, ts, A, B, alpha = _layer(q, n, k, r, f"mr{r}")
@@ -123,6 +123,42 @@ def test_decode_8b_layer_set_sampled(q, m):
         y_ref = _ref(x, codes, scales, ts, A, B, alpha, rows=rows)
         _assert_close(y[:, torch.from_numpy(rows).to(DEV)], y_ref, f"{layer.name} m={m}")
         del W, codes, scales
+
+
+@pytest.mark.parametrize("m", [1, 8, 64, 300])
+def test_grouped_layer_set(q, m):
+    """The grouped call over a mixed layer set (different N, K, ranks, one
+    layer without adapter) matches the oracle layer by layer."""
+    shapes = [(384, 1024, 32), (128, 256, 8), (256, 2048, 0), (512, 768, 64)]
+    layers = []
+    for i, (n, k, r) in enumerate(shapes):
+        W, codes, scales, ts, A, B, alpha = _layer(q, n, k, r, f"grp{i}")
+        x = inputs.activations(m, k, inputs.derive_seed(0, "grp-x", i, m), device=DEV)
+        layers.append(dict(x=x, codes=codes, scales=scales, tensor_scale=ts, lora_A=A, lora_B=B, alpha=alpha))
+    ys = q.linear_nvfp4_lora_grouped(layers)
+    torch.cuda.synchronize()
+    for i, d in enumerate(layers):
+        _assert_close(ys[i], _ref(d["x"], d["codes"], d["scales"], d["tensor_scale"], d["lora_A"], d["lora_B"],
+                                  d["alpha"]), f"grouped layer {i} m={m}")
+
+
+def test_grouped_8b_decode_sampled(q):
+    """The 8B-class layer set at 64 tokens in one grouped call; sampled columns."""
+    g = np.random.default_rng(9)
+    r = configs.DECODE_8B["r"]
+    layers = []
+    for layer in configs.LAYERS_8B:
+        W, codes, scales, ts, A, B, alpha = _layer(q, layer.n, layer.k, r, f"g8b/{layer.name}")
+        x = inputs.activations(64, layer.k, inputs.derive_seed(0, "g8b-x", layer.name), device=DEV)
+        layers.append(dict(x=x, codes=codes, scales=scales, tensor_scale=ts, lora_A=A, lora_B=B, alpha=alpha))
+        del W
+    ys = q.linear_nvfp4_lora_grouped(layers)
+    torch.cuda.synchronize()
+    for layer, d, y in zip(configs.LAYERS_8B, layers, ys):
+        rows = np.unique(np.concatenate([[0, layer.n - 1], g.integers(0, layer.n, 126)]))
+        y_ref = _ref(d["x"], d["codes"], d["scales"], d["tensor_scale"], d["lora_A"], d["lora_B"], d["alpha"],
+                     rows=rows)
+        _assert_close(y[:, torch.from_numpy(rows).to(DEV)], y_ref, f"grouped 8B {layer.name}")
 
 
 @pytest.mark.parametrize("mode", [0, 1])
