@@ -85,10 +85,14 @@ LinPlan plan_linear(int64_t M, const LinIn* in, int count) {
     p.l[j].kcps = kc[j];
   }
   if (decode) {
+    // Cost model in pipeline stages: a unit costs its K stages plus its
+    // epilogue (about half a stage, or three when it writes a split-K partial
+    // and may run the reduction); units go round-robin to the SMs, so the
+    // makespan is bounded by waves x the costliest unit.
     double best = -1.0;
     for (int ul = maxkc; ul >= 1; --ul) {
-      double work = 0.0;
-      int units = 0, longest = 1;
+      double work = 0.0, worst = 0.0;
+      int units = 0;
       int sp[kMaxW4Layers];
       for (int j = 0; j < count; ++j) {
         int s = std::min((kc[j] + ul - 1) / ul, std::min(cap[j], kc[j]));
@@ -98,10 +102,10 @@ LinPlan plan_linear(int64_t M, const LinIn* in, int count) {
         const int base = p.l[j].n_tiles * p.m_tiles;
         units += base * s;
         work += static_cast<double>(base) * kc[j];
-        longest = std::max(longest, kcps);
+        worst = std::max(worst, kcps + (s > 1 ? 3.0 : 0.5));
       }
       const int waves = (units + kSMs - 1) / kSMs;
-      const double eff = work / (static_cast<double>(waves) * kSMs * longest);
+      const double eff = work / (static_cast<double>(kSMs) * waves * worst);
       if (eff > best + 1e-9) {
         best = eff;
         for (int j = 0; j < count; ++j) {

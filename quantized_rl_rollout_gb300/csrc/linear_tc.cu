@@ -69,20 +69,24 @@ struct Cfg {
   static constexpr int DBUF = BN <= 128 ? 2 : 1;  // accumulator buffers in TMEM
   static constexpr int D_COLS = BN < 32 ? 32 : BN;
   static constexpr int A_COL = DBUF * D_COLS;
-  static constexpr int A_STAGE_COLS = BK / 2;
-  static constexpr int AST_RAW = (512 - A_COL) / A_STAGE_COLS;
+  // The A operand moves through TMEM in chunks of up to 128 K (64 columns), so
+  // a dequant group can fill its next chunk while the MMAs still read its last.
+  static constexpr int ACH = BK < 128 ? BK : 128;  // K per A chunk
+  static constexpr int ACOLS = ACH / 2;
+  static constexpr int CPS = BK / ACH;             // A chunks per stage
+  static constexpr int AST_RAW = (512 - A_COL) / ACOLS;
   static constexpr int AST = (AST_RAW > 8 ? 8 : AST_RAW) / G * G;
   static constexpr int THREADS = 32 * (2 + 4 + 4 * G);
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE + 1024;
   static_assert(STAGES >= 2, "shared memory ring too small");
-  static_assert(AST >= G, "TMEM ring too small");
-  static_assert(A_COL + AST * A_STAGE_COLS <= 512, "TMEM overflow");
+  static_assert(AST >= 2 * G, "TMEM ring too small");
+  static_assert(A_COL + AST * ACOLS <= 512, "TMEM overflow");
 };
 
 struct SharedCtl {
   uint64_t full[8], empty[8];
-  uint64_t a_full[8], a_empty[8];
+  uint64_t a_full[8], a_empty[8];  // per A chunk slot
   uint64_t d_full[2], d_empty[2];
   uint64_t done;
   uint32_t tmem;
@@ -175,7 +179,7 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&sh.full[s], 1);
-      mbar_init(&sh.empty[s], 5);  // MMA commit + the 4 warps of one dequant group
+      mbar_init(&sh.empty[s], 1 + 4 * C::CPS);  // MMA commit + 4 dequant warps per A chunk
     }
     for (int s = 0; s < C::AST; ++s) {
       mbar_init(&sh.a_full[s], 4);
@@ -268,21 +272,26 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
         const uint32_t duse = units / C::DBUF;
         if (duse > 0 && !mbar_wait(&sh.d_empty[db], (duse - 1) & 1, abort, p.status)) break;
         const uint32_t dcol = tmem + db * C::D_COLS;
-        for (int c = 0; c < nk + nl; ++c, st.next<C::STAGES>(), at.next<C::AST>()) {
-          if (!mbar_wait(&sh.a_full[at.idx], at.use & 1, abort, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        for (int c = 0; c < nk + nl && ok; ++c, st.next<C::STAGES>()) {
           const uint32_t xb = smem_u32(tiles + st.idx * C::STAGE);
-          const uint32_t a0 = tmem + C::A_COL + C::A_STAGE_COLS * at.idx;
           const uint32_t idesc = c < nk ? id_main : id_lora;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            mma_bf16_ts(dcol, a0 + 8 * k, sw128_desc(xb + (k >> 2) * C::X_SUB + 32 * (k & 3)), idesc,
-                        (c > 0 || k > 0) ? 1u : 0u);
-          mma_commit(&sh.empty[st.idx]);
-          mma_commit(&sh.a_empty[at.idx]);
+          for (int hc = 0; hc < C::CPS; ++hc, at.next<C::AST>()) {
+            if (!mbar_wait(&sh.a_full[at.idx], at.use & 1, abort, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = tmem + C::A_COL + C::ACOLS * at.idx;
+#pragma unroll
+            for (int k = 0; k < C::ACH / 16; ++k) {
+              const int kk = hc * (C::ACH / 16) + k;  // K16 step within the stage
+              mma_bf16_ts(dcol, a0 + 8 * k, sw128_desc(xb + (kk >> 2) * C::X_SUB + 32 * (kk & 3)), idesc,
+                          (c > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&sh.a_empty[at.idx]);
+          }
+          if (ok) mma_commit(&sh.empty[st.idx]);
         }
         if (!ok) break;
         mma_commit(&sh.d_full[db]);
@@ -334,30 +343,44 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.d_empty[db]);
       if (part) {
-        __threadfence();
+        // all 128 epilogue threads have written their partials; one thread
+        // makes them visible GPU-wide (the fence is cumulative over the
+        // barrier) and takes a ticket; the last split of the tile sums all
+        // partials in split order
         named_bar(1, 128);
         if (warp == 2 && lane == 0) {
+          __threadfence();
           uint32_t* cnt = L.counters + mt * L.n_tiles + nt;
           const uint32_t prev = atomicAdd(cnt, 1u);
           sh.last = prev == static_cast<uint32_t>(L.splits - 1);
-          if (sh.last) *cnt = 0u;  // ready for the next call
+          if (sh.last) {
+            *cnt = 0u;  // ready for the next call
+            __threadfence();
+          }
         }
         named_bar(1, 128);
         if (sh.last) {
-          __threadfence();
-          // sum the splits in fixed order, 16 tokens at a time
-          for (int i0 = 0; i0 < BN; i0 += 16) {
-            float sum[16];
+          constexpr int TB = 8, SB = 4;  // tokens per batch; loads of SB splits in flight
+          for (int i0 = 0; i0 < BN && m0 + i0 < L.M; i0 += TB) {
+            float sum[TB];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) sum[i] = 0.0f;
-            for (int s2 = 0; s2 < L.splits; ++s2) {
-              const float* src = L.partial + (static_cast<int64_t>(s2) * L.M + m0 + i0) * L.N + n;
+            for (int i = 0; i < TB; ++i) sum[i] = 0.0f;
+            for (int s0 = 0; s0 < L.splits; s0 += SB) {
+              float v[SB][TB];
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
-                if (m0 + i0 + i < L.M) sum[i] += __ldcg(src + static_cast<int64_t>(i) * L.N);
+              for (int s1 = 0; s1 < SB; ++s1)
+#pragma unroll
+                for (int i = 0; i < TB; ++i)
+                  v[s1][i] = (s0 + s1 < L.splits && m0 + i0 + i < L.M)
+                                 ? __ldcg(L.partial + (static_cast<int64_t>(s0 + s1) * L.M + m0 + i0 + i) * L.N + n)
+                                 : 0.0f;
+#pragma unroll
+              for (int s1 = 0; s1 < SB; ++s1)
+#pragma unroll
+                for (int i = 0; i < TB; ++i) sum[i] += v[s1][i];
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
+            for (int i = 0; i < TB; ++i)
               if (m0 + i0 + i < L.M) L.y[static_cast<int64_t>(m0 + i0 + i) * L.N + n] = __float2bfloat16_rn(sum[i]);
           }
         }
@@ -375,7 +398,7 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
     // which keeps every 8-thread phase of a 16-byte shared load on distinct banks
     const int rot = BK == 256 ? (row & 7) : ((row >> 2) & 1);
     Ring st, at;
-    int turn = 0;  // stage counter modulo G
+    int turn = 0;  // A-chunk counter modulo G
     bool ok = true;
     for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
       int j, nt, mt, sp, c0, nk, nl;
@@ -383,80 +406,79 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
       const W4Layer& L = p.layer[j];
       const int n = nt * 128 + row;
       const uint8_t* srow = L.scales + static_cast<int64_t>(n) * (L.K / 16);
-      for (int c = 0; c < nk + nl; ++c, st.next<C::STAGES>(), at.next<C::AST>(), turn = turn + 1 == G ? 0 : turn + 1) {
-        if (turn != grp) continue;
-        uint32_t scw[KSUB];
-        if constexpr (!C::SC_TMA) {
-          if (c < nk) scw[0] = __ldg(reinterpret_cast<const uint32_t*>(srow + (c0 + c) * (BK / 16)));
-        }
-        if (!mbar_wait(&sh.full[st.idx], st.use & 1, abort, p.status)) {
-          ok = false;
-          break;
-        }
-        // the TMEM slot of this stage was released by the MMAs issued
-        // AST stages ago (short latency), so take it before converting
-        if (at.use > 0 && !mbar_wait(&sh.a_empty[at.idx], (at.use - 1) & 1, abort, p.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint8_t* stage = tiles + st.idx * C::STAGE;
-        const uint32_t a_addr = tmem + lane_addr + C::A_COL + C::A_STAGE_COLS * at.idx;
-        if (c < nk) {
-          if constexpr (C::SC_TMA) {
-            const uint4 sv = *reinterpret_cast<const uint4*>(stage + C::X_BYTES + C::C_BYTES + row * (BK / 16));
-            scw[0] = sv.x;
-            scw[1] = sv.y;
-            scw[2] = sv.z;
-            scw[3] = sv.w;
+      for (int c = 0; c < nk + nl && ok; ++c, st.next<C::STAGES>()) {
+#pragma unroll 1
+        for (int hc = 0; hc < C::CPS; ++hc, at.next<C::AST>(), turn = turn + 1 == G ? 0 : turn + 1) {
+          if (turn != grp) continue;
+          uint32_t scw[C::ACH / 64];
+          if constexpr (!C::SC_TMA) {
+            if (c < nk) scw[0] = __ldg(reinterpret_cast<const uint32_t*>(srow + (c0 + c) * (BK / 16)));
           }
-          const uint4* crow = reinterpret_cast<const uint4*>(stage + C::X_BYTES + row * C::C_ROW);
-          // 64 values at a time: convert, then store (the store runs async
-          // while the next sub-chunk converts)
-#pragma unroll
-          for (int h = 0; h < KSUB; ++h) {
-            uint32_t w[8];
-#pragma unroll
-            for (int pc = 0; pc < 2; ++pc) {
-              const uint4 v = crow[(2 * h + pc) ^ rot];
-              w[4 * pc] = v.x;
-              w[4 * pc + 1] = v.y;
-              w[4 * pc + 2] = v.z;
-              w[4 * pc + 3] = v.w;
+          if (!mbar_wait(&sh.full[st.idx], st.use & 1, abort, p.status) ||
+              (at.use > 0 && !mbar_wait(&sh.a_empty[at.idx], (at.use - 1) & 1, abort, p.status))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint8_t* stage = tiles + st.idx * C::STAGE;
+          const uint32_t a_addr = tmem + lane_addr + C::A_COL + C::ACOLS * at.idx;
+          if (c < nk) {
+            if constexpr (C::SC_TMA) {
+              // this chunk's 8 scale bytes of the row's 16 (ACH = 128)
+              const uint2 sv =
+                  *reinterpret_cast<const uint2*>(stage + C::X_BYTES + C::C_BYTES + row * (BK / 16) + 8 * hc);
+              scw[0] = sv.x;
+              scw[1] = sv.y;
             }
-            uint32_t out[32];
-            dequant64<F16>(w, scw[h], out);
-            tmem_st32(a_addr + 32 * h, out);
-          }
-        } else {
-          // LoRA stage: A word i holds (B[n, rb+i], B[n, rb+i]) against the
-          // (high, low) halves of t'; zero past rank r
-          const int rb = (c - nk) * (BK / 2);
-          const uint16_t* brow = L.B + static_cast<int64_t>(n) * L.r + rb;
+            const uint4* crow = reinterpret_cast<const uint4*>(stage + C::X_BYTES + row * C::C_ROW);
+            // 64 values at a time: convert, then store (the store runs async
+            // while the next sub-chunk converts)
 #pragma unroll
-          for (int h = 0; h < KSUB; ++h) {
-            uint32_t out[32];
+            for (int h = 0; h < C::ACH / 64; ++h) {
+              const int piece0 = 2 * ((C::ACH / 64) * hc + h);
+              uint32_t w[8];
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              const int v8 = 4 * h + v4;
-              uint4 bv = make_uint4(0, 0, 0, 0);
-              if (rb + 8 * v8 < L.r) bv = __ldg(reinterpret_cast<const uint4*>(brow) + v8);
-              const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                out[8 * v4 + 2 * e] = (bw[e] & 0xFFFFu) * 0x10001u;
-                out[8 * v4 + 2 * e + 1] = (bw[e] >> 16) * 0x10001u;
+              for (int pc = 0; pc < 2; ++pc) {
+                const uint4 v = crow[(piece0 + pc) ^ rot];
+                w[4 * pc] = v.x;
+                w[4 * pc + 1] = v.y;
+                w[4 * pc + 2] = v.z;
+                w[4 * pc + 3] = v.w;
               }
+              uint32_t out[32];
+              dequant64<F16>(w, scw[h], out);
+              tmem_st32(a_addr + 32 * h, out);
             }
-            tmem_st32(a_addr + 32 * h, out);
+          } else {
+            // LoRA chunk: A word i holds (B[n, rb+i], B[n, rb+i]) against the
+            // (high, low) halves of t'; zero past rank r
+            const int rb = (c - nk) * (BK / 2) + hc * (C::ACH / 2);
+            const uint16_t* brow = L.B + static_cast<int64_t>(n) * L.r + rb;
+#pragma unroll
+            for (int h = 0; h < C::ACH / 64; ++h) {
+              uint32_t out[32];
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4) {
+                const int v8 = 4 * h + v4;
+                uint4 bv = make_uint4(0, 0, 0, 0);
+                if (rb + 8 * v8 < L.r) bv = __ldg(reinterpret_cast<const uint4*>(brow) + v8);
+                const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  out[8 * v4 + 2 * e] = (bw[e] & 0xFFFFu) * 0x10001u;
+                  out[8 * v4 + 2 * e + 1] = (bw[e] >> 16) * 0x10001u;
+                }
+              }
+              tmem_st32(a_addr + 32 * h, out);
+            }
           }
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&sh.a_full[at.idx]);
-          mbar_arrive(&sh.empty[st.idx]);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&sh.a_full[at.idx]);
+            mbar_arrive(&sh.empty[st.idx]);
+          }
         }
       }
     }
@@ -524,13 +546,17 @@ __global__ void __launch_bounds__(256) lora_prep_kernel(const __grid_constant__ 
   float part[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) part[i] = 0.0f;
+  const uint4* arow = reinterpret_cast<const uint4*>(a.A + static_cast<int64_t>(j0) * a.K);
   for (int v = threadIdx.x; v < nvec; v += 256) {
+    // issue every load of this step before any arithmetic
     const uint4 xv = __ldg(xr + v);
+    uint4 av8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) av8[i] = i < nj ? __ldg(arow + static_cast<int64_t>(i) * nvec + v) : make_uint4(0, 0, 0, 0);
     const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      if (i >= nj) break;
-      const uint4 av = __ldg(reinterpret_cast<const uint4*>(a.A + static_cast<int64_t>(j0 + i) * a.K) + v);
+      const uint4 av = av8[i];
       const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
       float s = part[i];
 #pragma unroll
