@@ -129,6 +129,35 @@ qrr_status qrr_linear_nvfp4_lora(const void* x, int64_t M, int64_t K, const uint
                                  int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* W4A16 + LoRA linear that allocates nothing.  The pages have no counterpart
+ * to this call; it exists for callers that cannot get device memory of their
+ * own: code that holds only the input and output buffers it was handed (a
+ * plugin or FFI binding inside a host framework that owns every device
+ * allocation, or a serving process that reserved its whole HBM budget up
+ * front), and code that runs while a CUDA graph is being captured, where
+ * cudaMalloc is not allowed.
+ *
+ * Same arguments, contract and result as qrr_linear_nvfp4_lora, minus the
+ * workspace.  Its scratch is a fixed block of QRR_NOALLOC_SCRATCH_BYTES of
+ * device memory built into the library, which every GPU that loads the
+ * library holds until the process exits.
+ *  - Calls whose scratch need (qrr_linear_nvfp4_lora_workspace_bytes(M, N, K,
+ *    r)) exceeds QRR_NOALLOC_SCRATCH_BYTES return QRR_ERR_WORKSPACE and launch
+ *    nothing.
+ *  - The first call on each device looks up the block's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call shares the block and it keeps the last call's contents (what
+ *    must start at zero is cleared on the stream).  Calls that overlap on the
+ *    GPU, on different streams or different host threads, race on it: order
+ *    them on one stream or serialize them. */
+#define QRR_NOALLOC_SCRATCH_BYTES (16u << 20)
+size_t qrr_noalloc_scratch_bytes(void);
+qrr_status qrr_linear_nvfp4_lora_noalloc(const void* x, int64_t M, int64_t K, const uint8_t* codes,
+                                         const uint8_t* scales, const float* tensor_scale, int64_t N,
+                                         const void* lora_A, const void* lora_B, int32_t r, float alpha,
+                                         void* y, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Grouped W4A16 + LoRA linear: up to 8 independent layers that share the
  * token count M (a decoder layer's q/k/v/o/gate/up/down at one decode step),
  * run as one prologue launch and one persistent tensor-core launch whose work

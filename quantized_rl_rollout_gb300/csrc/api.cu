@@ -4,6 +4,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
+
 #include <algorithm>
 
 #include "linear.cuh"
@@ -245,6 +247,33 @@ size_t linear_ws_bytes(int64_t M, int64_t N, int64_t K, int32_t r) {
   return plan_linear(M, &in, 1).total;
 }
 
+// ---- scratch for qrr_linear_nvfp4_lora_noalloc ----------------------------
+//
+// A fixed block of device memory that the library owns, for callers that
+// cannot allocate device memory themselves.  It is a file-scope __device__
+// array, so every GPU that loads the library holds it until the process
+// exits.  In host code its name is only a host-side stand-in: the device
+// address comes from cudaGetSymbolAddress, taken once per device (with that
+// device current) on the first call.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[QRR_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mutex;
+constexpr int kMaxDevices = 64;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+qrr_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QRR_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_addr[dev]) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || !addr) return QRR_ERR_CUDA;
+    g_noalloc_addr[dev] = addr;
+  }
+  *out = g_noalloc_addr[dev];
+  return QRR_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -333,6 +362,24 @@ qrr_status qrr_linear_nvfp4_lora_grouped(const qrr_linear_desc* descs, int32_t c
     if (st != QRR_OK) return st;
   }
   return run_linear(in, count, M, workspace, workspace_bytes, dev_status, as_stream(stream));
+}
+
+size_t qrr_noalloc_scratch_bytes(void) { return QRR_NOALLOC_SCRATCH_BYTES; }
+
+qrr_status qrr_linear_nvfp4_lora_noalloc(const void* x, int64_t M, int64_t K, const uint8_t* codes,
+                                         const uint8_t* scales, const float* tensor_scale, int64_t N,
+                                         const void* lora_A, const void* lora_B, int32_t r, float alpha, void* y,
+                                         int32_t* dev_status, void* stream) {
+  if (M < 0 || M > INT32_MAX) return M < 0 ? QRR_ERR_INVALID_ARG : QRR_ERR_UNSUPPORTED_SHAPE;
+  const LinIn in = make_in(x, N, K, codes, scales, tensor_scale, lora_A, lora_B, r, alpha, y);
+  qrr_status st = check_linear(in, M, lora_A, lora_B, r);
+  if (st != QRR_OK) return st;
+  // too large for the built-in scratch: refused before anything is launched
+  if (linear_ws_bytes(M, N, K, in.r) > QRR_NOALLOC_SCRATCH_BYTES) return QRR_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != QRR_OK) return st;
+  return run_linear(&in, 1, M, scratch, QRR_NOALLOC_SCRATCH_BYTES, dev_status, as_stream(stream));
 }
 
 qrr_status qrr_quantize_fp8_w128x128(const void* W, int64_t N, int64_t K, uint8_t* q, float* scales,

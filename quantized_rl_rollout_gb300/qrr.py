@@ -52,6 +52,9 @@ SIGNATURES = {
     "qrr_linear_nvfp4_lora_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_i64, _c_i32]),
     "qrr_linear_nvfp4_lora": (ctypes.c_int, [_c_p, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_p, _c_i32,
                                              ctypes.c_float, _c_p, _c_p, _c_sz, _c_p, _c_p]),
+    "qrr_noalloc_scratch_bytes": (_c_sz, []),
+    "qrr_linear_nvfp4_lora_noalloc": (ctypes.c_int, [_c_p, _c_i64, _c_i64, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_p,
+                                                     _c_i32, ctypes.c_float, _c_p, _c_p, _c_p]),
     "qrr_linear_nvfp4_lora_grouped_workspace_bytes": (_c_sz, [ctypes.POINTER(LinearDesc), _c_i32, _c_i64]),
     "qrr_linear_nvfp4_lora_grouped": (ctypes.c_int, [ctypes.POINTER(LinearDesc), _c_i32, _c_i64, _c_p, _c_sz, _c_p,
                                                      _c_p]),
@@ -157,6 +160,20 @@ def linear_nvfp4_lora(x, codes, scales, tensor_scale, lora_A=None, lora_B=None, 
                                        _ptr(lora_A), _ptr(lora_B), r, float(alpha), _ptr(y), _ptr(workspace),
                                        workspace.numel(), _ptr(dev_status), _stream(stream)),
            "qrr_linear_nvfp4_lora")
+    return y
+
+
+def linear_nvfp4_lora_noalloc(x, codes, scales, tensor_scale, lora_A=None, lora_B=None, alpha=0.0, y=None,
+                              dev_status=None, stream=None):
+    """Same as ``linear_nvfp4_lora`` but on the library's built-in scratch (no workspace)."""
+    _need(x, torch.bfloat16, "x")
+    m, k = x.shape
+    n = codes.shape[0]
+    r = 0 if lora_A is None or lora_B is None else int(lora_A.shape[0])
+    y = torch.empty(m, n, dtype=torch.bfloat16, device=x.device) if y is None else y
+    _check(lib().qrr_linear_nvfp4_lora_noalloc(_ptr(x), m, k, _ptr(codes), _ptr(scales), _ptr(tensor_scale), n,
+                                               _ptr(lora_A), _ptr(lora_B), r, float(alpha), _ptr(y),
+                                               _ptr(dev_status), _stream(stream)), "qrr_linear_nvfp4_lora_noalloc")
     return y
 
 
