@@ -52,6 +52,22 @@
 
 namespace qrr {
 
+// Pipeline tracing for development builds: compiled with -DQRR_TRACE_BUILD,
+// CTA 0 records SM clock stamps of its pipeline hand-offs into qrr_trace
+// (role, event, index); qrr_trace_read copies them out.  Ordinary builds
+// compile every stamp away.
+#ifdef QRR_TRACE_BUILD
+__device__ unsigned long long qrr_trace_buf[8][4][256];
+#define QRR_STAMP(role, ev, idx) \
+  do {                                                                  \
+    if (blockIdx.x == 0 && (idx) < 256) qrr_trace_buf[role][ev][idx] = clock64(); \
+  } while (0)
+#else
+#define QRR_STAMP(role, ev, idx) \
+  do {                           \
+  } while (0)
+#endif
+
 namespace {
 
 template <int BN, int BK, int G>
@@ -230,6 +246,7 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
             ok = false;
             break;
           }
+          QRR_STAMP(0, 0, issued);
           uint8_t* xs = tiles + st.idx * C::STAGE;
           uint64_t* fb = &sh.full[st.idx];
           if (c < nk) {
@@ -263,14 +280,16 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
       constexpr uint32_t id_main = make_idesc(F16 ? kFmtF16 : kFmtBF16, F16 ? kFmtF16 : kFmtBF16, 128, BN);
       constexpr uint32_t id_lora = make_idesc(kFmtBF16, kFmtBF16, 128, BN);
       Ring st, at;
-      uint32_t units = 0;
+      uint32_t units = 0, chunks = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x, ++units) {
         int j, nt, mt, sp, c0, nk, nl;
         locate(u, j, nt, mt, sp, c0, nk, nl);
         const int db = units % C::DBUF;
         const uint32_t duse = units / C::DBUF;
+        QRR_STAMP(1, 2, units);
         if (duse > 0 && !mbar_wait(&sh.d_empty[db], (duse - 1) & 1, abort, p.status)) break;
+        QRR_STAMP(1, 3, units);
         const uint32_t dcol = tmem + db * C::D_COLS;
         for (int c = 0; c < nk + nl && ok; ++c, st.next<C::STAGES>()) {
           const uint32_t xb = smem_u32(tiles + st.idx * C::STAGE);
@@ -281,6 +300,7 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
               ok = false;
               break;
             }
+            QRR_STAMP(1, 0, chunks);
             tc_fence_after();
             const uint32_t a0 = tmem + C::A_COL + C::ACOLS * at.idx;
 #pragma unroll
@@ -290,6 +310,8 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
                           (c > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit(&sh.a_empty[at.idx]);
+            QRR_STAMP(1, 1, chunks);
+            ++chunks;
           }
           if (ok) mma_commit(&sh.empty[st.idx]);
         }
@@ -311,7 +333,9 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
       const W4Layer& L = p.layer[j];
       const int n = nt * 128 + 32 * q + lane;
       const int db = units % C::DBUF;
+      if (warp == 2 && lane == 0) QRR_STAMP(3, 0, units);
       if (!mbar_wait(&sh.d_full[db], (units / C::DBUF) & 1, abort, p.status)) break;
+      if (warp == 2 && lane == 0) QRR_STAMP(3, 1, units);
       tc_fence_after();
       const float st = *L.tensor_scale;
       const float g = st > 0.0f ? st : 1.0f;
@@ -342,6 +366,7 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.d_empty[db]);
+      if (warp == 2 && lane == 0) QRR_STAMP(3, 2, units);
       if (part) {
         // all 128 epilogue threads have written their partials; one thread
         // makes them visible GPU-wide (the fence is cumulative over the
@@ -386,6 +411,7 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
         }
         named_bar(1, 128);
       }
+      if (warp == 2 && lane == 0) QRR_STAMP(3, 3, units);
     }
   } else {
     // ------------------------------ dequant ------------------------------
@@ -399,6 +425,7 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
     const int rot = BK == 256 ? (row & 7) : ((row >> 2) & 1);
     Ring st, at;
     int turn = 0;  // A-chunk counter modulo G
+    uint32_t chunk = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
       int j, nt, mt, sp, c0, nk, nl;
@@ -408,8 +435,9 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
       const uint8_t* srow = L.scales + static_cast<int64_t>(n) * (L.K / 16);
       for (int c = 0; c < nk + nl && ok; ++c, st.next<C::STAGES>()) {
 #pragma unroll 1
-        for (int hc = 0; hc < C::CPS; ++hc, at.next<C::AST>(), turn = turn + 1 == G ? 0 : turn + 1) {
+        for (int hc = 0; hc < C::CPS; ++hc, at.next<C::AST>(), turn = turn + 1 == G ? 0 : turn + 1, ++chunk) {
           if (turn != grp) continue;
+          if (q == 2 && lane == 0) QRR_STAMP(4, 0, chunk);
           uint32_t scw[C::ACH / 64];
           if constexpr (!C::SC_TMA) {
             if (c < nk) scw[0] = __ldg(reinterpret_cast<const uint32_t*>(srow + (c0 + c) * (BK / 16)));
@@ -419,6 +447,7 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
             ok = false;
             break;
           }
+          if (q == 2 && lane == 0) QRR_STAMP(4, 1, chunk);
           tc_fence_after();
           const uint8_t* stage = tiles + st.idx * C::STAGE;
           const uint32_t a_addr = tmem + lane_addr + C::A_COL + C::ACOLS * at.idx;
@@ -473,6 +502,7 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
             }
           }
           tmem_st_wait();
+          if (q == 2 && lane == 0) QRR_STAMP(4, 2, chunk);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
@@ -661,3 +691,13 @@ cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, cudaStream_t stream) 
 }
 
 }  // namespace qrr
+
+#ifdef QRR_TRACE_BUILD
+extern "C" int qrr_trace_read(unsigned long long* host) {
+  return static_cast<int>(cudaMemcpyFromSymbol(host, qrr::qrr_trace_buf, sizeof(qrr::qrr_trace_buf)));
+}
+extern "C" int qrr_trace_clear(void) {
+  static unsigned long long zeros[8 * 4 * 256] = {};
+  return static_cast<int>(cudaMemcpyToSymbol(qrr::qrr_trace_buf, zeros, sizeof(zeros)));
+}
+#endif
