@@ -56,8 +56,8 @@ struct LinPlan {
   bool f16;
   int bn, bk, m_tiles, count;
   struct Layer {
-    int n_tiles, splits, kcps, lora_chunks;
-    size_t t_off, x16_off, p_off, part_off, cnt_off;
+    int n_tiles, splits, kcps, lora_chunks, lora_ks;
+    size_t t_off, x16_off, p_off, part_off, tpart_off, cnt_off, ticket_off;
   } l[kMaxW4Layers];
   size_t cnt_begin, cnt_bytes, total;
 };
@@ -128,11 +128,18 @@ LinPlan plan_linear(int64_t M, const LinIn* in, int count) {
     if (p.f16) off += round_up(static_cast<size_t>(M) * 4);
     L.part_off = off;
     if (L.splits > 1) off += round_up(static_cast<size_t>(L.splits) * M * in[j].N * 4);
+    // LoRA down projection: fp32 partials over 512-wide K slices
+    L.lora_ks = static_cast<int>((in[j].K + 511) / 512);
+    L.tpart_off = off;
+    if (in[j].r > 0 && p.f16) off += round_up(static_cast<size_t>(L.lora_ks) * M * in[j].r * 4);
   }
+  // split-K tile counters and LoRA tickets: one block, zeroed per call
   p.cnt_begin = off;
   for (int j = 0; j < count; ++j) {
     p.l[j].cnt_off = off;
     off += static_cast<size_t>(p.m_tiles) * p.l[j].n_tiles * 4;
+    p.l[j].ticket_off = off;
+    off += static_cast<size_t>((in[j].r + 7) / 8) * 4;
   }
   p.cnt_bytes = off - p.cnt_begin;
   p.total = round_up(off) + kAlign;
@@ -167,6 +174,8 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
   // layers with K == 0 produce zeros; layers with N == 0 produce nothing
   W4Params p{};
   PrepBatch pb{};
+  LoraDownBatch lb{};
+  lb.status = dev_status;
   p.status = dev_status;
   bool any_split = false;
   for (int j = 0; j < count; ++j) {
@@ -180,7 +189,23 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
     __nv_bfloat16* tbuf = reinterpret_cast<__nv_bfloat16*>(ws + pj.t_off);
     __half* x16 = reinterpret_cast<__half*>(ws + pj.x16_off);
     int* pexp = reinterpret_cast<int*>(ws + pj.p_off);
-    if (pl.f16 || a.r > 0) {
+    if (!pl.f16 && a.r > 0) {
+      // many tokens: the LoRA down projection runs on the tensor cores
+      LoraDownLayer& ld = lb.l[lb.count++];
+      if (!make_tmap_2d(&ld.tx, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, M, a.K, a.K * 2, 128, 64,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !make_tmap_2d(&ld.ta, a.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.r, a.K, a.K * 2, (a.r + 15) / 16 * 16, 64,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+        return QRR_ERR_CUDA;
+      ld.t = tbuf;
+      ld.tensor_scale = a.tensor_scale;
+      ld.M = static_cast<int>(M);
+      ld.K = static_cast<int>(a.K);
+      ld.r = a.r;
+      ld.R = (a.r + 15) / 16 * 16;
+      ld.t_cols = 64 * pj.lora_chunks;
+      ld.lora_scale = a.alpha / static_cast<float>(a.r);
+    } else if (pl.f16) {
       PrepArgs& pa = pb.a[pb.count++];
       pa.x = static_cast<const uint16_t*>(a.x);
       pa.A = static_cast<const uint16_t*>(a.A);
@@ -194,6 +219,9 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
       pa.t_cols = 64 * pj.lora_chunks;
       pa.lora_scale = a.r > 0 ? a.alpha / static_cast<float>(a.r) : 0.0f;
       pa.status = dev_status;
+      pa.tpart = reinterpret_cast<float*>(ws + pj.tpart_off);
+      pa.tickets = reinterpret_cast<uint32_t*>(ws + pj.ticket_off);
+      pa.ks = pj.lora_ks;
     }
     W4Layer& L = p.layer[p.count++];
     const void* xsrc = pl.f16 ? static_cast<const void*>(x16) : a.x;
@@ -227,11 +255,12 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
     L.m_tiles = pl.m_tiles;
     L.splits = pj.splits;
     L.kcps = pj.kcps;
-    any_split = any_split || pj.splits > 1;
+    any_split = any_split || pj.splits > 1 || a.r > 0;
   }
   if (p.count == 0) return QRR_OK;
   if (any_split && cudaMemsetAsync(ws + pl.cnt_begin, 0, pl.cnt_bytes, s) != cudaSuccess) return QRR_ERR_CUDA;
   if (pb.count > 0 && launch_lora_prep(pb, pl.f16, s) != cudaSuccess) return QRR_ERR_CUDA;
+  if (lb.count > 0 && launch_lora_down_tc(lb, s) != cudaSuccess) return QRR_ERR_CUDA;
   return from_cuda(launch_w4a16_tc(p, pl.bn, pl.f16, s));
 }
 

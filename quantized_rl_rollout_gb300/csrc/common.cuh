@@ -89,6 +89,37 @@ struct Pow2Scaler {
   __device__ __forceinline__ float operator()(float x) const { return __fmul_rn(__fmul_rn(x, f1), f2); }
 };
 
+// ---- correctly rounded division by a value shared across many numerators ----
+//
+// x / d rounded to nearest-even in fp32 with FMA corrections (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990): with y = RN(1/d) and q an
+// approximation of x/d within one ulp, the residual r = x - d q is exact
+// under an FMA and RN(q + r y) = RN(x / d).  Here q0 = RN(x y) can miss by a
+// little more than an ulp, so one correction first makes it faithful
+// (q1 = RN(q0 + r0 y)) and a second gives the correctly rounded quotient.
+// The residuals stay exact while d (and so y) lies in [1e-20, 1e20]: every
+// quotient that can reach a nonzero E2M1 / E4M3 code (|x/d| >= 2^-10) then
+// has |x| >= 1e-23 and its residuals are far from the subnormal range.
+// Outside that range the divisor falls back to __fdiv_rn.  The divisor is
+// positive; the quotient takes the numerator's sign, which keeps -0 / d = -0
+// (the FMA corrections alone would turn it into +0).
+struct SharedDivisor {
+  float d, y;
+  bool ok;
+  __device__ __forceinline__ explicit SharedDivisor(float d_) : d(d_) {
+    y = __frcp_rn(d_);
+    const float ad = fabsf(d_);
+    ok = ad >= 1.0e-20f && ad <= 1.0e20f;
+  }
+  __device__ __forceinline__ float operator()(float x) const {
+    if (!ok) return __fdiv_rn(x, d);
+    const float q0 = __fmul_rn(x, y);
+    const float q1 = __fmaf_rn(__fmaf_rn(-q0, d, x), y, q0);
+    return copysignf(__fmaf_rn(__fmaf_rn(-q1, d, x), y, q1), x);
+  }
+};
+
 __device__ __forceinline__ void flag(int32_t* status, int32_t bit) {
   if (status) atomicOr(status, bit);
 }

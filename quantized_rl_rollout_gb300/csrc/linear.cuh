@@ -58,17 +58,23 @@ struct W4Params {
   int32_t* status;
 };
 
+// Prologue of one layer: x -> f16 rows (f16 path) and the LoRA down
+// projection t = x . A^T, split over 512-wide K slices whose fp32 partials
+// the last slice of each rank group sums in slice order into t'.
 struct PrepArgs {
   const uint16_t* x;  // bf16 [M, K]
   const uint16_t* A;  // bf16 [r, K]
   const float* tensor_scale;
   __half* x16;          // f16 [M, K] (f16 path)
   int* pexp;            // [M] (f16 path)
-  __nv_bfloat16* t;     // [M, t_cols]
+  __nv_bfloat16* t;     // [M, t_cols]: (high, low) bf16 of (alpha/r) t / g per rank
+  float* tpart;         // [ks, M, r] fp32 partials
+  uint32_t* tickets;    // [ceil(r/8)], zero before the launch
   int64_t M, K;
-  int r, t_cols;
+  int r, t_cols, ks;
   float lora_scale;
   int32_t* status;
+  int first_cta;  // this layer's first CTA in the launch
 };
 
 struct PrepBatch {
@@ -76,9 +82,28 @@ struct PrepBatch {
   int count;
 };
 
+// Tensor-core LoRA down projection for many tokens (lora_tc.cu).
+struct LoraDownLayer {
+  CUtensorMap tx;  // x bf16 [M, K], box [128, 64], 128 B swizzle
+  CUtensorMap ta;  // LoRA A bf16 [r, K], box [R, 64], 128 B swizzle
+  __nv_bfloat16* t;  // [M, t_cols]
+  const float* tensor_scale;
+  int M, K, r, R, t_cols;  // R: r rounded up to a multiple of 16
+  float lora_scale;
+  int first_cta;
+};
+
+struct LoraDownBatch {
+  LoraDownLayer l[kMaxW4Layers];
+  int count;
+  int32_t* status;
+};
+
+cudaError_t launch_lora_down_tc(LoraDownBatch& b, cudaStream_t stream);
+
 int w4_bn_for(int64_t M);
 int w4_bk_for(int64_t M);
-cudaError_t launch_lora_prep(const PrepBatch& b, bool f16, cudaStream_t stream);
+cudaError_t launch_lora_prep(PrepBatch& b, bool f16, cudaStream_t stream);
 cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, cudaStream_t stream);
 
 struct Fp8GemmArgs {

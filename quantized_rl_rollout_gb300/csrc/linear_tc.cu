@@ -25,9 +25,10 @@
 //               values per stage stored to a TMEM ring of A stages
 //
 // LoRA is folded into the same accumulator as extra K columns: the prologue
-// writes t' = (alpha/r) t / (g 2^p) (t = x . A^T, g = s_t or 1, 2^p the
-// per-token pre-scale below) as interleaved bf16 (high, low) pairs; the
-// matching A columns hold (B_j, B_j).  So y = g 2^p D with no separate pass.
+// writes t' = (alpha/r) t / g (t = x . A^T, g = s_t or 1) as interleaved bf16
+// (high, low) pairs, the f16 path scales each token row of that tile by its
+// pre-scale 2^-p in shared memory, and the matching A columns hold
+// (B_j, B_j).  So y = g 2^p D with no separate pass.
 //
 // Operand type.  Prefill (many tokens) feeds bf16 x directly and dequantizes
 // to bf16.  Decode (<= 64 tokens, HBM-bound) feeds f16: the prologue rescales
@@ -123,6 +124,24 @@ __device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t two) {
   return r;
 }
 
+// Four E4M3 bytes -> two f16x2 (bytes 0,1 and bytes 2,3), one unpack.
+__device__ __forceinline__ void f16x2x2_from_e4m3x4(uint32_t four, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, h0;\n\tcvt.rn.f16x2.e4m3x2 %1, h1;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four));
+}
+
+// Eight E2M1 codes (one word, code k in nibble k) -> four f16x2 (pairs 0-1,
+// 2-3, 4-5, 6-7), one byte unpack feeding four hardware conversions.
+__device__ __forceinline__ void f16x2x4_from_e2m1x8(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+}
+
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -142,27 +161,31 @@ __device__ __forceinline__ float f16_hi_to_f32(uint32_t h2) { return __half2floa
 template <bool F16>
 __device__ __forceinline__ void dequant64(const uint32_t* w, uint32_t scales4, uint32_t* out) {
   if constexpr (F16) {
-    const uint32_t s01 = f16x2_from_e4m3x2(scales4 & 0xFFFFu), s23 = f16x2_from_e4m3x2(scales4 >> 16);
+    uint32_t s01, s23;
+    f16x2x2_from_e4m3x4(scales4, s01, s23);
     const uint32_t sg[4] = {__byte_perm(s01, 0, 0x1010), __byte_perm(s01, 0, 0x3232), __byte_perm(s23, 0, 0x1010),
                             __byte_perm(s23, 0, 0x3232)};
 #pragma unroll
     for (int g = 0; g < 4; ++g)
 #pragma unroll
-      for (int q = 0; q < 2; ++q)
+      for (int q = 0; q < 2; ++q) {
+        uint32_t h[4];
+        f16x2x4_from_e2m1x8(w[2 * g + q], h);
 #pragma unroll
-        for (int b = 0; b < 4; ++b)
-          out[8 * g + 4 * q + b] = hmul2(f16x2_from_e2m1x2(w[2 * g + q] >> (8 * b)), sg[g]);
+        for (int b = 0; b < 4; ++b) out[8 * g + 4 * q + b] = hmul2(h[b], sg[g]);
+      }
   } else {
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       const float sv = e4m3_to_f32((scales4 >> (8 * g)) & 0xFFu);
 #pragma unroll
-      for (int q = 0; q < 2; ++q)
+      for (int q = 0; q < 2; ++q) {
+        uint32_t h[4];
+        f16x2x4_from_e2m1x8(w[2 * g + q], h);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const uint32_t h2 = f16x2_from_e2m1x2(w[2 * g + q] >> (8 * b));
-          out[8 * g + 4 * q + b] = pack_bf16x2(f16_lo_to_f32(h2) * sv, f16_hi_to_f32(h2) * sv);
-        }
+        for (int b = 0; b < 4; ++b)
+          out[8 * g + 4 * q + b] = pack_bf16x2(f16_lo_to_f32(h[b]) * sv, f16_hi_to_f32(h[b]) * sv);
+      }
     }
   }
 }
@@ -349,13 +372,21 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
           tmem_ld16(tmem + lane_addr + db * C::D_COLS, r);
         else
           tmem_ld32(tmem + lane_addr + db * C::D_COLS + 32 * cc, r);
+        // the per-token factors of this slab first: y / partial stores may
+        // alias the exponent array as far as the compiler knows, so loads
+        // interleaved with the stores would run one after another
+        float sc2[CW];
+#pragma unroll
+        for (int i = 0; i < CW; ++i) {
+          const int m = m0 + CW * cc + i;
+          sc2[i] = (L.pexp && m < L.M) ? __fmul_rn(g, pow2_from_exp(__ldg(L.pexp + m))) : g;
+        }
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < CW; ++i) {
           const int m = m0 + CW * cc + i;
           if (m < L.M) {
-            const float sc2 = L.pexp ? __fmul_rn(g, pow2_from_exp(L.pexp[m])) : g;
-            const float v = __uint_as_float(r[i]) * sc2;
+            const float v = __uint_as_float(r[i]) * sc2[i];
             if (part)
               part[static_cast<int64_t>(m) * L.N + n] = v;
             else
@@ -479,6 +510,28 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
               tmem_st32(a_addr + 32 * h, out);
             }
           } else {
+            if constexpr (F16) {
+              // t' holds (alpha/r) t / g; the f16 path's accumulator carries
+              // the per-token factor 2^-p_m, so scale this chunk's t' rows by
+              // it (exact) before the tensor core reads them
+              const int tig = q * 32 + lane;
+              constexpr int PIECES = (C::ACH / 64) * BN * 8;
+              const int m0 = mt * BN;
+              for (int idx = tig; idx < PIECES; idx += 128) {
+                const int sub = idx / (BN * 8), rem = idx % (BN * 8), mr = rem >> 3;
+                if (m0 + mr >= L.M) continue;
+                uint4* pc = reinterpret_cast<uint4*>(const_cast<uint8_t*>(stage) +
+                                                     (hc * (C::ACH / 64) + sub) * C::X_SUB + mr * 128 +
+                                                     (rem & 7) * 16);
+                const Pow2Scaler sc(L.pexp[m0 + mr]);
+                uint4 v = *pc;
+                uint32_t* wv = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) wv[e] = pack_bf16x2(sc(bf16_lo(wv[e])), sc(bf16_hi(wv[e])));
+                *pc = v;
+              }
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
             // LoRA chunk: A word i holds (B[n, rb+i], B[n, rb+i]) against the
             // (high, low) halves of t'; zero past rank r
             const int rb = (c - nk) * (BK / 2) + hc * (C::ACH / 2);
@@ -522,23 +575,31 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
 }
 
 // ---------------------------------------------------------------------------
-// Prologue: one CTA per (token row m, group of 8 LoRA ranks).
-//   F16: p_m so that max|x_m| 2^-p_m is in [2^14, 2^15); x16 = f16(x 2^-p_m)
-//        (written by the rank-group-0 CTA; every CTA derives p_m itself)
-//   LoRA: t_j = sum_k x[m,k] A[j,k] (fp32); v = (alpha/r) t_j / (g 2^p_m);
-//         t'[m, 2j] = bf16(v), t'[m, 2j + 1] = bf16(v - bf16(v)); zero to t_cols.
+// Prologue.  Per layer, CTAs of two kinds:
+//   x rows (f16 path): p_m so that max|x_m| 2^-p_m is in [2^14, 2^15) and
+//     x16 = f16(x 2^-p_m), one CTA per token row;
+//   LoRA slices: one CTA per (group of 8 ranks, 512-wide K slice) computes the
+//     fp32 partial dot products of every token with its ranks; the last slice
+//     of a rank group to finish (a ticket) sums the partials in slice order,
+//     t_j = sum_k x[m,k] A[j,k], and writes t'[m, 2j] = bf16(v),
+//     t'[m, 2j + 1] = bf16(v - bf16(v)) for v = (alpha/r) t_j / g (g = s_t,
+//     or 1 when s_t = 0).  The per-token 2^-p_m of the f16 path is applied to
+//     the t' tile inside the GEMM, so the two kinds do not depend on each other.
 template <bool F16>
 __global__ void __launch_bounds__(256) lora_prep_kernel(const __grid_constant__ PrepBatch batch) {
-  __shared__ float red[8][8];
   __shared__ uint32_t amax_s[8];
-  const PrepArgs& a = batch.a[blockIdx.z];
-  const int m = blockIdx.x, rg = blockIdx.y;
-  if (rg > 0 && 8 * rg >= a.r) return;  // this layer has fewer rank groups
+  __shared__ int last_s;
+  int j = 0;
+  while (j + 1 < batch.count && batch.a[j + 1].first_cta <= static_cast<int>(blockIdx.x)) ++j;
+  const PrepArgs& a = batch.a[j];
+  int local = static_cast<int>(blockIdx.x) - a.first_cta;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint4* xr = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(m) * a.K);
   const int nvec = static_cast<int>(a.K / 8);
-  int pexp = 0;
-  if constexpr (F16) {
+  const int nx = F16 ? static_cast<int>(a.M) : 0;
+  if (local < nx) {
+    // ---- x row -> f16 with its power-of-two pre-scale ----
+    const int m = local;
+    const uint4* xr = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(m) * a.K);
     uint32_t mx = 0;
     for (int v = threadIdx.x; v < nvec; v += 256) mx = max(mx, absmax_bits8(__ldg(xr + v)));
     mx = __reduce_max_sync(0xFFFFFFFFu, mx);
@@ -547,82 +608,105 @@ __global__ void __launch_bounds__(256) lora_prep_kernel(const __grid_constant__ 
     mx = amax_s[0];
 #pragma unroll
     for (int i = 1; i < 8; ++i) mx = max(mx, amax_s[i]);
+    int pexp = 0;
     if (mx != 0u) {
       int e;
       frexpf(bf16bits_to_f32(mx), &e);  // amax = f 2^e, 0.5 <= f < 1
       pexp = e - 15;                    // amax 2^-p in [2^14, 2^15)
     }
-    if (rg == 0) {
-      if (mx >= 0x7F80u && threadIdx.x == 0) flag(a.status, QRR_DEV_NONFINITE);
-      if (threadIdx.x == 0) a.pexp[m] = pexp;
-      const Pow2Scaler sc(pexp);
-      uint4* x16 = reinterpret_cast<uint4*>(a.x16 + static_cast<int64_t>(m) * a.K);
-      for (int v = threadIdx.x; v < nvec; v += 256) {
-        const uint4 xv = __ldg(xr + v);
-        const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
-        uint32_t o[4];
+    if (mx >= 0x7F80u && threadIdx.x == 0) flag(a.status, QRR_DEV_NONFINITE);
+    if (threadIdx.x == 0) a.pexp[m] = pexp;
+    const Pow2Scaler sc(pexp);
+    uint4* x16 = reinterpret_cast<uint4*>(a.x16 + static_cast<int64_t>(m) * a.K);
+    for (int v = threadIdx.x; v < nvec; v += 256) {
+      const uint4 xv = __ldg(xr + v);
+      const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+      uint32_t o[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const __half2 h = __floats2half2_rn(sc(bf16_lo(w[i])), sc(bf16_hi(w[i])));
-          o[i] = *reinterpret_cast<const uint32_t*>(&h);
+      for (int i = 0; i < 4; ++i) {
+        const __half2 h = __floats2half2_rn(sc(bf16_lo(w[i])), sc(bf16_hi(w[i])));
+        o[i] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      x16[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    return;
+  }
+  local -= nx;
+  // ---- LoRA slice: ranks [8 rg, 8 rg + 8), vectors [64 ks, 64 ks + 64) ----
+  const int rg = local / a.ks, kslice = local % a.ks;
+  const int j0 = rg * 8, nj = min(8, a.r - j0);
+  const int v0 = kslice * 64, v1 = min(nvec, v0 + 64);
+  // each lane holds two 8-element vectors of the 8 A rows
+  uint4 av[2][8];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int v = v0 + lane + 32 * h;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      av[h][i] = (v < v1 && i < nj)
+                     ? __ldg(reinterpret_cast<const uint4*>(a.A + static_cast<int64_t>(j0 + i) * a.K) + v)
+                     : make_uint4(0, 0, 0, 0);
+  }
+  for (int m = warp; m < a.M; m += 8) {
+    const uint4* xr = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(m) * a.K);
+    float d[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = 0.0f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int v = v0 + lane + 32 * h;
+      const uint4 xv = v < v1 ? __ldg(xr + v) : make_uint4(0, 0, 0, 0);
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t aw[4] = {av[h][i].x, av[h][i].y, av[h][i].z, av[h][i].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          d[i] = fmaf(bf16_lo(xw[q]), bf16_lo(aw[q]), d[i]);
+          d[i] = fmaf(bf16_hi(xw[q]), bf16_hi(aw[q]), d[i]);
         }
-        x16[v] = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
-  }
-  if (a.r == 0) return;
-  const int j0 = rg * 8;
-  const int nj = min(8, a.r - j0);
-  float part[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) part[i] = 0.0f;
-  const uint4* arow = reinterpret_cast<const uint4*>(a.A + static_cast<int64_t>(j0) * a.K);
-  for (int v = threadIdx.x; v < nvec; v += 256) {
-    // issue every load of this step before any arithmetic
-    const uint4 xv = __ldg(xr + v);
-    uint4 av8[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) av8[i] = i < nj ? __ldg(arow + static_cast<int64_t>(i) * nvec + v) : make_uint4(0, 0, 0, 0);
-    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint4 av = av8[i];
-      const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
-      float s = part[i];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        s = fmaf(bf16_lo(xw[q]), bf16_lo(aw[q]), s);
-        s = fmaf(bf16_hi(xw[q]), bf16_hi(aw[q]), s);
-      }
-      part[i] = s;
+      for (int o = 16; o >= 1; o >>= 1) d[i] += __shfl_xor_sync(0xFFFFFFFFu, d[i], o);
+    }
+    if (lane < nj) {
+      float mine = d[0];
+#pragma unroll
+      for (int i = 1; i < 8; ++i)
+        if (lane == i) mine = d[i];
+      a.tpart[(static_cast<int64_t>(kslice) * a.M + m) * a.r + j0 + lane] = mine;
     }
   }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) part[i] += __shfl_xor_sync(0xFFFFFFFFu, part[i], o);
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) red[warp][i] = part[i];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t prev = atomicAdd(a.tickets + rg, 1u);
+    last_s = prev == static_cast<uint32_t>(a.ks - 1);
+    if (last_s) __threadfence();
   }
   __syncthreads();
-  __nv_bfloat16* trow = a.t + static_cast<int64_t>(m) * a.t_cols;
-  if (threadIdx.x < nj) {
+  if (!last_s) return;
+  const float st = *a.tensor_scale;
+  const float g = st > 0.0f ? st : 1.0f;
+  for (int idx = threadIdx.x; idx < a.M * nj; idx += 256) {
+    const int m = idx / nj, i = idx % nj;
     float t = 0.0f;
-#pragma unroll
-    for (int w2 = 0; w2 < 8; ++w2) t += red[w2][threadIdx.x];
-    const float st = *a.tensor_scale;
-    const float g = st > 0.0f ? st : 1.0f;
-    // (alpha/r) t / (g 2^p): divide by g, then scale by the power of two
-    const float v = Pow2Scaler(pexp)(__fdiv_rn(a.lora_scale * t, g));
+    for (int s2 = 0; s2 < a.ks; ++s2) t += __ldcg(a.tpart + (static_cast<int64_t>(s2) * a.M + m) * a.r + j0 + i);
+    const float v = __fdiv_rn(a.lora_scale * t, g);
     const __nv_bfloat16 hi = __float2bfloat16_rn(v);
     const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-    trow[2 * (j0 + threadIdx.x)] = hi;
-    trow[2 * (j0 + threadIdx.x) + 1] = lo;
+    __nv_bfloat16* trow = a.t + static_cast<int64_t>(m) * a.t_cols;
+    trow[2 * (j0 + i)] = hi;
+    trow[2 * (j0 + i) + 1] = lo;
   }
-  if (rg == 0)
-    for (int j = 2 * a.r + threadIdx.x; j < a.t_cols; j += 256) trow[j] = __float2bfloat16_rn(0.0f);
+  if (rg == 0) {
+    const int pad = a.t_cols - 2 * a.r;
+    for (int idx = threadIdx.x; idx < a.M * pad; idx += 256)
+      a.t[static_cast<int64_t>(idx / pad) * a.t_cols + 2 * a.r + idx % pad] = __float2bfloat16_rn(0.0f);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -657,15 +741,19 @@ int w4_bn_for(int64_t M) {
 // scales staged by TMA); prefill tiles use 64-wide stages.
 int w4_bk_for(int64_t M) { return M <= 64 ? 256 : 64; }
 
-cudaError_t launch_lora_prep(const PrepBatch& b, bool f16, cudaStream_t stream) {
+cudaError_t launch_lora_prep(PrepBatch& b, bool f16, cudaStream_t stream) {
   if (b.count == 0 || b.a[0].M == 0) return cudaSuccess;
-  int groups = 1;
-  for (int j = 0; j < b.count; ++j) groups = max(groups, (b.a[j].r + 7) / 8);
-  const dim3 grid(static_cast<unsigned>(b.a[0].M), static_cast<unsigned>(groups), static_cast<unsigned>(b.count));
+  int ctas = 0;
+  for (int j = 0; j < b.count; ++j) {
+    PrepArgs& a = b.a[j];
+    a.first_cta = ctas;
+    ctas += (f16 ? static_cast<int>(a.M) : 0) + (a.r > 0 ? ((a.r + 7) / 8) * a.ks : 0);
+  }
+  if (ctas == 0) return cudaSuccess;
   if (f16)
-    lora_prep_kernel<true><<<grid, 256, 0, stream>>>(b);
+    lora_prep_kernel<true><<<ctas, 256, 0, stream>>>(b);
   else
-    lora_prep_kernel<false><<<grid, 256, 0, stream>>>(b);
+    lora_prep_kernel<false><<<ctas, 256, 0, stream>>>(b);
   return cudaGetLastError();
 }
 

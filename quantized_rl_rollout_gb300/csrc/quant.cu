@@ -21,27 +21,42 @@ namespace qrr {
 // NVFP4 pass 1: tensor absmax.  A block's absmax is the max of |bf16| bit
 // patterns; `amax_bits[j]` must be zero before the launch.
 
+// Each warp keeps a running max over the chunks it visits and publishes it
+// with one atomic per tensor it leaves (not one per chunk: same-address
+// atomics serialize in L2).
 __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __grid_constant__ Nvfp4Batch batch) {
   const int64_t chunks = batch.total_amax_chunks;
+  int cur = -1;
+  uint32_t run = 0;
+  auto publish = [&]() {
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, run);
+    if ((threadIdx.x & 31) == 0 && m) {
+      atomicMax(batch.amax_bits + cur, m);
+      if (m >= 0x7F80u) flag(batch.status, QRR_DEV_NONFINITE);
+    }
+    run = 0;
+  };
   for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x) {
     int j = 0;
     while (j + 1 < batch.count && batch.job[j + 1].first_amax_chunk <= c) ++j;
+    if (j != cur) {
+      if (cur >= 0) publish();
+      cur = j;
+    }
     const Nvfp4Job& job = batch.job[j];
     const int64_t nvec = job.N * job.K / 8;  // uint4 of 8 bf16
     const int64_t base = (c - job.first_amax_chunk) * kAmaxChunkVecs;
     const uint4* src = reinterpret_cast<const uint4*>(job.W);
-    uint32_t m = 0;
+    uint4 v[kAmaxChunkVecs / 256];
 #pragma unroll
     for (int u = 0; u < kAmaxChunkVecs / 256; ++u) {
       const int64_t i = base + u * 256 + threadIdx.x;
-      if (i < nvec) m = max(m, absmax_bits8(__ldg(src + i)));
+      v[u] = i < nvec ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
     }
-    m = __reduce_max_sync(0xFFFFFFFFu, m);
-    if ((threadIdx.x & 31) == 0 && m) {
-      atomicMax(batch.amax_bits + j, m);
-      if (m >= 0x7F80u) flag(batch.status, QRR_DEV_NONFINITE);
-    }
+#pragma unroll
+    for (int u = 0; u < kAmaxChunkVecs / 256; ++u) run = max(run, absmax_bits8(v[u]));
   }
+  if (cur >= 0) publish();
 }
 
 // NVFP4 pass 2: encode.  One thread per 16-element block; block b of a tensor
@@ -69,12 +84,13 @@ __global__ void __launch_bounds__(256) nvfp4_encode_kernel(const __grid_constant
       sb = cvt_e4m3x2(__fdiv_rn(amax_b, six_st), 0.0f) & 0xFFu;
       const float d = __fmul_rn(e4m3_to_f32(sb), s_t);
       if (d > 0.0f) {
+        const SharedDivisor div(d);  // 16 quotients x / d, each correctly rounded
         const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
         uint32_t out[2] = {0u, 0u};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float q0 = __fdiv_rn(bf16_lo(w[i]), d);
-          const float q1 = __fdiv_rn(bf16_hi(w[i]), d);
+          const float q0 = div(bf16_lo(w[i]));
+          const float q1 = div(bf16_hi(w[i]));
           out[i >> 2] |= cvt_e2m1x2(q0, q1) << (8 * (i & 3));
         }
         packed = make_uint2(out[0], out[1]);
@@ -114,9 +130,9 @@ __global__ void __launch_bounds__(256) fp8_a1x128_kernel(const uint16_t* __restr
     if (v448 > 0.0f) {
       if (mode == QRR_SCALE_FP32) {
         s = v448;
+        const SharedDivisor div(s);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          out[k >> 1] |= cvt_e4m3x2(__fdiv_rn(bf16_lo(w[k]), s), __fdiv_rn(bf16_hi(w[k]), s)) << (16 * (k & 1));
+        for (int k = 0; k < 4; ++k) out[k >> 1] |= cvt_e4m3x2(div(bf16_lo(w[k])), div(bf16_hi(w[k]))) << (16 * (k & 1));
       } else {
         const int e = pow2_ceil_exp(v448);
         s = pow2_from_exp(e);
@@ -181,6 +197,7 @@ __global__ void __launch_bounds__(256) fp8_w128_kernel(const __grid_constant__ F
     }
     if (threadIdx.x == 0) job.scales[tr * kt + tc] = s;
     const Pow2Scaler sc(e);
+    const SharedDivisor div(s > 0.0f ? s : 1.0f);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int64_t row = row0 + u * 16 + (threadIdx.x >> 4);
@@ -190,8 +207,8 @@ __global__ void __launch_bounds__(256) fp8_w128_kernel(const __grid_constant__ F
       if (s > 0.0f) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float a = batch.mode == QRR_SCALE_FP32 ? __fdiv_rn(bf16_lo(w[k]), s) : sc(bf16_lo(w[k]));
-          const float b = batch.mode == QRR_SCALE_FP32 ? __fdiv_rn(bf16_hi(w[k]), s) : sc(bf16_hi(w[k]));
+          const float a = batch.mode == QRR_SCALE_FP32 ? div(bf16_lo(w[k])) : sc(bf16_lo(w[k]));
+          const float b = batch.mode == QRR_SCALE_FP32 ? div(bf16_hi(w[k])) : sc(bf16_hi(w[k]));
           out[k >> 1] |= cvt_e4m3x2(a, b) << (16 * (k & 1));
         }
       }

@@ -174,3 +174,58 @@ def test_fp8_degenerate(q):
         torch.cuda.synchronize()
         rq, rs = oracle.fp8.quantize_a1x128(to_np(x), mode)
         assert np.array_equal(sa.cpu().numpy(), rs) and np.array_equal(qa.cpu().numpy(), rq)
+
+
+def _bf16_neighbours(v):
+    """bf16 values at, just below and just above each float in v."""
+    b = torch.from_numpy(np.asarray(v, np.float32)).to(torch.bfloat16)
+    bits = b.view(torch.int16).to(torch.int32)
+    out = [bits, bits + 1, bits - 1]
+    return torch.cat(out).to(torch.int16).view(torch.bfloat16).float().numpy()
+
+
+def test_fp8_quotients_at_midpoints(q):
+    """Elements placed on bf16 neighbours of every E4M3 midpoint times the
+    block scale: the division and the tie rule decide every code."""
+    g = np.random.default_rng(11)
+    grid = formats.E4M3_VALUES[:127]
+    mids = (grid[1:] + grid[:-1]) / 2
+    rows = []
+    for _ in range(64):
+        c = float(torch.tensor(g.uniform(0.01, 100.0), dtype=torch.bfloat16).float())  # block scale s = c
+        vals = _bf16_neighbours(mids * c)
+        vals = vals[np.abs(vals) < 448 * c]
+        sgn = np.where(g.random(vals.size) < 0.5, -1.0, 1.0)
+        row = np.concatenate([[448 * c], vals * sgn]).astype(np.float32)
+        row = np.resize(row, 128 * ((row.size + 127) // 128))
+        row[0::128] = 448 * c  # every 1x128 block keeps its absmax, so s = c exactly
+        rows.append(row[:512])
+    x = torch.from_numpy(np.stack(rows)).to(torch.bfloat16).to(DEV)
+    qa, sa = q.quantize_fp8_a1x128(x, 0)
+    torch.cuda.synchronize()
+    rq, rs = oracle.fp8.quantize_a1x128(to_np(x), 0)
+    assert np.array_equal(sa.cpu().numpy(), rs)
+    assert np.array_equal(qa.cpu().numpy(), rq)
+
+
+def test_nvfp4_quotients_at_midpoints(q):
+    """Blocks whose elements sit on bf16 neighbours of E2M1 midpoints times
+    the block's own divisor d_b (absmax kept, so s_t and d_b do not move)."""
+    g = np.random.default_rng(12)
+    W0 = inputs.weight(256, 512, 99, device=DEV)
+    w0 = to_np(W0)
+    c0, s0, t0 = oracle.nvfp4.quantize(w0)
+    d = formats.e4m3_value(s0) * np.float64(t0)  # [256, 32]
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    w1 = w0.copy().reshape(256, 32, 16)
+    amax_pos = np.argmax(np.abs(w1), axis=-1)
+    for n in range(256):
+        for b in range(32):
+            cand = _bf16_neighbours(mids * d[n, b])
+            picks = g.choice(cand, 16) * np.where(g.random(16) < 0.5, -1.0, 1.0)
+            keep = w1[n, b, amax_pos[n, b]]
+            picks = np.where(np.abs(picks) < abs(keep), picks, 0.0)
+            w1[n, b] = picks
+            w1[n, b, amax_pos[n, b]] = keep
+    W1 = torch.from_numpy(w1.reshape(256, 512).astype(np.float32)).to(torch.bfloat16).to(DEV)
+    _check_nvfp4(q, W1)
