@@ -406,6 +406,7 @@ def main():
     torch.cuda.set_device(device)
     phases = [p for p in args.phases.split(",") if p]
     w = Workload(qrr, device)
+    w.requant()  # valid NVFP4 weights for every phase, whichever phases run
     # warm-up (untimed)
     for _ in range(warmup):
         for p in phases:

@@ -56,7 +56,7 @@ struct LinPlan {
   bool f16;
   int bn, bk, m_tiles, count;
   struct Layer {
-    int n_tiles, splits, kcps, lora_chunks, lora_ks;
+    int n_tiles, splits, kcps, lora_chunks, lora_ks, lora_slice;
     size_t t_off, x16_off, p_off, part_off, tpart_off, cnt_off, ticket_off;
   } l[kMaxW4Layers];
   size_t cnt_begin, cnt_bytes, total;
@@ -128,10 +128,13 @@ LinPlan plan_linear(int64_t M, const LinIn* in, int count) {
     if (p.f16) off += round_up(static_cast<size_t>(M) * 4);
     L.part_off = off;
     if (L.splits > 1) off += round_up(static_cast<size_t>(L.splits) * M * in[j].N * 4);
-    // LoRA down projection: fp32 partials over 512-wide K slices
-    L.lora_ks = static_cast<int>((in[j].K + 511) / 512);
+    // decode LoRA down projection: fp32 partials over K slices, narrow for a
+    // token or a few (many CTAs, one wave), wider for more tokens (fewer
+    // partials for the last slice to sum)
+    L.lora_slice = M <= 16 ? 512 : 2048;
+    L.lora_ks = static_cast<int>((in[j].K + L.lora_slice - 1) / L.lora_slice);
     L.tpart_off = off;
-    if (in[j].r > 0 && p.f16) off += round_up(static_cast<size_t>(L.lora_ks) * M * in[j].r * 4);
+    if (in[j].r > 0 && p.f16) off += round_up(static_cast<size_t>((L.lora_ks + 3) & ~3) * M * in[j].r * 4);
   }
   // split-K tile counters and LoRA tickets: one block, zeroed per call
   p.cnt_begin = off;
@@ -139,7 +142,7 @@ LinPlan plan_linear(int64_t M, const LinIn* in, int count) {
     p.l[j].cnt_off = off;
     off += static_cast<size_t>(p.m_tiles) * p.l[j].n_tiles * 4;
     p.l[j].ticket_off = off;
-    off += static_cast<size_t>((in[j].r + 7) / 8) * 4;
+    off += (in[j].r > 0 ? static_cast<size_t>((M + 127) / 128) : 0) * 4;  // one per 128-token tile
   }
   p.cnt_bytes = off - p.cnt_begin;
   p.total = round_up(off) + kAlign;
@@ -173,7 +176,6 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   // layers with K == 0 produce zeros; layers with N == 0 produce nothing
   W4Params p{};
-  PrepBatch pb{};
   LoraDownBatch lb{};
   lb.status = dev_status;
   p.status = dev_status;
@@ -189,39 +191,35 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
     __nv_bfloat16* tbuf = reinterpret_cast<__nv_bfloat16*>(ws + pj.t_off);
     __half* x16 = reinterpret_cast<__half*>(ws + pj.x16_off);
     int* pexp = reinterpret_cast<int*>(ws + pj.p_off);
-    if (!pl.f16 && a.r > 0) {
-      // many tokens: the LoRA down projection runs on the tensor cores
+    if (a.r > 0 || pl.f16) {
+      // prologue: the LoRA down projection on the tensor cores (decode: cut
+      // into 512-wide K slices so it runs in one wave) and the f16 image of x
       LoraDownLayer& ld = lb.l[lb.count++];
       if (!make_tmap_2d(&ld.tx, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, M, a.K, a.K * 2, 128, 64,
-                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-          !make_tmap_2d(&ld.ta, a.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.r, a.K, a.K * 2, (a.r + 15) / 16 * 16, 64,
                         CU_TENSOR_MAP_SWIZZLE_128B))
         return QRR_ERR_CUDA;
+      if (a.r > 0) {
+        if (!make_tmap_2d(&ld.ta, a.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.r, a.K, a.K * 2, (a.r + 15) / 16 * 16, 64,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+          return QRR_ERR_CUDA;
+      } else {
+        ld.ta = ld.tx;  // never read without an adapter
+      }
       ld.t = tbuf;
       ld.tensor_scale = a.tensor_scale;
+      ld.tpart = reinterpret_cast<float*>(ws + pj.tpart_off);
+      ld.tickets = reinterpret_cast<uint32_t*>(ws + pj.ticket_off);
+      ld.x = static_cast<const uint16_t*>(a.x);
+      ld.x16 = pl.f16 ? x16 : nullptr;
+      ld.pexp = pexp;
       ld.M = static_cast<int>(M);
       ld.K = static_cast<int>(a.K);
       ld.r = a.r;
       ld.R = (a.r + 15) / 16 * 16;
       ld.t_cols = 64 * pj.lora_chunks;
-      ld.lora_scale = a.alpha / static_cast<float>(a.r);
-    } else if (pl.f16) {
-      PrepArgs& pa = pb.a[pb.count++];
-      pa.x = static_cast<const uint16_t*>(a.x);
-      pa.A = static_cast<const uint16_t*>(a.A);
-      pa.tensor_scale = a.tensor_scale;
-      pa.x16 = x16;
-      pa.pexp = pexp;
-      pa.t = tbuf;
-      pa.M = M;
-      pa.K = a.K;
-      pa.r = a.r;
-      pa.t_cols = 64 * pj.lora_chunks;
-      pa.lora_scale = a.r > 0 ? a.alpha / static_cast<float>(a.r) : 0.0f;
-      pa.status = dev_status;
-      pa.tpart = reinterpret_cast<float*>(ws + pj.tpart_off);
-      pa.tickets = reinterpret_cast<uint32_t*>(ws + pj.ticket_off);
-      pa.ks = pj.lora_ks;
+      ld.ks = pl.f16 ? pj.lora_ks : 1;
+      ld.slice_steps = pl.f16 ? pj.lora_slice / 64 : static_cast<int>(a.K / 64);
+      ld.lora_scale = a.r > 0 ? a.alpha / static_cast<float>(a.r) : 0.0f;
     }
     W4Layer& L = p.layer[p.count++];
     const void* xsrc = pl.f16 ? static_cast<const void*>(x16) : a.x;
@@ -259,9 +257,8 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
   }
   if (p.count == 0) return QRR_OK;
   if (any_split && cudaMemsetAsync(ws + pl.cnt_begin, 0, pl.cnt_bytes, s) != cudaSuccess) return QRR_ERR_CUDA;
-  if (pb.count > 0 && launch_lora_prep(pb, pl.f16, s) != cudaSuccess) return QRR_ERR_CUDA;
   if (lb.count > 0 && launch_lora_down_tc(lb, s) != cudaSuccess) return QRR_ERR_CUDA;
-  return from_cuda(launch_w4a16_tc(p, pl.bn, pl.f16, s));
+  return from_cuda(launch_w4a16_tc(p, pl.bn, pl.f16, lb.count > 0, s));
 }
 
 LinIn make_in(const void* x, int64_t N, int64_t K, const uint8_t* codes, const uint8_t* scales, const float* ts,

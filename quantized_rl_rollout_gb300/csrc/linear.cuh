@@ -12,24 +12,6 @@
 
 namespace qrr {
 
-struct LinearArgs {
-  const uint16_t* x;      // bf16 [M, K]
-  const uint8_t* codes;   // [N, K/2]
-  const uint8_t* scales;  // [N, K/16] E4M3
-  const float* tensor_scale;
-  const uint16_t* A;  // bf16 [r, K] (nullable when r == 0)
-  const uint16_t* B;  // bf16 [N, r]
-  const float* t;     // fp32 [M, r] LoRA down projection (workspace)
-  void* y;            // bf16 [M, N]
-  int64_t M, N, K;
-  int r;
-  float lora_scale;  // alpha / r
-};
-
-cudaError_t launch_lora_down_simt(const void* x, const void* A, int64_t M, int64_t K, int r, float* t,
-                                  cudaStream_t stream);
-cudaError_t launch_linear_simt(const LinearArgs& a, cudaStream_t stream);
-
 // ---- tensor-core W4A16 linear (linear_tc.cu) ----
 
 constexpr int kMaxW4Layers = 8;
@@ -58,37 +40,23 @@ struct W4Params {
   int32_t* status;
 };
 
-// Prologue of one layer: x -> f16 rows (f16 path) and the LoRA down
-// projection t = x . A^T, split over 512-wide K slices whose fp32 partials
-// the last slice of each rank group sums in slice order into t'.
-struct PrepArgs {
-  const uint16_t* x;  // bf16 [M, K]
-  const uint16_t* A;  // bf16 [r, K]
-  const float* tensor_scale;
-  __half* x16;          // f16 [M, K] (f16 path)
-  int* pexp;            // [M] (f16 path)
-  __nv_bfloat16* t;     // [M, t_cols]: (high, low) bf16 of (alpha/r) t / g per rank
-  float* tpart;         // [ks, M, r] fp32 partials
-  uint32_t* tickets;    // [ceil(r/8)], zero before the launch
-  int64_t M, K;
-  int r, t_cols, ks;
-  float lora_scale;
-  int32_t* status;
-  int first_cta;  // this layer's first CTA in the launch
-};
-
-struct PrepBatch {
-  PrepArgs a[kMaxW4Layers];
-  int count;
-};
-
-// Tensor-core LoRA down projection for many tokens (lora_tc.cu).
+// Prologue of one layer (lora_tc.cu): the LoRA down projection on the tensor
+// cores into t' (ks > 1: split over K slices of slice_steps x 64 with fp32
+// partials and a ticket per 128-token tile), and, when x16 is set, the f16
+// image of x with its per-token pre-scales.
 struct LoraDownLayer {
   CUtensorMap tx;  // x bf16 [M, K], box [128, 64], 128 B swizzle
   CUtensorMap ta;  // LoRA A bf16 [r, K], box [R, 64], 128 B swizzle
   __nv_bfloat16* t;  // [M, t_cols]
   const float* tensor_scale;
+  float* tpart;        // [M, r, ks rounded up to 4] fp32 partials (ks > 1)
+  uint32_t* tickets;   // [ceil(M / 128)], zero before the launch (ks > 1)
+  const uint16_t* x;   // bf16 [M, K] (x rows)
+  __half* x16;         // f16 [M, K], or null for no x-row CTAs
+  int* pexp;           // [M]
   int M, K, r, R, t_cols;  // R: r rounded up to a multiple of 16
+  int ks, slice_steps;     // K slices and 64-wide steps per slice
+  int x_rows_per_cta;      // set by the launcher
   float lora_scale;
   int first_cta;
 };
@@ -103,8 +71,7 @@ cudaError_t launch_lora_down_tc(LoraDownBatch& b, cudaStream_t stream);
 
 int w4_bn_for(int64_t M);
 int w4_bk_for(int64_t M);
-cudaError_t launch_lora_prep(PrepBatch& b, bool f16, cudaStream_t stream);
-cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, cudaStream_t stream);
+cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, bool after_prologue, cudaStream_t stream);
 
 struct Fp8GemmArgs {
   const uint8_t* qa;  // [M, K]

@@ -14,15 +14,15 @@
 // bf16 and in f16, so the tensor core forms every product exactly and sums in
 // fp32; s_t is applied once in the epilogue.
 //
-//   warp 0      TMA: per BK-wide K stage, x [BN x BK] (128 B swizzle, in
+//   warps 0..4G-1  G dequant warpgroups taking the A chunks in turn: thread =
+//               weight row (its TMEM lane); codes and scales from shared
+//               memory, stored to a TMEM ring of A chunks
+//   warps 4G..4G+3  epilogue: D out of TMEM (double-buffered when it fits),
+//               scale, store y or a split-K partial
+//   warp 4G+4   TMA: per BK-wide K stage, x [BN x BK] (128 B swizzle, in
 //               64-wide sub-tiles), the packed codes [128 x BK/2 B] and, for
 //               BK = 256, the block scales [128 x 16 B] into an S-stage ring
-//   warp 1      MMA: BK/16 x tcgen05.mma (M128 x BN x K16) per stage, A from TMEM
-//   warps 2..5  epilogue: D out of TMEM (double-buffered when it fits), scale,
-//               store y or a split-K partial
-//   warps 6..   G dequant warpgroups taking the stages in turn: thread = weight
-//               row (its TMEM lane); codes and scales from shared memory, BK
-//               values per stage stored to a TMEM ring of A stages
+//   warp 4G+5   MMA: BK/16 x tcgen05.mma (M128 x BN x K16) per stage, A from TMEM
 //
 // LoRA is folded into the same accumulator as extra K columns: the prologue
 // writes t' = (alpha/r) t / g (t = x . A^T, g = s_t or 1) as interleaved bf16
@@ -91,9 +91,19 @@ struct Cfg {
   static constexpr int ACH = BK < 128 ? BK : 128;  // K per A chunk
   static constexpr int ACOLS = ACH / 2;
   static constexpr int CPS = BK / ACH;             // A chunks per stage
-  static constexpr int AST_RAW = (512 - A_COL) / ACOLS;
+  // A slot of chunk c is rewritten for chunk c + AST once the stage of chunk
+  // c has been released; that stage must still be in the shared-memory ring
+  // (at most STAGES stages back) for its barrier phase to be unambiguous
+  static constexpr int AST_FIT = (512 - A_COL) / ACOLS;
+  static constexpr int AST_RAW = AST_FIT < CPS * STAGES ? AST_FIT : CPS * STAGES;
   static constexpr int AST = (AST_RAW > 8 ? 8 : AST_RAW) / G * G;
   static constexpr int THREADS = 32 * (2 + 4 + 4 * G);
+  // registers per thread for one resident CTA: each of the SM's four
+  // sub-partitions holds 16K registers and ceil(warps / 4) of the warps, in
+  // the allocator's steps of 8
+  static constexpr int WARPS_PER_SMSP = (THREADS / 32 + 3) / 4;
+  static constexpr int REGS_RAW = 16384 / (32 * WARPS_PER_SMSP) / 8 * 8;
+  static constexpr int MAXNREG = REGS_RAW > 255 ? 255 : REGS_RAW;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE + 1024;
   static_assert(STAGES >= 2, "shared memory ring too small");
@@ -102,27 +112,15 @@ struct Cfg {
 };
 
 struct SharedCtl {
-  uint64_t full[8], empty[8];
-  uint64_t a_full[8], a_empty[8];  // per A chunk slot
+  uint64_t full[8], full_x[8], empty[8];  // full: codes + scales landed; full_x: x (or t') landed
+  uint64_t a_full[8];  // per A chunk slot
   uint64_t d_full[2], d_empty[2];
   uint64_t done;
+  uint32_t next_chunk[4];  // next A chunk to take, per TMEM lane quarter
   uint32_t tmem;
   int abort;
   int last;
 };
-
-__device__ __forceinline__ uint32_t f16x2_from_e2m1x2(uint32_t byte) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(r) : "r"(byte));
-  return r;
-}
-
-// Two E4M3 bytes (low 16 bits) -> f16x2, exactly (every E4M3 value is an f16).
-__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t two) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 b;\n\tcvt.u16.u32 b, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, b;\n\t}" : "=r"(r) : "r"(two));
-  return r;
-}
 
 // Four E4M3 bytes -> two f16x2 (bytes 0,1 and bytes 2,3), one unpack.
 __device__ __forceinline__ void f16x2x2_from_e4m3x4(uint32_t four, uint32_t& lo, uint32_t& hi) {
@@ -206,7 +204,7 @@ struct Ring {
 }  // namespace
 
 template <int BN, int BK, bool F16, int G>
-__global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(const __grid_constant__ W4Params p) {
+__global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __grid_constant__ W4Params p) {
   using C = Cfg<BN, BK, G>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -218,21 +216,25 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.full_x[s], 1);
       mbar_init(&sh.empty[s], 1 + 4 * C::CPS);  // MMA commit + 4 dequant warps per A chunk
     }
-    for (int s = 0; s < C::AST; ++s) {
-      mbar_init(&sh.a_full[s], 4);
-      mbar_init(&sh.a_empty[s], 1);
-    }
+    for (int s = 0; s < C::AST; ++s) mbar_init(&sh.a_full[s], 4);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.d_full[b], 1);
       mbar_init(&sh.d_empty[b], 4);
     }
     mbar_init(&sh.done, 1);
+    for (int i = 0; i < 4; ++i) sh.next_chunk[i] = 0;
     sh.abort = 0;
     fence_barrier_init();
   }
-  if (warp == 1) tmem_alloc(&sh.tmem, C::TMEM_COLS);
+  // warp roles: the dequant warpgroups take the lowest warp numbers (the
+  // schedulers favour them when a sub-partition is busy, and a lagging dequant
+  // warp holds up its whole A chunk), then the four epilogue warps, then the
+  // TMA and MMA issuers
+  constexpr int kEpi = 4 * G, kTma = 4 * G + 4, kMma = 4 * G + 5;
+  if (warp == kMma) tmem_alloc(&sh.tmem, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -254,51 +256,94 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
     nl = (L.r > 0 && sp == L.splits - 1) ? (L.lora_chunks + KSUB - 1) / KSUB : 0;
   };
 
-  if (warp == 0) {
+  if (warp == kTma) {
     // ------------------------------ TMA ------------------------------
+    // The weight stream does not depend on the prologue kernel that writes
+    // the f16 x and t' (this kernel may start while it runs, as its
+    // programmatic dependent): the first ring of stages gets its codes and
+    // scales at once, then x waits for the prologue to complete.
     if (elect_one()) {
-      Ring st;
-      uint32_t issued = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
-        int j, nt, mt, sp, c0, nk, nl;
-        locate(u, j, nt, mt, sp, c0, nk, nl);
-        const W4Layer& L = p.layer[j];
-        for (int c = 0; c < nk + nl; ++c, st.next<C::STAGES>(), ++issued) {
-          if (st.use > 0 && !mbar_wait(&sh.empty[st.idx], (st.use - 1) & 1, abort, p.status)) {
-            ok = false;
-            break;
-          }
-          QRR_STAMP(0, 0, issued);
-          uint8_t* xs = tiles + st.idx * C::STAGE;
-          uint64_t* fb = &sh.full[st.idx];
-          if (c < nk) {
-            const int kb = (c0 + c) * BK;
-            mbar_arrive_expect_tx(fb, C::STAGE);
-#pragma unroll
-            for (int q = 0; q < KSUB; ++q) tma_load_2d(&L.tx, fb, xs + q * C::X_SUB, kb + 64 * q, mt * BN);
-            tma_load_2d(&L.tcodes, fb, xs + C::X_BYTES, kb / 2, nt * 128);
-            if constexpr (C::SC_TMA) tma_load_2d(&L.tscales, fb, xs + C::X_BYTES + C::C_BYTES, kb / 16, nt * 128);
-          } else {
-            // LoRA stage: t' sub-tiles past the tensor's width read as zeros
-            const int lsub = (c - nk) * KSUB;
-            mbar_arrive_expect_tx(fb, C::X_BYTES);
-#pragma unroll
-            for (int q = 0; q < KSUB; ++q) tma_load_2d(&L.tt, fb, xs + q * C::X_SUB, (lsub + q) * 64, mt * BN);
-          }
+      struct Cursor {
+        int u = -1, c = 0, j = 0, nt = 0, mt = 0, sp = 0, c0 = 0, nk = 0, nl = 0;
+      };
+      auto next = [&](Cursor& k) {  // advance to the next stage of the CTA; false past the last
+        if (k.u >= 0 && ++k.c < k.nk + k.nl) return true;
+        k.c = 0;
+        for (k.u = k.u < 0 ? static_cast<int>(blockIdx.x) : k.u + static_cast<int>(gridDim.x); k.u < p.total_units;
+             k.u += gridDim.x) {
+          locate(k.u, k.j, k.nt, k.mt, k.sp, k.c0, k.nk, k.nl);
+          if (k.nk + k.nl > 0) return true;
         }
+        return false;
+      };
+      auto issue_w = [&](const Cursor& k, int idx) {
+        uint64_t* fb = &sh.full[idx];
+        if (k.c < k.nk) {
+          const int kb = (k.c0 + k.c) * BK;
+          uint8_t* xs = tiles + idx * C::STAGE;
+          mbar_arrive_expect_tx(fb, C::C_BYTES + C::S_BYTES);
+          tma_load_2d(&p.layer[k.j].tcodes, fb, xs + C::X_BYTES, kb / 2, k.nt * 128);
+          if constexpr (C::SC_TMA)
+            tma_load_2d(&p.layer[k.j].tscales, fb, xs + C::X_BYTES + C::C_BYTES, kb / 16, k.nt * 128);
+        } else {
+          mbar_arrive(fb);  // LoRA stage: no codes
+        }
+      };
+      auto issue_x = [&](const Cursor& k, int idx) {
+        uint64_t* fb = &sh.full_x[idx];
+        uint8_t* xs = tiles + idx * C::STAGE;
+        mbar_arrive_expect_tx(fb, C::X_BYTES);
+        if (k.c < k.nk) {
+          const int kb = (k.c0 + k.c) * BK;
+#pragma unroll
+          for (int q = 0; q < KSUB; ++q) tma_load_2d(&p.layer[k.j].tx, fb, xs + q * C::X_SUB, kb + 64 * q, k.mt * BN);
+        } else {
+          // LoRA stage: t' sub-tiles past the tensor's width read as zeros
+          const int lsub = (k.c - k.nk) * KSUB;
+#pragma unroll
+          for (int q = 0; q < KSUB; ++q)
+            tma_load_2d(&p.layer[k.j].tt, fb, xs + q * C::X_SUB, (lsub + q) * 64, k.mt * BN);
+        }
+      };
+      Cursor kw, kx;
+      uint32_t nw = 0;  // stages whose weights are issued
+      while (nw < static_cast<uint32_t>(C::STAGES) && next(kw)) {
+        QRR_STAMP(0, 0, nw);
+        issue_w(kw, static_cast<int>(nw));
+        ++nw;
       }
-      // drain: the last load of every stage has landed before the CTA exits
+      griddep_wait();
+      uint32_t nx = 0;
+      bool ok = true;
+      while (nx < nw) {
+        next(kx);
+        issue_x(kx, static_cast<int>(nx));
+        ++nx;
+      }
+      while (ok && next(kw)) {
+        next(kx);
+        const uint32_t idx = nw % C::STAGES, use = nw / C::STAGES;
+        if (!mbar_wait(&sh.empty[idx], (use - 1) & 1, abort, p.status)) {
+          ok = false;
+          break;
+        }
+        QRR_STAMP(0, 0, nw);
+        issue_w(kw, static_cast<int>(idx));
+        issue_x(kx, static_cast<int>(idx));
+        ++nw;
+      }
+      // drain: the last loads of every stage have landed before the CTA exits
       volatile int no_abort = 0;
-      for (uint32_t k = 0; k < static_cast<uint32_t>(C::STAGES) && k < issued; ++k) {
-        const uint32_t i = issued - 1 - k;
+      for (uint32_t k = 0; k < static_cast<uint32_t>(C::STAGES) && k < nw; ++k) {
+        const uint32_t i = nw - 1 - k;
         mbar_wait(&sh.full[i % C::STAGES], (i / C::STAGES) & 1, &no_abort, p.status);
+        mbar_wait(&sh.full_x[i % C::STAGES], (i / C::STAGES) & 1, &no_abort, p.status);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kMma) {
     // ------------------------------ MMA ------------------------------
-    // A stage sa is ready only after its dequant group saw the stage's TMA
-    // data land (it waits on `full` first), so this thread waits on a_full alone.
+    // Per stage: the x (or t') tile has landed; per A chunk: its dequant
+    // warps have stored it to TMEM.
     if (elect_one()) {
       constexpr uint32_t id_main = make_idesc(F16 ? kFmtF16 : kFmtBF16, F16 ? kFmtF16 : kFmtBF16, 128, BN);
       constexpr uint32_t id_lora = make_idesc(kFmtBF16, kFmtBF16, 128, BN);
@@ -315,10 +360,17 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
         QRR_STAMP(1, 3, units);
         const uint32_t dcol = tmem + db * C::D_COLS;
         for (int c = 0; c < nk + nl && ok; ++c, st.next<C::STAGES>()) {
-          const uint32_t xb = smem_u32(tiles + st.idx * C::STAGE);
+          if (!mbar_wait(&sh.full_x[st.idx], st.use & 1, abort, p.status)) {
+            ok = false;
+            break;
+          }
+          // descriptor of the stage's first x sub-tile; the K16 steps only move
+          // its start-address field (16-byte units, no carry inside shared memory)
+          const uint64_t bdesc = sw128_desc(smem_u32(tiles + st.idx * C::STAGE));
           const uint32_t idesc = c < nk ? id_main : id_lora;
 #pragma unroll
           for (int hc = 0; hc < C::CPS; ++hc, at.next<C::AST>()) {
+            QRR_STAMP(2, 2, chunks);
             if (!mbar_wait(&sh.a_full[at.idx], at.use & 1, abort, p.status)) {
               ok = false;
               break;
@@ -326,44 +378,61 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
             QRR_STAMP(1, 0, chunks);
             tc_fence_after();
             const uint32_t a0 = tmem + C::A_COL + C::ACOLS * at.idx;
+            constexpr int NK = C::ACH / 16;  // K16 steps per chunk
+            static_assert(NK == 4 || NK == 8, "chunk of 64 or 128 K");
+            uint64_t bd[NK];
 #pragma unroll
-            for (int k = 0; k < C::ACH / 16; ++k) {
-              const int kk = hc * (C::ACH / 16) + k;  // K16 step within the stage
-              mma_bf16_ts(dcol, a0 + 8 * k, sw128_desc(xb + (kk >> 2) * C::X_SUB + 32 * (kk & 3)), idesc,
-                          (c > 0 || kk > 0) ? 1u : 0u);
+            for (int k = 0; k < NK; ++k) {
+              const int kk = hc * NK + k;  // K16 step within the stage
+              bd[k] = bdesc + static_cast<uint64_t>(((kk >> 2) * C::X_SUB + 32 * (kk & 3)) >> 4);
             }
-            mma_commit(&sh.a_empty[at.idx]);
+            const uint32_t acc = (c > 0 || hc > 0) ? 1u : 0u;
+            if constexpr (NK == 8)
+              mma8_ts(dcol, a0, bd, idesc, acc);
+            else
+              mma4_ts(dcol, a0, bd, idesc, acc);
             QRR_STAMP(1, 1, chunks);
             ++chunks;
           }
+          QRR_STAMP(2, 0, chunks / C::CPS);
           if (ok) mma_commit(&sh.empty[st.idx]);
+          QRR_STAMP(2, 1, chunks / C::CPS);
         }
         if (!ok) break;
         mma_commit(&sh.d_full[db]);
+        QRR_STAMP(2, 3, units);
       }
       mma_commit(&sh.done);
       volatile int no_abort = 0;
       mbar_wait(&sh.done, 0, &no_abort, p.status);
     }
-  } else if (warp < 6) {
+  } else if (warp >= kEpi) {
     // ------------------------------ epilogue ------------------------------
+    // Layer fields are copied to registers once per unit: read through the
+    // parameter reference they would be re-read after every store (the
+    // compiler cannot rule out aliasing), each a dependent memory round trip.
     const int q = warp & 3;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+    griddep_wait();  // the per-token exponents come from the prologue kernel
     uint32_t units = 0;
     for (int u = blockIdx.x; u < p.total_units; u += gridDim.x, ++units) {
       int j, nt, mt, sp, c0, nk, nl;
       locate(u, j, nt, mt, sp, c0, nk, nl);
-      const W4Layer& L = p.layer[j];
+      const int M = p.layer[j].M, N = p.layer[j].N, splits = p.layer[j].splits, n_tiles = p.layer[j].n_tiles;
+      const int* const pexp = p.layer[j].pexp;
+      __nv_bfloat16* const y = p.layer[j].y;
+      float* const partial = p.layer[j].partial;
+      uint32_t* const counters = p.layer[j].counters;
+      const float st = *p.layer[j].tensor_scale;
       const int n = nt * 128 + 32 * q + lane;
       const int db = units % C::DBUF;
-      if (warp == 2 && lane == 0) QRR_STAMP(3, 0, units);
+      if (warp == kEpi && lane == 0) QRR_STAMP(3, 0, units);
       if (!mbar_wait(&sh.d_full[db], (units / C::DBUF) & 1, abort, p.status)) break;
-      if (warp == 2 && lane == 0) QRR_STAMP(3, 1, units);
+      if (warp == kEpi && lane == 0) QRR_STAMP(3, 1, units);
       tc_fence_after();
-      const float st = *L.tensor_scale;
       const float g = st > 0.0f ? st : 1.0f;
       const int m0 = mt * BN;
-      float* part = L.splits > 1 ? L.partial + static_cast<int64_t>(sp) * L.M * L.N : nullptr;
+      float* const part = splits > 1 ? partial + static_cast<int64_t>(sp) * M * N : nullptr;
       constexpr int CW = BN == 16 ? 16 : 32;
 #pragma unroll 1
       for (int cc = 0; cc < BN / CW; ++cc) {
@@ -372,43 +441,41 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
           tmem_ld16(tmem + lane_addr + db * C::D_COLS, r);
         else
           tmem_ld32(tmem + lane_addr + db * C::D_COLS + 32 * cc, r);
-        // the per-token factors of this slab first: y / partial stores may
-        // alias the exponent array as far as the compiler knows, so loads
-        // interleaved with the stores would run one after another
+        // the per-token factors of this slab first, all loads in flight
         float sc2[CW];
 #pragma unroll
         for (int i = 0; i < CW; ++i) {
           const int m = m0 + CW * cc + i;
-          sc2[i] = (L.pexp && m < L.M) ? __fmul_rn(g, pow2_from_exp(__ldg(L.pexp + m))) : g;
+          sc2[i] = (pexp && m < M) ? __fmul_rn(g, pow2_from_exp(__ldg(pexp + m))) : g;
         }
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < CW; ++i) {
           const int m = m0 + CW * cc + i;
-          if (m < L.M) {
+          if (m < M) {
             const float v = __uint_as_float(r[i]) * sc2[i];
             if (part)
-              part[static_cast<int64_t>(m) * L.N + n] = v;
+              part[static_cast<int64_t>(m) * N + n] = v;
             else
-              L.y[static_cast<int64_t>(m) * L.N + n] = __float2bfloat16_rn(v);
+              y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(v);
           }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.d_empty[db]);
-      if (warp == 2 && lane == 0) QRR_STAMP(3, 2, units);
+      if (warp == kEpi && lane == 0) QRR_STAMP(3, 2, units);
       if (part) {
         // all 128 epilogue threads have written their partials; one thread
         // makes them visible GPU-wide (the fence is cumulative over the
         // barrier) and takes a ticket; the last split of the tile sums all
         // partials in split order
         named_bar(1, 128);
-        if (warp == 2 && lane == 0) {
+        if (warp == kEpi && lane == 0) {
           __threadfence();
-          uint32_t* cnt = L.counters + mt * L.n_tiles + nt;
+          uint32_t* cnt = counters + mt * n_tiles + nt;
           const uint32_t prev = atomicAdd(cnt, 1u);
-          sh.last = prev == static_cast<uint32_t>(L.splits - 1);
+          sh.last = prev == static_cast<uint32_t>(splits - 1);
           if (sh.last) {
             *cnt = 0u;  // ready for the next call
             __threadfence();
@@ -417,18 +484,18 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
         named_bar(1, 128);
         if (sh.last) {
           constexpr int TB = 8, SB = 4;  // tokens per batch; loads of SB splits in flight
-          for (int i0 = 0; i0 < BN && m0 + i0 < L.M; i0 += TB) {
+          for (int i0 = 0; i0 < BN && m0 + i0 < M; i0 += TB) {
             float sum[TB];
 #pragma unroll
             for (int i = 0; i < TB; ++i) sum[i] = 0.0f;
-            for (int s0 = 0; s0 < L.splits; s0 += SB) {
+            for (int s0 = 0; s0 < splits; s0 += SB) {
               float v[SB][TB];
 #pragma unroll
               for (int s1 = 0; s1 < SB; ++s1)
 #pragma unroll
                 for (int i = 0; i < TB; ++i)
-                  v[s1][i] = (s0 + s1 < L.splits && m0 + i0 + i < L.M)
-                                 ? __ldcg(L.partial + (static_cast<int64_t>(s0 + s1) * L.M + m0 + i0 + i) * L.N + n)
+                  v[s1][i] = (s0 + s1 < splits && m0 + i0 + i < M)
+                                 ? __ldcg(partial + (static_cast<int64_t>(s0 + s1) * M + m0 + i0 + i) * N + n)
                                  : 0.0f;
 #pragma unroll
               for (int s1 = 0; s1 < SB; ++s1)
@@ -437,16 +504,18 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
             }
 #pragma unroll
             for (int i = 0; i < TB; ++i)
-              if (m0 + i0 + i < L.M) L.y[static_cast<int64_t>(m0 + i0 + i) * L.N + n] = __float2bfloat16_rn(sum[i]);
+              if (m0 + i0 + i < M) y[static_cast<int64_t>(m0 + i0 + i) * N + n] = __float2bfloat16_rn(sum[i]);
           }
         }
         named_bar(1, 128);
       }
-      if (warp == 2 && lane == 0) QRR_STAMP(3, 3, units);
+      if (warp == kEpi && lane == 0) QRR_STAMP(3, 3, units);
     }
   } else {
     // ------------------------------ dequant ------------------------------
-    const int grp = (warp - 6) >> 2;
+    // The G warps of a sub-partition share its TMEM lane quarter q and take A
+    // chunks from a per-quarter counter in order, so a warp that falls behind
+    // holds up only its own chunk: the next free warp takes the chunks after it.
     const int q = warp & 3;
     const int row = 32 * q + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
@@ -454,34 +523,67 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
     // p ^ (r & 7) for 128-byte rows and p ^ ((r >> 2) & 1) for 32-byte rows,
     // which keeps every 8-thread phase of a 16-byte shared load on distinct banks
     const int rot = BK == 256 ? (row & 7) : ((row >> 2) & 1);
-    Ring st, at;
-    int turn = 0;  // A-chunk counter modulo G
-    uint32_t chunk = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
+    // this CTA's A chunks: its units in order, (nk + nl) stages of CPS chunks
+    uint32_t total = 0;
+    for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
       int j, nt, mt, sp, c0, nk, nl;
       locate(u, j, nt, mt, sp, c0, nk, nl);
-      const W4Layer& L = p.layer[j];
+      total += static_cast<uint32_t>((nk + nl) * C::CPS);
+    }
+    int u = static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x);
+    uint32_t ubeg = 0, uend = 0;  // chunk range of unit u
+    int j = 0, nt = 0, mt = 0, sp = 0, c0 = 0, nk = 0, nl = 0;
+    while (true) {
+      uint32_t chunk = 0;
+      if (lane == 0) chunk = atomicAdd(&sh.next_chunk[q], 1u);
+      chunk = __shfl_sync(0xFFFFFFFFu, chunk, 0);
+      if (chunk >= total) break;
+      while (chunk >= uend) {  // claims only grow: move forward to the chunk's unit
+        u += gridDim.x;
+        locate(u, j, nt, mt, sp, c0, nk, nl);
+        ubeg = uend;
+        uend += static_cast<uint32_t>((nk + nl) * C::CPS);
+      }
+      // layer fields in registers (see the epilogue)
+      const int LM = p.layer[j].M, Lr = p.layer[j].r;
+      const int* const Lpexp = p.layer[j].pexp;
+      const uint16_t* const LB = p.layer[j].B;
       const int n = nt * 128 + row;
-      const uint8_t* srow = L.scales + static_cast<int64_t>(n) * (L.K / 16);
-      for (int c = 0; c < nk + nl && ok; ++c, st.next<C::STAGES>()) {
-#pragma unroll 1
-        for (int hc = 0; hc < C::CPS; ++hc, at.next<C::AST>(), turn = turn + 1 == G ? 0 : turn + 1, ++chunk) {
-          if (turn != grp) continue;
+      const uint8_t* srow = p.layer[j].scales + static_cast<int64_t>(n) * (p.layer[j].K / 16);
+      const int c = static_cast<int>((chunk - ubeg) / C::CPS);   // stage within the unit
+      const int hc = static_cast<int>((chunk - ubeg) % C::CPS);  // chunk within the stage
+      const uint32_t sseq = chunk / C::CPS;                      // stage sequence number of the CTA
+      const int sidx = static_cast<int>(sseq % C::STAGES);
+      const int slot = static_cast<int>(chunk % C::AST);
+      {
+        {
           if (q == 2 && lane == 0) QRR_STAMP(4, 0, chunk);
+          if (q != 2 && lane == 0) QRR_STAMP(5 + (q == 3 ? 2 : q), 2, chunk);
           uint32_t scw[C::ACH / 64];
           if constexpr (!C::SC_TMA) {
             if (c < nk) scw[0] = __ldg(reinterpret_cast<const uint32_t*>(srow + (c0 + c) * (BK / 16)));
           }
-          if (!mbar_wait(&sh.full[st.idx], st.use & 1, abort, p.status) ||
-              (at.use > 0 && !mbar_wait(&sh.a_empty[at.idx], (at.use - 1) & 1, abort, p.status))) {
-            ok = false;
-            break;
+          // the slot was last written for chunk - AST; its MMAs are done once
+          // the stage that chunk belonged to has been released (one commit per
+          // stage, no per-chunk commits on the tensor pipe)
+          bool free = true;
+          if (chunk >= static_cast<uint32_t>(C::AST)) {
+            const uint32_t prev = (chunk - C::AST) / C::CPS;  // stage sequence number
+            free = mbar_wait(&sh.empty[prev % C::STAGES], (prev / C::STAGES) & 1, abort, p.status);
+          }
+          if (q == 2 && lane == 0) QRR_STAMP(4, 3, chunk);
+          if (!free || !mbar_wait(&sh.full[sidx], (sseq / C::STAGES) & 1, abort, p.status)) break;
+          // a LoRA chunk reads the t' tile (and the per-token exponents) that
+          // the prologue kernel wrote
+          if (c >= nk) {
+            griddep_wait();
+            if (!mbar_wait(&sh.full_x[sidx], (sseq / C::STAGES) & 1, abort, p.status)) break;
           }
           if (q == 2 && lane == 0) QRR_STAMP(4, 1, chunk);
+          if (q != 2 && lane == 0) QRR_STAMP(5 + (q == 3 ? 2 : q), 1, chunk);
           tc_fence_after();
-          const uint8_t* stage = tiles + st.idx * C::STAGE;
-          const uint32_t a_addr = tmem + lane_addr + C::A_COL + C::ACOLS * at.idx;
+          const uint8_t* stage = tiles + sidx * C::STAGE;
+          const uint32_t a_addr = tmem + lane_addr + C::A_COL + C::ACOLS * slot;
           if (c < nk) {
             if constexpr (C::SC_TMA) {
               // this chunk's 8 scale bytes of the row's 16 (ACH = 128)
@@ -519,11 +621,11 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
               const int m0 = mt * BN;
               for (int idx = tig; idx < PIECES; idx += 128) {
                 const int sub = idx / (BN * 8), rem = idx % (BN * 8), mr = rem >> 3;
-                if (m0 + mr >= L.M) continue;
+                if (m0 + mr >= LM) continue;
                 uint4* pc = reinterpret_cast<uint4*>(const_cast<uint8_t*>(stage) +
                                                      (hc * (C::ACH / 64) + sub) * C::X_SUB + mr * 128 +
                                                      (rem & 7) * 16);
-                const Pow2Scaler sc(L.pexp[m0 + mr]);
+                const Pow2Scaler sc(Lpexp[m0 + mr]);
                 uint4 v = *pc;
                 uint32_t* wv = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
@@ -535,7 +637,7 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
             // LoRA chunk: A word i holds (B[n, rb+i], B[n, rb+i]) against the
             // (high, low) halves of t'; zero past rank r
             const int rb = (c - nk) * (BK / 2) + hc * (C::ACH / 2);
-            const uint16_t* brow = L.B + static_cast<int64_t>(n) * L.r + rb;
+            const uint16_t* brow = LB + static_cast<int64_t>(n) * Lr + rb;
 #pragma unroll
             for (int h = 0; h < C::ACH / 64; ++h) {
               uint32_t out[32];
@@ -543,7 +645,7 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
               for (int v4 = 0; v4 < 4; ++v4) {
                 const int v8 = 4 * h + v4;
                 uint4 bv = make_uint4(0, 0, 0, 0);
-                if (rb + 8 * v8 < L.r) bv = __ldg(reinterpret_cast<const uint4*>(brow) + v8);
+                if (rb + 8 * v8 < Lr) bv = __ldg(reinterpret_cast<const uint4*>(brow) + v8);
                 const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -556,11 +658,12 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
           }
           tmem_st_wait();
           if (q == 2 && lane == 0) QRR_STAMP(4, 2, chunk);
+          if (q != 2 && lane == 0) QRR_STAMP(5 + (q == 3 ? 2 : q), 0, chunk);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(&sh.a_full[at.idx]);
-            mbar_arrive(&sh.empty[st.idx]);
+            mbar_arrive(&sh.a_full[slot]);
+            mbar_arrive(&sh.empty[sidx]);
           }
         }
       }
@@ -568,144 +671,9 @@ __global__ void __launch_bounds__(Cfg<BN, BK, G>::THREADS, 1) w4a16_tc_kernel(co
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMma) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Prologue.  Per layer, CTAs of two kinds:
-//   x rows (f16 path): p_m so that max|x_m| 2^-p_m is in [2^14, 2^15) and
-//     x16 = f16(x 2^-p_m), one CTA per token row;
-//   LoRA slices: one CTA per (group of 8 ranks, 512-wide K slice) computes the
-//     fp32 partial dot products of every token with its ranks; the last slice
-//     of a rank group to finish (a ticket) sums the partials in slice order,
-//     t_j = sum_k x[m,k] A[j,k], and writes t'[m, 2j] = bf16(v),
-//     t'[m, 2j + 1] = bf16(v - bf16(v)) for v = (alpha/r) t_j / g (g = s_t,
-//     or 1 when s_t = 0).  The per-token 2^-p_m of the f16 path is applied to
-//     the t' tile inside the GEMM, so the two kinds do not depend on each other.
-template <bool F16>
-__global__ void __launch_bounds__(256) lora_prep_kernel(const __grid_constant__ PrepBatch batch) {
-  __shared__ uint32_t amax_s[8];
-  __shared__ int last_s;
-  int j = 0;
-  while (j + 1 < batch.count && batch.a[j + 1].first_cta <= static_cast<int>(blockIdx.x)) ++j;
-  const PrepArgs& a = batch.a[j];
-  int local = static_cast<int>(blockIdx.x) - a.first_cta;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nvec = static_cast<int>(a.K / 8);
-  const int nx = F16 ? static_cast<int>(a.M) : 0;
-  if (local < nx) {
-    // ---- x row -> f16 with its power-of-two pre-scale ----
-    const int m = local;
-    const uint4* xr = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(m) * a.K);
-    uint32_t mx = 0;
-    for (int v = threadIdx.x; v < nvec; v += 256) mx = max(mx, absmax_bits8(__ldg(xr + v)));
-    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
-    if (lane == 0) amax_s[warp] = mx;
-    __syncthreads();
-    mx = amax_s[0];
-#pragma unroll
-    for (int i = 1; i < 8; ++i) mx = max(mx, amax_s[i]);
-    int pexp = 0;
-    if (mx != 0u) {
-      int e;
-      frexpf(bf16bits_to_f32(mx), &e);  // amax = f 2^e, 0.5 <= f < 1
-      pexp = e - 15;                    // amax 2^-p in [2^14, 2^15)
-    }
-    if (mx >= 0x7F80u && threadIdx.x == 0) flag(a.status, QRR_DEV_NONFINITE);
-    if (threadIdx.x == 0) a.pexp[m] = pexp;
-    const Pow2Scaler sc(pexp);
-    uint4* x16 = reinterpret_cast<uint4*>(a.x16 + static_cast<int64_t>(m) * a.K);
-    for (int v = threadIdx.x; v < nvec; v += 256) {
-      const uint4 xv = __ldg(xr + v);
-      const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __half2 h = __floats2half2_rn(sc(bf16_lo(w[i])), sc(bf16_hi(w[i])));
-        o[i] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      x16[v] = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-    return;
-  }
-  local -= nx;
-  // ---- LoRA slice: ranks [8 rg, 8 rg + 8), vectors [64 ks, 64 ks + 64) ----
-  const int rg = local / a.ks, kslice = local % a.ks;
-  const int j0 = rg * 8, nj = min(8, a.r - j0);
-  const int v0 = kslice * 64, v1 = min(nvec, v0 + 64);
-  // each lane holds two 8-element vectors of the 8 A rows
-  uint4 av[2][8];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int v = v0 + lane + 32 * h;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      av[h][i] = (v < v1 && i < nj)
-                     ? __ldg(reinterpret_cast<const uint4*>(a.A + static_cast<int64_t>(j0 + i) * a.K) + v)
-                     : make_uint4(0, 0, 0, 0);
-  }
-  for (int m = warp; m < a.M; m += 8) {
-    const uint4* xr = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(m) * a.K);
-    float d[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) d[i] = 0.0f;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int v = v0 + lane + 32 * h;
-      const uint4 xv = v < v1 ? __ldg(xr + v) : make_uint4(0, 0, 0, 0);
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t aw[4] = {av[h][i].x, av[h][i].y, av[h][i].z, av[h][i].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          d[i] = fmaf(bf16_lo(xw[q]), bf16_lo(aw[q]), d[i]);
-          d[i] = fmaf(bf16_hi(xw[q]), bf16_hi(aw[q]), d[i]);
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) d[i] += __shfl_xor_sync(0xFFFFFFFFu, d[i], o);
-    }
-    if (lane < nj) {
-      float mine = d[0];
-#pragma unroll
-      for (int i = 1; i < 8; ++i)
-        if (lane == i) mine = d[i];
-      a.tpart[(static_cast<int64_t>(kslice) * a.M + m) * a.r + j0 + lane] = mine;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const uint32_t prev = atomicAdd(a.tickets + rg, 1u);
-    last_s = prev == static_cast<uint32_t>(a.ks - 1);
-    if (last_s) __threadfence();
-  }
-  __syncthreads();
-  if (!last_s) return;
-  const float st = *a.tensor_scale;
-  const float g = st > 0.0f ? st : 1.0f;
-  for (int idx = threadIdx.x; idx < a.M * nj; idx += 256) {
-    const int m = idx / nj, i = idx % nj;
-    float t = 0.0f;
-    for (int s2 = 0; s2 < a.ks; ++s2) t += __ldcg(a.tpart + (static_cast<int64_t>(s2) * a.M + m) * a.r + j0 + i);
-    const float v = __fdiv_rn(a.lora_scale * t, g);
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-    __nv_bfloat16* trow = a.t + static_cast<int64_t>(m) * a.t_cols;
-    trow[2 * (j0 + i)] = hi;
-    trow[2 * (j0 + i) + 1] = lo;
-  }
-  if (rg == 0) {
-    const int pad = a.t_cols - 2 * a.r;
-    for (int idx = threadIdx.x; idx < a.M * pad; idx += 256)
-      a.t[static_cast<int64_t>(idx / pad) * a.t_cols + 2 * a.r + idx % pad] = __float2bfloat16_rn(0.0f);
   }
 }
 
@@ -713,8 +681,14 @@ __global__ void __launch_bounds__(256) lora_prep_kernel(const __grid_constant__ 
 
 namespace {
 
+// dequant warpgroups of the decode (f16) kernels
+#ifndef QRR_DECODE_GROUPS
+#define QRR_DECODE_GROUPS 3
+#endif
+constexpr int kDecodeGroups = QRR_DECODE_GROUPS;
+
 template <int BN, int BK, bool F16, int G>
-cudaError_t launch_bn(const W4Params& p, int grid, cudaStream_t stream) {
+cudaError_t launch_bn(const W4Params& p, int grid, bool after_prologue, cudaStream_t stream) {
   using C = Cfg<BN, BK, G>;
   static bool attr = false;
   if (!attr) {
@@ -723,8 +697,17 @@ cudaError_t launch_bn(const W4Params& p, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  w4a16_tc_kernel<BN, BK, F16, G><<<grid, C::THREADS, C::SMEM, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute la[1];
+  la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  la[0].val.programmaticStreamSerializationAllowed = after_prologue ? 1 : 0;
+  cfg.attrs = la;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<BN, BK, F16, G>, p);
 }
 
 }  // namespace
@@ -741,23 +724,9 @@ int w4_bn_for(int64_t M) {
 // scales staged by TMA); prefill tiles use 64-wide stages.
 int w4_bk_for(int64_t M) { return M <= 64 ? 256 : 64; }
 
-cudaError_t launch_lora_prep(PrepBatch& b, bool f16, cudaStream_t stream) {
-  if (b.count == 0 || b.a[0].M == 0) return cudaSuccess;
-  int ctas = 0;
-  for (int j = 0; j < b.count; ++j) {
-    PrepArgs& a = b.a[j];
-    a.first_cta = ctas;
-    ctas += (f16 ? static_cast<int>(a.M) : 0) + (a.r > 0 ? ((a.r + 7) / 8) * a.ks : 0);
-  }
-  if (ctas == 0) return cudaSuccess;
-  if (f16)
-    lora_prep_kernel<true><<<ctas, 256, 0, stream>>>(b);
-  else
-    lora_prep_kernel<false><<<ctas, 256, 0, stream>>>(b);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, cudaStream_t stream) {
+// after_prologue: the previous kernel in the stream is the prologue that
+// writes x16 / pexp / t'; this launch may then start before it completes.
+cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, bool after_prologue, cudaStream_t stream) {
   int units = 0;
   for (int j = 0; j < p.count; ++j) {
     p.layer[j].first_unit = units;
@@ -770,12 +739,13 @@ cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, cudaStream_t stream) 
   const int grid = units < sms ? units : sms;
   if (f16) {
     switch (bn) {
-      case 16: return launch_bn<16, 256, true, 3>(p, grid, stream);
-      case 32: return launch_bn<32, 256, true, 3>(p, grid, stream);
-      default: return launch_bn<64, 256, true, 3>(p, grid, stream);
+      case 16: return launch_bn<16, 256, true, kDecodeGroups>(p, grid, after_prologue, stream);
+      case 32: return launch_bn<32, 256, true, kDecodeGroups>(p, grid, after_prologue, stream);
+      default: return launch_bn<64, 256, true, kDecodeGroups>(p, grid, after_prologue, stream);
     }
   }
-  return bn == 128 ? launch_bn<128, 64, false, 2>(p, grid, stream) : launch_bn<256, 64, false, 2>(p, grid, stream);
+  return bn == 128 ? launch_bn<128, 64, false, 2>(p, grid, after_prologue, stream)
+                   : launch_bn<256, 64, false, 2>(p, grid, after_prologue, stream);
 }
 
 }  // namespace qrr

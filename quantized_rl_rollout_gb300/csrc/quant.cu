@@ -43,10 +43,11 @@ __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __grid_constant__
       if (cur >= 0) publish();
       cur = j;
     }
-    const Nvfp4Job& job = batch.job[j];
-    const int64_t nvec = job.N * job.K / 8;  // uint4 of 8 bf16
-    const int64_t base = (c - job.first_amax_chunk) * kAmaxChunkVecs;
-    const uint4* src = reinterpret_cast<const uint4*>(job.W);
+    // job fields into registers: read through the parameter reference they
+    // would be re-read after every store (aliasing), a memory round trip each
+    const int64_t nvec = batch.job[j].N * batch.job[j].K / 8;  // uint4 of 8 bf16
+    const int64_t base = (c - batch.job[j].first_amax_chunk) * kAmaxChunkVecs;
+    const uint4* src = reinterpret_cast<const uint4*>(batch.job[j].W);
     uint4 v[kAmaxChunkVecs / 256];
 #pragma unroll
     for (int u = 0; u < kAmaxChunkVecs / 256; ++u) {
@@ -67,14 +68,15 @@ __global__ void __launch_bounds__(256) nvfp4_encode_kernel(const __grid_constant
   for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x) {
     int j = 0;
     while (j + 1 < batch.count && batch.job[j + 1].first_encode_chunk <= c) ++j;
-    const Nvfp4Job& job = batch.job[j];
-    const int64_t nblocks = job.N * job.K / 16;
-    const int64_t b = (c - job.first_encode_chunk) * 256 + threadIdx.x;
+    const int64_t nblocks = batch.job[j].N * batch.job[j].K / 16;
+    const int64_t b = (c - batch.job[j].first_encode_chunk) * 256 + threadIdx.x;
+    uint8_t* const codes = batch.job[j].codes;
+    uint8_t* const scales = batch.job[j].scales;
     const float amax_t = bf16bits_to_f32(batch.amax_bits[j]);
     const float s_t = __fdiv_rn(amax_t, 2688.0f);
-    if (b == 0) *job.tensor_scale = s_t;
+    if (b == 0) *batch.job[j].tensor_scale = s_t;
     if (b >= nblocks) continue;
-    const uint4* src = reinterpret_cast<const uint4*>(job.W) + 2 * b;
+    const uint4* src = reinterpret_cast<const uint4*>(batch.job[j].W) + 2 * b;
     const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
     uint32_t sb = 0;
     uint2 packed = make_uint2(0u, 0u);
@@ -96,8 +98,8 @@ __global__ void __launch_bounds__(256) nvfp4_encode_kernel(const __grid_constant
         packed = make_uint2(out[0], out[1]);
       }
     }
-    reinterpret_cast<uint2*>(job.codes)[b] = packed;
-    job.scales[b] = static_cast<uint8_t>(sb);
+    reinterpret_cast<uint2*>(codes)[b] = packed;
+    scales[b] = static_cast<uint8_t>(sb);
   }
 }
 
@@ -158,9 +160,14 @@ __global__ void __launch_bounds__(256) fp8_w128_kernel(const __grid_constant__ F
   for (int64_t t = blockIdx.x; t < batch.total_tiles; t += gridDim.x) {
     int j = 0;
     while (j + 1 < batch.count && batch.job[j + 1].first_tile <= t) ++j;
-    const Fp8WJob& job = batch.job[j];
-    const int64_t local = t - job.first_tile;
-    const int64_t kt = job.K / 128;
+    // job fields into registers (see the NVFP4 kernels)
+    const int64_t N = batch.job[j].N, K = batch.job[j].K;
+    const uint16_t* const W = batch.job[j].W;
+    uint8_t* const qout = batch.job[j].q;
+    float* const scales = batch.job[j].scales;
+    const int mode = batch.mode;
+    const int64_t local = t - batch.job[j].first_tile;
+    const int64_t kt = K / 128;
     const int64_t tr = local / kt, tc = local % kt;
     const int64_t row0 = tr * 128;
     const int cchunk = threadIdx.x & 15;
@@ -169,8 +176,8 @@ __global__ void __launch_bounds__(256) fp8_w128_kernel(const __grid_constant__ F
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int64_t row = row0 + u * 16 + (threadIdx.x >> 4);
-      if (row < job.N) {
-        v[u] = __ldg(reinterpret_cast<const uint4*>(job.W + row * job.K + tc * 128) + cchunk);
+      if (row < N) {
+        v[u] = __ldg(reinterpret_cast<const uint4*>(W + row * K + tc * 128) + cchunk);
         m = max(m, absmax_bits8(v[u]));
       } else {
         v[u] = make_uint4(0, 0, 0, 0);
@@ -188,31 +195,31 @@ __global__ void __launch_bounds__(256) fp8_w128_kernel(const __grid_constant__ F
     float s = 0.0f;
     int e = 0;
     if (v448 > 0.0f) {
-      if (batch.mode == QRR_SCALE_FP32) {
+      if (mode == QRR_SCALE_FP32) {
         s = v448;
       } else {
         e = pow2_ceil_exp(v448);
         s = pow2_from_exp(e);
       }
     }
-    if (threadIdx.x == 0) job.scales[tr * kt + tc] = s;
+    if (threadIdx.x == 0) scales[tr * kt + tc] = s;
     const Pow2Scaler sc(e);
     const SharedDivisor div(s > 0.0f ? s : 1.0f);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int64_t row = row0 + u * 16 + (threadIdx.x >> 4);
-      if (row >= job.N) continue;
+      if (row >= N) continue;
       const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
       uint32_t out[2] = {0u, 0u};
       if (s > 0.0f) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float a = batch.mode == QRR_SCALE_FP32 ? div(bf16_lo(w[k])) : sc(bf16_lo(w[k]));
-          const float b = batch.mode == QRR_SCALE_FP32 ? div(bf16_hi(w[k])) : sc(bf16_hi(w[k]));
+          const float a = mode == QRR_SCALE_FP32 ? div(bf16_lo(w[k])) : sc(bf16_lo(w[k]));
+          const float b = mode == QRR_SCALE_FP32 ? div(bf16_hi(w[k])) : sc(bf16_hi(w[k]));
           out[k >> 1] |= cvt_e4m3x2(a, b) << (16 * (k & 1));
         }
       }
-      reinterpret_cast<uint2*>(job.q + row * job.K + tc * 128)[cchunk] = make_uint2(out[0], out[1]);
+      reinterpret_cast<uint2*>(qout + row * K + tc * 128)[cchunk] = make_uint2(out[0], out[1]);
     }
   }
 }

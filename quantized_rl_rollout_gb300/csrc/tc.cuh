@@ -57,6 +57,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same, but a thread whose phase is still open is parked by the hardware until
+// the phase completes or about `ns` nanoseconds pass, instead of spinning: a
+// spinning waiter takes issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+constexpr uint32_t kWaitSliceNs = 1u << 20;  // about 1 ms per parked try
+
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false (and raises the abort flag) on timeout or when another wait of the
 // CTA already timed out.
@@ -66,7 +81,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   // microsecond, which would add that much latency to every hand-off)
   const long long t0 = clock64();
   while (true) {
+#ifdef QRR_WAIT_SPIN
     if (mbar_try_wait(bar, parity)) return true;
+#else
+    if (mbar_try_wait_sleep(bar, parity, kWaitSliceNs)) return true;
+#endif
     if (*abort) return false;
     if (clock64() - t0 > kWaitLimitCycles) {
       *abort = 1;
@@ -74,6 +93,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       return false;
     }
   }
+}
+
+// ---- programmatic dependent launch ------------------------------------------
+
+// In a kernel launched as the programmatic dependent of the previous kernel in
+// its stream: wait until that kernel has completed and its writes are
+// visible.  Without such a dependency it returns at once.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// In the earlier kernel: let the dependent kernel be scheduled (its CTAs start
+// once every CTA of this grid has executed this or exited).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---- TMA ------------------------------------------------------------------
@@ -180,6 +212,46 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Four / eight kind::f16 MMAs with A from TMEM, issued back to back from one
+// asm block: A chunk k sits 8 columns after chunk k - 1, `b[k]` are the B
+// descriptors, only the first MMA takes `accumulate` (the others always add).
+// The MMA pipe accepts an instruction about every 46 cycles; operand setup
+// between single MMAs, on a sub-partition busy with other warps, would
+// leave it idle.
+__device__ __forceinline__ void mma4_ts(uint32_t d_tmem, uint32_t a_tmem, const uint64_t (&b)[4], uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b32 a1, a2, a3;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 q, %6, %6;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %7, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], %3, %7, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], %4, %7, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], %5, %7, q;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(accumulate), "r"(idesc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma8_ts(uint32_t d_tmem, uint32_t a_tmem, const uint64_t (&b)[8], uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t"
+      "setp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 q, %10, %10;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\tadd.u32 a4, %1, 32;\n\t"
+      "add.u32 a5, %1, 40;\n\tadd.u32 a6, %1, 48;\n\tadd.u32 a7, %1, 56;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %11, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], %3, %11, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], %4, %11, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], %5, %11, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], %6, %11, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], %7, %11, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], %8, %11, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], %9, %11, q;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
+      "r"(accumulate), "r"(idesc)
       : "memory");
 }
 
