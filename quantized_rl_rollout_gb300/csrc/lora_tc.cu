@@ -10,7 +10,7 @@
 //
 // LoRA CTAs, one per (128-token tile, K slice):
 //   warp 0      TMA: x [128 x 64] and A [R x 64] (R = r rounded up to 16;
-//               rows past M or r read as zeros), 128-byte swizzle, 6-stage ring
+//               rows past M or r read as zeros), 128-byte swizzle, 4-stage ring
 //   warp 1      MMA: 4 x tcgen05.mma kind::f16 (M128 x R x K16) per stage
 //   warps 2..5  epilogue: thread = token row.  With one slice (many tokens)
 //               t goes straight from TMEM to t'.  With several (decode, few
@@ -46,7 +46,7 @@ __device__ unsigned long long qrr_ptrace_buf[256][16];
 
 namespace {
 
-constexpr int kStages = 6;
+constexpr int kStages = 4;  // 97 KB: two CTAs per SM, so a decode prologue fits in one wave
 constexpr int kXBytes = 128 * 128;  // [128 x 64] bf16
 constexpr int kABytes = 64 * 128;   // up to [64 x 64] bf16
 constexpr int kStage = kXBytes + kABytes;

@@ -142,23 +142,29 @@ def test_grouped_layer_set(q, m):
                                   d["alpha"]), f"grouped layer {i} m={m}")
 
 
-def test_grouped_8b_decode_sampled(q):
-    """The 8B-class layer set at 64 tokens in one grouped call; sampled columns."""
+@pytest.mark.parametrize("m", [1, 8, 64])
+def test_grouped_8b_decode_sampled(q, m):
+    """The 8B-class layer set in one grouped call, the bench's launch
+    configuration: every CTA runs several units, so accumulator reuse, issuer
+    alternation across unit boundaries and split-K tickets all take part;
+    sampled columns of every 128-row tile."""
     g = np.random.default_rng(9)
     r = configs.DECODE_8B["r"]
     layers = []
     for layer in configs.LAYERS_8B:
         W, codes, scales, ts, A, B, alpha = _layer(q, layer.n, layer.k, r, f"g8b/{layer.name}")
-        x = inputs.activations(64, layer.k, inputs.derive_seed(0, "g8b-x", layer.name), device=DEV)
+        x = inputs.activations(m, layer.k, inputs.derive_seed(0, "g8b-x", layer.name, m), device=DEV)
         layers.append(dict(x=x, codes=codes, scales=scales, tensor_scale=ts, lora_A=A, lora_B=B, alpha=alpha))
         del W
     ys = q.linear_nvfp4_lora_grouped(layers)
     torch.cuda.synchronize()
     for layer, d, y in zip(configs.LAYERS_8B, layers, ys):
-        rows = np.unique(np.concatenate([[0, layer.n - 1], g.integers(0, layer.n, 126)]))
+        tiles = np.arange(layer.n // 128) * 128
+        rows = np.unique(np.concatenate([[0, layer.n - 1], tiles + g.integers(0, 128, tiles.size),
+                                         g.integers(0, layer.n, 64)]))
         y_ref = _ref(d["x"], d["codes"], d["scales"], d["tensor_scale"], d["lora_A"], d["lora_B"], d["alpha"],
                      rows=rows)
-        _assert_close(y[:, torch.from_numpy(rows).to(DEV)], y_ref, f"grouped 8B {layer.name}")
+        _assert_close(y[:, torch.from_numpy(rows).to(DEV)], y_ref, f"grouped 8B {layer.name} m={m}")
 
 
 @pytest.mark.parametrize("mode", [0, 1])
