@@ -13,6 +13,11 @@ tokens.  One step is one pass of the whole hot path over that layer set:
   fp8      FP8 path at M = 4096: activation 1x128 quantize, 128x128 weight
            re-quantize, blockwise-scaled GEMM
 
+On request (--phases ...,decode32b,requant32b) the 32B-class stack (64 layers
+of hidden 5120, LoRA r = 64) is measured too: decode at M = 64 (one grouped
+call per layer) and the full bf16 -> NVFP4 re-quantization of its 31.2 G
+weight elements.  It is another configuration, not part of the step.
+
 Each phase is timed with CUDA events on the launching stream after an L2
 flush (a 512 MB write), so no phase reads its weights from L2 left by the
 previous one.  ``value`` is the decode phase's HBM throughput: its
@@ -228,8 +233,51 @@ class Workload:
     def do_flush(self):
         self.flush.fill_(self.launches & 0xFF)
 
+    # -- 32B-class stack (built on first use: ~62 GB of bf16 masters) --
+    def _stack32(self):
+        if getattr(self, "s32", None) is None:
+            L, c = configs.LAYERS_32B, configs.DECODE_32B
+            masters, outs, groups = [], [], []
+            for li in range(c["depth"]):
+                grp = []
+                for l in L:
+                    masters.append(inputs.weight(l.n, l.k, inputs.derive_seed(0, "32b", li, l.name, "W"),
+                                                 device=self.dev))
+                    codes = torch.empty(l.n, l.k // 2, dtype=torch.uint8, device=self.dev)
+                    scales = torch.empty(l.n, l.k // 16, dtype=torch.uint8, device=self.dev)
+                    ts = torch.empty(1, dtype=torch.float32, device=self.dev)
+                    outs.append((codes, scales, ts))
+                    A, B, alpha = inputs.lora(c["r"], l.k, l.n, inputs.derive_seed(0, "32b", li, l.name, "lora"),
+                                              device=self.dev)
+                    x = inputs.activations(c["tokens"], l.k, inputs.derive_seed(0, "32b", li, l.name, "x"),
+                                           device=self.dev)
+                    grp.append(dict(x=x, codes=codes, scales=scales, tensor_scale=ts, lora_A=A, lora_B=B, alpha=alpha,
+                                    y=torch.empty(c["tokens"], l.n, dtype=torch.bfloat16, device=self.dev)))
+                groups.append(grp)
+            ws = torch.empty(self.q.linear_nvfp4_lora_grouped_workspace_bytes(groups[0]), dtype=torch.uint8,
+                             device=self.dev)
+            rq_ws = torch.empty(self.q.lib().qrr_requantize_workspace_bytes(len(masters)), dtype=torch.uint8,
+                                device=self.dev)
+            self.s32 = (masters, outs, groups, ws, rq_ws)
+            self.requant32()
+        return self.s32
 
+    def requant32(self):
+        masters, outs, _, _, rq_ws = self._stack32()
+        self.q.requantize_weights(masters, outs, self.q.FORMAT_NVFP4, workspace=rq_ws)
+        return 2 * ((len(masters) + 47) // 48)
+
+    def decode32(self):
+        _, _, groups, ws, _ = self._stack32()
+        for grp in groups:
+            self.q.linear_nvfp4_lora_grouped(grp, workspace=ws)
+        return 2 * len(groups)
+
+
+# one step over the 8B-class workload; the 32B-class stack (another
+# configuration, ~85 GB resident) is measured only when asked for by --phases
 PHASES = ["requant", "decode_m1", "decode_m8", "decode_m64", "prefill", "fp8_quant", "fp8_gemm"]
+EXTRA_PHASES = ["decode32b", "requant32b"]
 
 
 def run_phase(w, name):
@@ -241,6 +289,10 @@ def run_phase(w, name):
         return w.prefill()
     if name == "fp8_quant":
         return w.fp8_quant()
+    if name == "decode32b":
+        return w.decode32()
+    if name == "requant32b":
+        return w.requant32()
     return w.fp8_gemm()
 
 
@@ -453,6 +505,13 @@ def main():
             bw, ba = fp8_quant_bytes(L, PREFILL_TOKENS)
             breakdown[p] = {"ms": ms, "GB/s": (bw + ba) / ms / 1e6, "frac_hbm": (bw + ba) / ms / 1e6 / peaks["hbm_gbs"],
                             "bytes": bw + ba}
+        elif p == "decode32b":
+            c32 = configs.DECODE_32B
+            b = c32["depth"] * decode_bytes(configs.LAYERS_32B, c32["tokens"], c32["r"])
+            breakdown[p] = {"ms": ms, "GB/s": b / ms / 1e6, "frac_hbm": b / ms / 1e6 / peaks["hbm_gbs"], "bytes": b}
+        elif p == "requant32b":
+            b = configs.DECODE_32B["depth"] * requant_nvfp4_bytes(configs.LAYERS_32B)
+            breakdown[p] = {"ms": ms, "GB/s": b / ms / 1e6, "frac_hbm": b / ms / 1e6 / peaks["hbm_gbs"], "bytes": b}
         elif p == "fp8_gemm":
             f = sum(2 * PREFILL_TOKENS * l.n * l.k for l in L)
             breakdown[p] = {"ms": ms, "TFLOP/s": f / ms / 1e9, "frac_fp8_nominal": f / ms / 1e9 / fp8_peak, "flops": f}
