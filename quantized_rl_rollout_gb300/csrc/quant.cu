@@ -20,34 +20,49 @@ namespace qrr {
 // ---------------------------------------------------------------------------
 // NVFP4 pass 1: tensor absmax.  A block's absmax is the max of |bf16| bit
 // patterns; `amax_bits[j]` must be zero before the launch.
+//
+// Both passes copy the job table (chunk boundaries, pointers) into shared
+// memory once per CTA: looked up through the kernel parameters per chunk it
+// costs a dependent memory round trip before each chunk's loads can issue.
 
 // Each warp keeps a running max over the chunks it visits and publishes it
 // with one atomic per tensor it leaves (not one per chunk: same-address
 // atomics serialize in L2).
 __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __grid_constant__ Nvfp4Batch batch) {
+  __shared__ int64_t s_first[kMaxJobs + 1];
+  __shared__ int64_t s_nvec[kMaxJobs];
+  __shared__ const uint4* s_src[kMaxJobs];
+  const int count = batch.count;
   const int64_t chunks = batch.total_amax_chunks;
+  for (int j = threadIdx.x; j < count; j += blockDim.x) {
+    s_first[j] = batch.job[j].first_amax_chunk;
+    s_nvec[j] = batch.job[j].N * batch.job[j].K / 8;  // uint4 of 8 bf16
+    s_src[j] = reinterpret_cast<const uint4*>(batch.job[j].W);
+  }
+  if (threadIdx.x == 0) s_first[count] = chunks;
+  __syncthreads();
+  uint32_t* const amax_bits = batch.amax_bits;
+  int32_t* const status = batch.status;
   int cur = -1;
   uint32_t run = 0;
   auto publish = [&]() {
     const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, run);
     if ((threadIdx.x & 31) == 0 && m) {
-      atomicMax(batch.amax_bits + cur, m);
-      if (m >= 0x7F80u) flag(batch.status, QRR_DEV_NONFINITE);
+      atomicMax(amax_bits + cur, m);
+      if (m >= 0x7F80u) flag(status, QRR_DEV_NONFINITE);
     }
     run = 0;
   };
+  int j = 0;
   for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x) {
-    int j = 0;
-    while (j + 1 < batch.count && batch.job[j + 1].first_amax_chunk <= c) ++j;
+    while (s_first[j + 1] <= c) ++j;  // chunks only grow; s_first[count] = chunks ends the scan
     if (j != cur) {
       if (cur >= 0) publish();
       cur = j;
     }
-    // job fields into registers: read through the parameter reference they
-    // would be re-read after every store (aliasing), a memory round trip each
-    const int64_t nvec = batch.job[j].N * batch.job[j].K / 8;  // uint4 of 8 bf16
-    const int64_t base = (c - batch.job[j].first_amax_chunk) * kAmaxChunkVecs;
-    const uint4* src = reinterpret_cast<const uint4*>(batch.job[j].W);
+    const int64_t nvec = s_nvec[j];
+    const int64_t base = (c - s_first[j]) * kAmaxChunkVecs;
+    const uint4* src = s_src[j];
     uint4 v[kAmaxChunkVecs / 256];
 #pragma unroll
     for (int u = 0; u < kAmaxChunkVecs / 256; ++u) {
@@ -60,46 +75,77 @@ __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __grid_constant__
   if (cur >= 0) publish();
 }
 
-// NVFP4 pass 2: encode.  One thread per 16-element block; block b of a tensor
+// NVFP4 pass 2: encode.  One thread per 16-element block (two per step); block b of a tensor
 // is elements [16b, 16b+16) of the flat row-major matrix (K % 16 == 0), its
-// codes are bytes [8b, 8b+8) and its scale is byte b.
+// codes are bytes [8b, 8b+8) and its scale is byte b.  The chunks run in the
+// reverse of the absmax pass's order, so the first ones read what that pass
+// read last, while it is still in L2.
 __global__ void __launch_bounds__(256) nvfp4_encode_kernel(const __grid_constant__ Nvfp4Batch batch) {
+  __shared__ int64_t s_first[kMaxJobs + 1];
+  __shared__ int64_t s_nblocks[kMaxJobs];
+  __shared__ const uint4* s_src[kMaxJobs];
+  __shared__ uint8_t* s_codes[kMaxJobs];
+  __shared__ uint8_t* s_scales[kMaxJobs];
+  __shared__ float* s_ts[kMaxJobs];
+  __shared__ float s_st[kMaxJobs];
+  const int count = batch.count;
   const int64_t chunks = batch.total_encode_chunks;
-  for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x) {
-    int j = 0;
-    while (j + 1 < batch.count && batch.job[j + 1].first_encode_chunk <= c) ++j;
-    const int64_t nblocks = batch.job[j].N * batch.job[j].K / 16;
-    const int64_t b = (c - batch.job[j].first_encode_chunk) * 256 + threadIdx.x;
-    uint8_t* const codes = batch.job[j].codes;
-    uint8_t* const scales = batch.job[j].scales;
-    const float amax_t = bf16bits_to_f32(batch.amax_bits[j]);
-    const float s_t = __fdiv_rn(amax_t, 2688.0f);
-    if (b == 0) *batch.job[j].tensor_scale = s_t;
-    if (b >= nblocks) continue;
-    const uint4* src = reinterpret_cast<const uint4*>(batch.job[j].W) + 2 * b;
-    const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
-    uint32_t sb = 0;
-    uint2 packed = make_uint2(0u, 0u);
-    if (s_t > 0.0f) {
-      const float amax_b = bf16bits_to_f32(max(absmax_bits8(v0), absmax_bits8(v1)));
-      const float six_st = __fmul_rn(6.0f, s_t);
-      sb = cvt_e4m3x2(__fdiv_rn(amax_b, six_st), 0.0f) & 0xFFu;
-      const float d = __fmul_rn(e4m3_to_f32(sb), s_t);
-      if (d > 0.0f) {
-        const SharedDivisor div(d);  // 16 quotients x / d, each correctly rounded
-        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        uint32_t out[2] = {0u, 0u};
+  for (int j = threadIdx.x; j < count; j += blockDim.x) {
+    s_first[j] = batch.job[j].first_encode_chunk;
+    s_nblocks[j] = batch.job[j].N * batch.job[j].K / 16;
+    s_src[j] = reinterpret_cast<const uint4*>(batch.job[j].W);
+    s_codes[j] = batch.job[j].codes;
+    s_scales[j] = batch.job[j].scales;
+    s_ts[j] = batch.job[j].tensor_scale;
+    s_st[j] = __fdiv_rn(bf16bits_to_f32(batch.amax_bits[j]), 2688.0f);
+  }
+  if (threadIdx.x == 0) s_first[count] = chunks;
+  __syncthreads();
+  int j = count - 1;
+  for (int64_t k = blockIdx.x; k < chunks; k += gridDim.x) {
+    const int64_t c = chunks - 1 - k;
+    while (s_first[j] > c) --j;  // chunks only shrink
+    const float s_t = s_st[j];
+    const int64_t nb = s_nblocks[j];
+    // two blocks per thread, both loaded before either is encoded
+    const int64_t b0 = (c - s_first[j]) * 512 + threadIdx.x;
+    if (b0 == 0) *s_ts[j] = s_t;
+    uint4 v[2][2];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float q0 = div(bf16_lo(w[i]));
-          const float q1 = div(bf16_hi(w[i]));
-          out[i >> 2] |= cvt_e2m1x2(q0, q1) << (8 * (i & 3));
-        }
-        packed = make_uint2(out[0], out[1]);
-      }
+    for (int h = 0; h < 2; ++h) {
+      const int64_t b = b0 + 256 * h;
+      const uint4* src = s_src[j] + 2 * b;
+      v[h][0] = b < nb ? __ldg(src) : make_uint4(0, 0, 0, 0);
+      v[h][1] = b < nb ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
     }
-    reinterpret_cast<uint2*>(codes)[b] = packed;
-    scales[b] = static_cast<uint8_t>(sb);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t b = b0 + 256 * h;
+      if (b >= nb) continue;
+      uint32_t sb = 0;
+      uint2 packed = make_uint2(0u, 0u);
+      if (s_t > 0.0f) {
+        const float amax_b = bf16bits_to_f32(max(absmax_bits8(v[h][0]), absmax_bits8(v[h][1])));
+        const float six_st = __fmul_rn(6.0f, s_t);
+        sb = cvt_e4m3x2(__fdiv_rn(amax_b, six_st), 0.0f) & 0xFFu;
+        const float d = __fmul_rn(e4m3_to_f32(sb), s_t);
+        if (d > 0.0f) {
+          const SharedDivisor div(d);  // 16 quotients x / d, each correctly rounded
+          const uint32_t w[8] = {v[h][0].x, v[h][0].y, v[h][0].z, v[h][0].w,
+                                 v[h][1].x, v[h][1].y, v[h][1].z, v[h][1].w};
+          uint32_t out[2] = {0u, 0u};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float q0 = div(bf16_lo(w[i]));
+            const float q1 = div(bf16_hi(w[i]));
+            out[i >> 2] |= cvt_e2m1x2(q0, q1) << (8 * (i & 3));
+          }
+          packed = make_uint2(out[0], out[1]);
+        }
+      }
+      reinterpret_cast<uint2*>(s_codes[j])[b] = packed;
+      s_scales[j][b] = static_cast<uint8_t>(sb);
+    }
   }
 }
 
@@ -111,41 +157,51 @@ __global__ void __launch_bounds__(256) nvfp4_encode_kernel(const __grid_constant
 __global__ void __launch_bounds__(256) fp8_a1x128_kernel(const uint16_t* __restrict__ x, int64_t nvec,
                                                         uint8_t* __restrict__ q, float* __restrict__ scales,
                                                         int mode, int32_t* status) {
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  // the loop test is uniform across the warp (its first element), so every
-  // shuffle below has all 32 lanes; nvec is a multiple of 16, so a half warp is
-  // wholly live or wholly past the end
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i - (threadIdx.x & 31) < nvec;
-       i += stride) {
-    const bool live = i < nvec;
-    const uint4 v = live ? __ldg(reinterpret_cast<const uint4*>(x) + i) : make_uint4(0, 0, 0, 0);
-    uint32_t m = absmax_bits8(v);
+  // U vectors per thread per step, all loads issued first: one 16-byte load
+  // in flight per thread is too few bytes in flight per SM to cover HBM latency
+  constexpr int U = 4;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * U;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * U; base < nvec; base += stride) {
+    uint4 v[U];
 #pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    if (!live) continue;
-    if (m >= 0x7F80u && (threadIdx.x & 15) == 0) flag(status, QRR_DEV_NONFINITE);
-    const float amax = bf16bits_to_f32(m);
-    const float v448 = __fdiv_rn(amax, 448.0f);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t out[2] = {0u, 0u};
-    float s = 0.0f;
-    if (v448 > 0.0f) {
-      if (mode == QRR_SCALE_FP32) {
-        s = v448;
-        const SharedDivisor div(s);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) out[k >> 1] |= cvt_e4m3x2(div(bf16_lo(w[k])), div(bf16_hi(w[k]))) << (16 * (k & 1));
-      } else {
-        const int e = pow2_ceil_exp(v448);
-        s = pow2_from_exp(e);
-        const Pow2Scaler sc(e);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          out[k >> 1] |= cvt_e4m3x2(sc(bf16_lo(w[k])), sc(bf16_hi(w[k]))) << (16 * (k & 1));
-      }
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = base + u * 256 + threadIdx.x;
+      v[u] = i < nvec ? __ldg(reinterpret_cast<const uint4*>(x) + i) : make_uint4(0, 0, 0, 0);
     }
-    reinterpret_cast<uint2*>(q)[i] = make_uint2(out[0], out[1]);
-    if ((threadIdx.x & 15) == 0) scales[i >> 4] = s;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = base + u * 256 + threadIdx.x;
+      // all 32 lanes shuffle; nvec is a multiple of 16, so a half warp (one
+      // 128-block) is wholly live or wholly past the end
+      uint32_t m = absmax_bits8(v[u]);
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+      if (i >= nvec) continue;
+      if (m >= 0x7F80u && (threadIdx.x & 15) == 0) flag(status, QRR_DEV_NONFINITE);
+      const float amax = bf16bits_to_f32(m);
+      const float v448 = __fdiv_rn(amax, 448.0f);
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      uint32_t out[2] = {0u, 0u};
+      float s = 0.0f;
+      if (v448 > 0.0f) {
+        if (mode == QRR_SCALE_FP32) {
+          s = v448;
+          const SharedDivisor div(s);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            out[k >> 1] |= cvt_e4m3x2(div(bf16_lo(w[k])), div(bf16_hi(w[k]))) << (16 * (k & 1));
+        } else {
+          const int e = pow2_ceil_exp(v448);
+          s = pow2_from_exp(e);
+          const Pow2Scaler sc(e);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            out[k >> 1] |= cvt_e4m3x2(sc(bf16_lo(w[k])), sc(bf16_hi(w[k]))) << (16 * (k & 1));
+        }
+      }
+      reinterpret_cast<uint2*>(q)[i] = make_uint2(out[0], out[1]);
+      if ((threadIdx.x & 15) == 0) scales[i >> 4] = s;
+    }
   }
 }
 
@@ -157,16 +213,21 @@ __global__ void __launch_bounds__(256) fp8_a1x128_kernel(const uint16_t* __restr
 
 __global__ void __launch_bounds__(256) fp8_w128_kernel(const __grid_constant__ Fp8WBatch batch) {
   __shared__ uint32_t warp_max[8];
-  for (int64_t t = blockIdx.x; t < batch.total_tiles; t += gridDim.x) {
-    int j = 0;
-    while (j + 1 < batch.count && batch.job[j + 1].first_tile <= t) ++j;
-    // job fields into registers (see the NVFP4 kernels)
+  __shared__ int64_t s_first[kMaxJobs + 1];  // job table in shared memory (see the NVFP4 kernels)
+  const int count = batch.count;
+  const int64_t total = batch.total_tiles;
+  for (int j = threadIdx.x; j < count; j += blockDim.x) s_first[j] = batch.job[j].first_tile;
+  if (threadIdx.x == 0) s_first[count] = total;
+  __syncthreads();
+  const int mode = batch.mode;
+  int j = 0;
+  for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+    while (s_first[j + 1] <= t) ++j;  // tiles only grow
     const int64_t N = batch.job[j].N, K = batch.job[j].K;
     const uint16_t* const W = batch.job[j].W;
     uint8_t* const qout = batch.job[j].q;
     float* const scales = batch.job[j].scales;
-    const int mode = batch.mode;
-    const int64_t local = t - batch.job[j].first_tile;
+    const int64_t local = t - s_first[j];
     const int64_t kt = K / 128;
     const int64_t tr = local / kt, tc = local % kt;
     const int64_t row0 = tr * 128;
@@ -252,8 +313,8 @@ cudaError_t launch_nvfp4(Nvfp4Batch& batch, cudaStream_t stream) {
     job.first_encode_chunk = enc_chunks;
     const int64_t nvec = job.N * job.K / 8;
     amax_chunks += (nvec + kAmaxChunkVecs - 1) / kAmaxChunkVecs;
-    // every tensor gets at least one encode chunk: block 0's thread writes s_t
-    enc_chunks += std::max<int64_t>(1, (job.N * job.K / 16 + 255) / 256);
+    // every tensor gets at least one encode chunk (512 blocks): block 0's thread writes s_t
+    enc_chunks += std::max<int64_t>(1, (job.N * job.K / 16 + 511) / 512);
   }
   batch.total_amax_chunks = amax_chunks;
   batch.total_encode_chunks = enc_chunks;
@@ -268,8 +329,8 @@ cudaError_t launch_fp8_a1x128(const void* x, int64_t M, int64_t K, uint8_t* q, f
                               int32_t* status, cudaStream_t stream) {
   const int64_t nvec = M * K / 8;
   if (nvec == 0) return cudaSuccess;
-  fp8_a1x128_kernel<<<grid_for((nvec + 255) / 256, 8), 256, 0, stream>>>(static_cast<const uint16_t*>(x), nvec, q,
-                                                                           scales, mode, status);
+  fp8_a1x128_kernel<<<grid_for((nvec + 1023) / 1024, 8), 256, 0, stream>>>(static_cast<const uint16_t*>(x), nvec, q,
+                                                                            scales, mode, status);
   return cudaGetLastError();
 }
 
