@@ -23,6 +23,19 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
   return r;
 }
 
+// Eight fp32 -> one word of eight E2M1 codes, value k in nibble k: four
+// conversions whose bytes are packed by one register move.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&v)[8]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\tcvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\tcvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
 // Two fp32 -> two E4M3 bytes; `lo` lands in bits 7..0.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   uint16_t r;
@@ -36,6 +49,16 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
   float mag = e ? __uint_as_float(((e + 120u) << 23) | (m << 20))  // (1 + m/8) 2^(e-7)
                 : static_cast<float>(m) * 0.001953125f;            // m 2^-9
   return __uint_as_float(__float_as_uint(mag) | ((b & 0x80u) << 24));
+}
+
+// The same value through the hardware conversion (every E4M3 value is an
+// f16, and every f16 an fp32).
+__device__ __forceinline__ float e4m3_to_f32_cvt(uint32_t b) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h2) : "r"(b));
+  float f;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}" : "=f"(f) : "r"(h2));
+  return f;
 }
 
 // bf16 bits -> fp32 (exact).
@@ -107,6 +130,7 @@ struct Pow2Scaler {
 struct SharedDivisor {
   float d, y;
   bool ok;
+  SharedDivisor() = default;
   __device__ __forceinline__ explicit SharedDivisor(float d_) : d(d_) {
     y = __frcp_rn(d_);
     const float ad = fabsf(d_);
@@ -117,6 +141,41 @@ struct SharedDivisor {
     const float q0 = __fmul_rn(x, y);
     const float q1 = __fmaf_rn(__fmaf_rn(-q0, d, x), y, q0);
     return copysignf(__fmaf_rn(__fmaf_rn(-q1, d, x), y, q1), x);
+  }
+};
+
+// The same division for two numerators at once on the paired fp32 pipe
+// (fma.rn.f32x2: each half an ordinary correctly-rounded fp32 FMA, so the
+// quotients are bit-identical to SharedDivisor's).  The residual x - q d is
+// formed as fma(q, -d, x), the same exact value as fma(-q, d, x).
+struct SharedDivisor2 {
+  float d;
+  uint64_t y2, nd2;
+  bool ok;
+  __device__ __forceinline__ explicit SharedDivisor2(float d_) : d(d_) {
+    const float y = __frcp_rn(d_);
+    const float ad = fabsf(d_);
+    ok = ad >= 1.0e-20f && ad <= 1.0e20f;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(y2) : "f"(y));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(nd2) : "f"(-d_));
+  }
+  __device__ __forceinline__ void operator()(float x0, float x1, float& q0, float& q1) const {
+    if (!ok) {
+      q0 = __fdiv_rn(x0, d);
+      q1 = __fdiv_rn(x1, d);
+      return;
+    }
+    uint64_t x, q, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q) : "l"(x), "l"(y2));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(q), "l"(nd2), "l"(x));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(r), "l"(y2), "l"(q));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(q), "l"(nd2), "l"(x));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(r), "l"(y2), "l"(q));
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(q));
+    q0 = copysignf(a, x0);
+    q1 = copysignf(b, x1);
   }
 };
 

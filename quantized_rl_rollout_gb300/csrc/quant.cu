@@ -14,36 +14,91 @@
 // codes with one scale per 1x128 activation block / 128x128 weight tile,
 // s = amax/448 or the next power of two.
 #include "quant.cuh"
+#include "tc.cuh"
 
 namespace qrr {
 
 // ---------------------------------------------------------------------------
-// NVFP4 pass 1: tensor absmax.  A block's absmax is the max of |bf16| bit
-// patterns; `amax_bits[j]` must be zero before the launch.
-//
-// Both passes copy the job table (chunk boundaries, pointers) into shared
-// memory once per CTA: looked up through the kernel parameters per chunk it
-// costs a dependent memory round trip before each chunk's loads can issue.
+// NVFP4, both passes streamed through shared memory by bulk copies (TMA):
+// one thread keeps kStreamStages chunks of kStreamChunk bytes in flight per
+// CTA, two CTAs per SM, whatever the registers the arithmetic needs (loads
+// into registers cap the bytes in flight by occupancy).  A chunk lies inside
+// one tensor; chunk c of the launch is taken by CTA c mod grid.  The job table
+// (chunk boundaries, pointers) sits in shared memory.
 
-// Each warp keeps a running max over the chunks it visits and publishes it
-// with one atomic per tensor it leaves (not one per chunk: same-address
-// atomics serialize in L2).
+namespace {
+
+constexpr int kStreamChunk = 16384;  // bytes: 8192 bf16, 512 NVFP4 blocks
+constexpr int kStreamStages = 6;     // absmax: 2 CTAs per SM
+constexpr int kEncodeStages = 4;     // encode: 3 CTAs per SM (more warps for its arithmetic)
+
+struct StreamRing {
+  uint64_t full[kStreamStages], empty[kStreamStages];
+  int abort;
+};
+
+// Producer side, run by thread 0 before consuming step i: issue the load of
+// the CTA's step i + kStreamStages - 1 once that ring slot has been consumed.
+template <int S, typename ChunkSrc>
+__device__ __forceinline__ bool stream_issue(StreamRing& r, uint8_t* ring, int64_t step, int64_t steps,
+                                             const ChunkSrc& src_of, int32_t* status) {
+  if (step >= steps) return true;
+  const int s = static_cast<int>(step % S);
+  const int64_t use = step / S;
+  if (use > 0 && !mbar_wait(&r.empty[s], (use - 1) & 1, &r.abort, status)) return false;
+  const void* src;
+  uint32_t bytes;
+  src_of(step, src, bytes);
+  mbar_arrive_expect_tx(&r.full[s], bytes);
+  bulk_load(ring + static_cast<size_t>(s) * kStreamChunk, src, bytes, &r.full[s]);
+  return true;
+}
+
+}  // namespace
+
+// NVFP4 pass 1: tensor absmax.  A block's absmax is the max of |bf16| bit
+// patterns; `amax_bits[j]` must be zero before the launch.  Each warp keeps a
+// running max over its chunks and publishes it with one atomic per tensor it
+// leaves (same-address atomics serialize in L2).
 __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __grid_constant__ Nvfp4Batch batch) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* ring = smem_raw;
+  StreamRing& r = *reinterpret_cast<StreamRing*>(smem_raw + kStreamStages * kStreamChunk);
   __shared__ int64_t s_first[kMaxJobs + 1];
-  __shared__ int64_t s_nvec[kMaxJobs];
-  __shared__ const uint4* s_src[kMaxJobs];
+  __shared__ int64_t s_bytes[kMaxJobs];
+  __shared__ const uint8_t* s_src[kMaxJobs];
   const int count = batch.count;
   const int64_t chunks = batch.total_amax_chunks;
   for (int j = threadIdx.x; j < count; j += blockDim.x) {
     s_first[j] = batch.job[j].first_amax_chunk;
-    s_nvec[j] = batch.job[j].N * batch.job[j].K / 8;  // uint4 of 8 bf16
-    s_src[j] = reinterpret_cast<const uint4*>(batch.job[j].W);
+    s_bytes[j] = batch.job[j].N * batch.job[j].K * 2;
+    s_src[j] = reinterpret_cast<const uint8_t*>(batch.job[j].W);
   }
-  if (threadIdx.x == 0) s_first[count] = chunks;
+  if (threadIdx.x == 0) {
+    s_first[count] = chunks;
+    for (int s = 0; s < kStreamStages; ++s) {
+      mbar_init(&r.full[s], 1);
+      mbar_init(&r.empty[s], 8);  // one arrival per warp
+    }
+    r.abort = 0;
+    fence_barrier_init();
+  }
   __syncthreads();
   uint32_t* const amax_bits = batch.amax_bits;
   int32_t* const status = batch.status;
-  int cur = -1;
+  const int64_t steps = chunks > blockIdx.x ? (chunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  int jp = 0;  // producer's job cursor
+  auto src_of = [&](int64_t step, const void*& src, uint32_t& bytes) {
+    const int64_t c = blockIdx.x + step * gridDim.x;
+    while (s_first[jp + 1] <= c) ++jp;
+    const int64_t off = (c - s_first[jp]) * kStreamChunk;
+    src = s_src[jp] + off;
+    const int64_t left = s_bytes[jp] - off;
+    bytes = static_cast<uint32_t>(left < kStreamChunk ? left : kStreamChunk);
+  };
+  if (threadIdx.x == 0)
+    for (int64_t i = 0; i < kStreamStages - 1; ++i) stream_issue<kStreamStages>(r, ring, i, steps, src_of, status);
+  int cur = -1, j = 0;
   uint32_t run = 0;
   auto publish = [&]() {
     const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, run);
@@ -53,99 +108,129 @@ __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __grid_constant__
     }
     run = 0;
   };
-  int j = 0;
-  for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x) {
-    while (s_first[j + 1] <= c) ++j;  // chunks only grow; s_first[count] = chunks ends the scan
+  for (int64_t i = 0; i < steps; ++i) {
+    if (threadIdx.x == 0 && !stream_issue<kStreamStages>(r, ring, i + kStreamStages - 1, steps, src_of, status)) break;
+    const int s = static_cast<int>(i % kStreamStages);
+    if (!mbar_wait(&r.full[s], (i / kStreamStages) & 1, &r.abort, status)) break;
+    const int64_t c = blockIdx.x + i * gridDim.x;
+    while (s_first[j + 1] <= c) ++j;
     if (j != cur) {
       if (cur >= 0) publish();
       cur = j;
     }
-    const int64_t nvec = s_nvec[j];
-    const int64_t base = (c - s_first[j]) * kAmaxChunkVecs;
-    const uint4* src = s_src[j];
-    uint4 v[kAmaxChunkVecs / 256];
+    const int64_t left = s_bytes[j] - (c - s_first[j]) * kStreamChunk;
+    const int nvec = static_cast<int>((left < kStreamChunk ? left : kStreamChunk) / 16);
+    const uint4* v = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * kStreamChunk);
 #pragma unroll
-    for (int u = 0; u < kAmaxChunkVecs / 256; ++u) {
-      const int64_t i = base + u * 256 + threadIdx.x;
-      v[u] = i < nvec ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+    for (int u = 0; u < kStreamChunk / 16 / 256; ++u) {
+      const int e = u * 256 + threadIdx.x;
+      if (e < nvec) run = max(run, absmax_bits8(v[e]));
     }
-#pragma unroll
-    for (int u = 0; u < kAmaxChunkVecs / 256; ++u) run = max(run, absmax_bits8(v[u]));
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&r.empty[s]);
   }
   if (cur >= 0) publish();
+  // every issued copy has landed before the CTA exits
+  if (threadIdx.x == 0) {
+    volatile int no_abort = 0;
+    for (int64_t k = steps - 1; k >= 0 && k >= steps - kStreamStages; --k)
+      mbar_wait(&r.full[k % kStreamStages], (k / kStreamStages) & 1, &no_abort, status);
+  }
 }
 
-// NVFP4 pass 2: encode.  One thread per 16-element block (two per step); block b of a tensor
-// is elements [16b, 16b+16) of the flat row-major matrix (K % 16 == 0), its
-// codes are bytes [8b, 8b+8) and its scale is byte b.  The chunks run in the
-// reverse of the absmax pass's order, so the first ones read what that pass
-// read last, while it is still in L2.
-__global__ void __launch_bounds__(256) nvfp4_encode_kernel(const __grid_constant__ Nvfp4Batch batch) {
+// NVFP4 pass 2: encode.  Block b of a tensor (16 elements, K % 16 == 0) is
+// elements [16b, 16b+16) of the flat row-major matrix; its codes are bytes
+// [8b, 8b+8) and its scale is byte b.  512 threads, one block of a chunk
+// each (the encode is arithmetic-heavy: more warps hide its latency).  The
+// chunks run in the reverse of the absmax pass's order, so the first ones
+// read what that pass read last, while it is still in L2.
+__global__ void __launch_bounds__(512, 3) nvfp4_encode_kernel(const __grid_constant__ Nvfp4Batch batch) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* ring = smem_raw;
+  StreamRing& r = *reinterpret_cast<StreamRing*>(smem_raw + kEncodeStages * kStreamChunk);
   __shared__ int64_t s_first[kMaxJobs + 1];
-  __shared__ int64_t s_nblocks[kMaxJobs];
-  __shared__ const uint4* s_src[kMaxJobs];
+  __shared__ int64_t s_bytes[kMaxJobs];
+  __shared__ const uint8_t* s_src[kMaxJobs];
   __shared__ uint8_t* s_codes[kMaxJobs];
   __shared__ uint8_t* s_scales[kMaxJobs];
   __shared__ float* s_ts[kMaxJobs];
   __shared__ float s_st[kMaxJobs];
+  __shared__ SharedDivisor s_six[kMaxJobs];  // the per-tensor divisor 6 s_t of every block's absmax
   const int count = batch.count;
   const int64_t chunks = batch.total_encode_chunks;
   for (int j = threadIdx.x; j < count; j += blockDim.x) {
     s_first[j] = batch.job[j].first_encode_chunk;
-    s_nblocks[j] = batch.job[j].N * batch.job[j].K / 16;
-    s_src[j] = reinterpret_cast<const uint4*>(batch.job[j].W);
+    s_bytes[j] = batch.job[j].N * batch.job[j].K * 2;
+    s_src[j] = reinterpret_cast<const uint8_t*>(batch.job[j].W);
     s_codes[j] = batch.job[j].codes;
     s_scales[j] = batch.job[j].scales;
     s_ts[j] = batch.job[j].tensor_scale;
     s_st[j] = __fdiv_rn(bf16bits_to_f32(batch.amax_bits[j]), 2688.0f);
+    s_six[j] = SharedDivisor(__fmul_rn(6.0f, s_st[j]));
   }
-  if (threadIdx.x == 0) s_first[count] = chunks;
+  if (threadIdx.x == 0) {
+    s_first[count] = chunks;
+    for (int s = 0; s < kEncodeStages; ++s) {
+      mbar_init(&r.full[s], 1);
+      mbar_init(&r.empty[s], 16);  // one arrival per warp
+    }
+    r.abort = 0;
+    fence_barrier_init();
+  }
   __syncthreads();
+  int32_t* const status = batch.status;
+  const int64_t steps = chunks > blockIdx.x ? (chunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  int jp = count - 1;  // producer's job cursor (chunks shrink)
+  auto chunk_of = [&](int64_t step) { return chunks - 1 - (blockIdx.x + step * gridDim.x); };
+  auto src_of = [&](int64_t step, const void*& src, uint32_t& bytes) {
+    const int64_t c = chunk_of(step);
+    while (s_first[jp] > c) --jp;
+    const int64_t off = (c - s_first[jp]) * kStreamChunk;
+    src = s_src[jp] + off;
+    const int64_t left = s_bytes[jp] - off;
+    bytes = static_cast<uint32_t>(left < kStreamChunk ? left : kStreamChunk);
+  };
+  if (threadIdx.x == 0)
+    for (int64_t i = 0; i < kEncodeStages - 1; ++i) stream_issue<kEncodeStages>(r, ring, i, steps, src_of, status);
   int j = count - 1;
-  for (int64_t k = blockIdx.x; k < chunks; k += gridDim.x) {
-    const int64_t c = chunks - 1 - k;
-    while (s_first[j] > c) --j;  // chunks only shrink
+  for (int64_t i = 0; i < steps; ++i) {
+    if (threadIdx.x == 0 && !stream_issue<kEncodeStages>(r, ring, i + kEncodeStages - 1, steps, src_of, status)) break;
+    const int s = static_cast<int>(i % kEncodeStages);
+    const int64_t c = chunk_of(i);
+    while (s_first[j] > c) --j;
     const float s_t = s_st[j];
-    const int64_t nb = s_nblocks[j];
-    // two blocks per thread, both loaded before either is encoded
-    const int64_t b0 = (c - s_first[j]) * 512 + threadIdx.x;
-    if (b0 == 0) *s_ts[j] = s_t;
-    uint4 v[2][2];
+    const int64_t nb = s_bytes[j] / 32;                    // blocks of the tensor
+    const int64_t b0 = (c - s_first[j]) * (kStreamChunk / 32);  // first block of the chunk
+    if (b0 == 0 && threadIdx.x == 0) *s_ts[j] = s_t;
+    if (!mbar_wait(&r.full[s], (i / kEncodeStages) & 1, &r.abort, status)) break;
+    const uint4* v = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * kStreamChunk);
+    const uint4 x0 = v[2 * threadIdx.x], x1 = v[2 * threadIdx.x + 1];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&r.empty[s]);
+    const int64_t b = b0 + threadIdx.x;
+    if (b >= nb) continue;
+    uint32_t sb = 0;
+    uint2 packed = make_uint2(0u, 0u);
+    if (s_t > 0.0f) {
+      const float amax_b = bf16bits_to_f32(max(absmax_bits8(x0), absmax_bits8(x1)));
+      sb = cvt_e4m3x2(s_six[j](amax_b), 0.0f) & 0xFFu;
+      const float d = __fmul_rn(e4m3_to_f32_cvt(sb), s_t);
+      if (d > 0.0f) {
+        const SharedDivisor2 div(d);  // 16 quotients x / d, each correctly rounded
+        const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        float q[2][8];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t b = b0 + 256 * h;
-      const uint4* src = s_src[j] + 2 * b;
-      v[h][0] = b < nb ? __ldg(src) : make_uint4(0, 0, 0, 0);
-      v[h][1] = b < nb ? __ldg(src + 1) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t b = b0 + 256 * h;
-      if (b >= nb) continue;
-      uint32_t sb = 0;
-      uint2 packed = make_uint2(0u, 0u);
-      if (s_t > 0.0f) {
-        const float amax_b = bf16bits_to_f32(max(absmax_bits8(v[h][0]), absmax_bits8(v[h][1])));
-        const float six_st = __fmul_rn(6.0f, s_t);
-        sb = cvt_e4m3x2(__fdiv_rn(amax_b, six_st), 0.0f) & 0xFFu;
-        const float d = __fmul_rn(e4m3_to_f32(sb), s_t);
-        if (d > 0.0f) {
-          const SharedDivisor div(d);  // 16 quotients x / d, each correctly rounded
-          const uint32_t w[8] = {v[h][0].x, v[h][0].y, v[h][0].z, v[h][0].w,
-                                 v[h][1].x, v[h][1].y, v[h][1].z, v[h][1].w};
-          uint32_t out[2] = {0u, 0u};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float q0 = div(bf16_lo(w[i]));
-            const float q1 = div(bf16_hi(w[i]));
-            out[i >> 2] |= cvt_e2m1x2(q0, q1) << (8 * (i & 3));
-          }
-          packed = make_uint2(out[0], out[1]);
-        }
+        for (int k = 0; k < 8; ++k) div(bf16_lo(w[k]), bf16_hi(w[k]), q[k >> 2][2 * (k & 3)], q[k >> 2][2 * (k & 3) + 1]);
+        packed = make_uint2(cvt_e2m1x8(q[0]), cvt_e2m1x8(q[1]));
       }
-      reinterpret_cast<uint2*>(s_codes[j])[b] = packed;
-      s_scales[j][b] = static_cast<uint8_t>(sb);
     }
+    reinterpret_cast<uint2*>(s_codes[j])[b] = packed;
+    s_scales[j][b] = static_cast<uint8_t>(sb);
+  }
+  if (threadIdx.x == 0) {
+    volatile int no_abort = 0;
+    for (int64_t k = steps - 1; k >= 0 && k >= steps - kEncodeStages; --k)
+      mbar_wait(&r.full[k % kEncodeStages], (k / kEncodeStages) & 1, &no_abort, status);
   }
 }
 
@@ -186,10 +271,13 @@ __global__ void __launch_bounds__(256) fp8_a1x128_kernel(const uint16_t* __restr
       if (v448 > 0.0f) {
         if (mode == QRR_SCALE_FP32) {
           s = v448;
-          const SharedDivisor div(s);
+          const SharedDivisor2 div(s);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            out[k >> 1] |= cvt_e4m3x2(div(bf16_lo(w[k])), div(bf16_hi(w[k]))) << (16 * (k & 1));
+          for (int k = 0; k < 4; ++k) {
+            float a, b;
+            div(bf16_lo(w[k]), bf16_hi(w[k]), a, b);
+            out[k >> 1] |= cvt_e4m3x2(a, b) << (16 * (k & 1));
+          }
         } else {
           const int e = pow2_ceil_exp(v448);
           s = pow2_from_exp(e);
@@ -265,7 +353,7 @@ __global__ void __launch_bounds__(256) fp8_w128_kernel(const __grid_constant__ F
     }
     if (threadIdx.x == 0) scales[tr * kt + tc] = s;
     const Pow2Scaler sc(e);
-    const SharedDivisor div(s > 0.0f ? s : 1.0f);
+    const SharedDivisor2 div(s > 0.0f ? s : 1.0f);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int64_t row = row0 + u * 16 + (threadIdx.x >> 4);
@@ -275,8 +363,13 @@ __global__ void __launch_bounds__(256) fp8_w128_kernel(const __grid_constant__ F
       if (s > 0.0f) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float a = mode == QRR_SCALE_FP32 ? div(bf16_lo(w[k])) : sc(bf16_lo(w[k]));
-          const float b = mode == QRR_SCALE_FP32 ? div(bf16_hi(w[k])) : sc(bf16_hi(w[k]));
+          float a, b;
+          if (mode == QRR_SCALE_FP32) {
+            div(bf16_lo(w[k]), bf16_hi(w[k]), a, b);
+          } else {
+            a = sc(bf16_lo(w[k]));
+            b = sc(bf16_hi(w[k]));
+          }
           out[k >> 1] |= cvt_e4m3x2(a, b) << (16 * (k & 1));
         }
       }
@@ -305,23 +398,35 @@ int grid_for(int64_t work_units, int per_sm) {
   return static_cast<int>(work_units < cap ? (work_units > 0 ? work_units : 1) : cap);
 }
 
+constexpr int kNvfp4Chunk = kStreamChunk;
+constexpr int kNvfp4Smem = kStreamStages * kStreamChunk + static_cast<int>(sizeof(StreamRing));
+constexpr int kEncodeSmem = kEncodeStages * kStreamChunk + static_cast<int>(sizeof(StreamRing));
+
 cudaError_t launch_nvfp4(Nvfp4Batch& batch, cudaStream_t stream) {
   int64_t amax_chunks = 0, enc_chunks = 0;
   for (int j = 0; j < batch.count; ++j) {
     Nvfp4Job& job = batch.job[j];
     job.first_amax_chunk = amax_chunks;
     job.first_encode_chunk = enc_chunks;
-    const int64_t nvec = job.N * job.K / 8;
-    amax_chunks += (nvec + kAmaxChunkVecs - 1) / kAmaxChunkVecs;
-    // every tensor gets at least one encode chunk (512 blocks): block 0's thread writes s_t
-    enc_chunks += std::max<int64_t>(1, (job.N * job.K / 16 + 511) / 512);
+    const int64_t bytes = job.N * job.K * 2;
+    amax_chunks += (bytes + kNvfp4Chunk - 1) / kNvfp4Chunk;
+    // every tensor gets at least one encode chunk: its first thread writes s_t
+    enc_chunks += std::max<int64_t>(1, (bytes + kNvfp4Chunk - 1) / kNvfp4Chunk);
   }
   batch.total_amax_chunks = amax_chunks;
   batch.total_encode_chunks = enc_chunks;
   cudaError_t err = cudaMemsetAsync(batch.amax_bits, 0, sizeof(uint32_t) * batch.count, stream);
   if (err != cudaSuccess) return err;
-  if (amax_chunks > 0) nvfp4_amax_kernel<<<grid_for(amax_chunks, 8), 256, 0, stream>>>(batch);
-  nvfp4_encode_kernel<<<grid_for(enc_chunks, 8), 256, 0, stream>>>(batch);
+  static bool attr = false;
+  if (!attr) {
+    err = cudaFuncSetAttribute(nvfp4_amax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kNvfp4Smem);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(nvfp4_encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kEncodeSmem);
+    if (err != cudaSuccess) return err;
+    attr = true;
+  }
+  if (amax_chunks > 0) nvfp4_amax_kernel<<<grid_for(amax_chunks, 2), 256, kNvfp4Smem, stream>>>(batch);
+  nvfp4_encode_kernel<<<grid_for(enc_chunks, 3), 512, kEncodeSmem, stream>>>(batch);
   return cudaGetLastError();
 }
 

@@ -11,7 +11,6 @@
 namespace qrr {
 
 constexpr int kMaxJobs = 48;          // tensors per grouped launch (kernel parameters stay < 4 KB)
-constexpr int kAmaxChunkVecs = 1024;  // uint4 per absmax work chunk (16 KB of bf16)
 
 struct Nvfp4Job {
   const uint16_t* W;  // bf16 [N, K]
