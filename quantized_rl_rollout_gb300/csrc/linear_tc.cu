@@ -432,32 +432,59 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
       tc_fence_after();
       const float g = st > 0.0f ? st : 1.0f;
       const int m0 = mt * BN;
-      float* const part = splits > 1 ? partial + static_cast<int64_t>(sp) * M * N : nullptr;
+      // split-K is planned for the decode (f16) path only
+      float* const part = (F16 && splits > 1) ? partial + static_cast<int64_t>(sp) * M * N : nullptr;
       constexpr int CW = BN == 16 ? 16 : 32;
+      // Every test below is warp-uniform and taken once per slab: with one
+      // epilogue warp per sub-partition, a branch per element would cost a
+      // branch resolution each (about ten times the slab's arithmetic).
 #pragma unroll 1
       for (int cc = 0; cc < BN / CW; ++cc) {
+        const int mb = m0 + CW * cc;
+        const int cnt = M - mb;  // tokens of this slab, when fewer than CW
+        if (cnt <= 0) break;
         uint32_t r[CW];
         if constexpr (CW == 16)
           tmem_ld16(tmem + lane_addr + db * C::D_COLS, r);
         else
           tmem_ld32(tmem + lane_addr + db * C::D_COLS + 32 * cc, r);
         // the per-token factors of this slab first, all loads in flight
-        float sc2[CW];
+        float v[CW];
+        if (pexp != nullptr) {
+          if (cnt >= CW) {
 #pragma unroll
-        for (int i = 0; i < CW; ++i) {
-          const int m = m0 + CW * cc + i;
-          sc2[i] = (pexp && m < M) ? __fmul_rn(g, pow2_from_exp(__ldg(pexp + m))) : g;
+            for (int i = 0; i < CW; ++i) v[i] = __fmul_rn(g, pow2_from_exp(__ldg(pexp + mb + i)));
+          } else {
+#pragma unroll
+            for (int i = 0; i < CW; ++i) v[i] = __fmul_rn(g, pow2_from_exp(__ldg(pexp + mb + min(i, cnt - 1))));
+          }
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]) * v[i];
+        } else {
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]) * g;
         }
-        tmem_ld_wait();
+        if (part != nullptr) {
+          float* const dst = part + static_cast<int64_t>(mb) * N + n;
+          if (cnt >= CW) {
 #pragma unroll
-        for (int i = 0; i < CW; ++i) {
-          const int m = m0 + CW * cc + i;
-          if (m < M) {
-            const float v = __uint_as_float(r[i]) * sc2[i];
-            if (part)
-              part[static_cast<int64_t>(m) * N + n] = v;
-            else
-              y[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(v);
+            for (int i = 0; i < CW; ++i) dst[static_cast<int64_t>(i) * N] = v[i];
+          } else {
+#pragma unroll
+            for (int i = 0; i < CW; ++i)
+              if (i < cnt) dst[static_cast<int64_t>(i) * N] = v[i];
+          }
+        } else {
+          __nv_bfloat16* const dst = y + static_cast<int64_t>(mb) * N + n;
+          if (cnt >= CW) {
+#pragma unroll
+            for (int i = 0; i < CW; ++i) dst[static_cast<int64_t>(i) * N] = __float2bfloat16_rn(v[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < CW; ++i)
+              if (i < cnt) dst[static_cast<int64_t>(i) * N] = __float2bfloat16_rn(v[i]);
           }
         }
       }
@@ -465,7 +492,7 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.d_empty[db]);
       if (warp == kEpi && lane == 0) QRR_STAMP(3, 2, units);
-      if (part) {
+      if (F16 && part != nullptr) {
         // all 128 epilogue threads have written their partials; one thread
         // makes them visible GPU-wide (the fence is cumulative over the
         // barrier) and takes a ticket; the last split of the tile sums all
@@ -488,23 +515,39 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
             float sum[TB];
 #pragma unroll
             for (int i = 0; i < TB; ++i) sum[i] = 0.0f;
+            const bool whole = m0 + i0 + TB <= M;  // a batch of TB tokens without a ragged end
             for (int s0 = 0; s0 < splits; s0 += SB) {
               float v[SB][TB];
+              const float* const src = partial + (static_cast<int64_t>(s0) * M + m0 + i0) * N + n;
+              const int64_t sstride = static_cast<int64_t>(M) * N;
+              if (whole && s0 + SB <= splits) {
 #pragma unroll
-              for (int s1 = 0; s1 < SB; ++s1)
+                for (int s1 = 0; s1 < SB; ++s1)
 #pragma unroll
-                for (int i = 0; i < TB; ++i)
-                  v[s1][i] = (s0 + s1 < splits && m0 + i0 + i < M)
-                                 ? __ldcg(partial + (static_cast<int64_t>(s0 + s1) * M + m0 + i0 + i) * N + n)
-                                 : 0.0f;
+                  for (int i = 0; i < TB; ++i) v[s1][i] = __ldcg(src + s1 * sstride + static_cast<int64_t>(i) * N);
+              } else {
+#pragma unroll
+                for (int s1 = 0; s1 < SB; ++s1)
+#pragma unroll
+                  for (int i = 0; i < TB; ++i)
+                    v[s1][i] = (s0 + s1 < splits && m0 + i0 + i < M)
+                                   ? __ldcg(src + s1 * sstride + static_cast<int64_t>(i) * N)
+                                   : 0.0f;
+              }
 #pragma unroll
               for (int s1 = 0; s1 < SB; ++s1)
 #pragma unroll
                 for (int i = 0; i < TB; ++i) sum[i] += v[s1][i];
             }
+            __nv_bfloat16* const dst = y + static_cast<int64_t>(m0 + i0) * N + n;
+            if (whole) {
 #pragma unroll
-            for (int i = 0; i < TB; ++i)
-              if (m0 + i0 + i < M) y[static_cast<int64_t>(m0 + i0 + i) * N + n] = __float2bfloat16_rn(sum[i]);
+              for (int i = 0; i < TB; ++i) dst[static_cast<int64_t>(i) * N] = __float2bfloat16_rn(sum[i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < TB; ++i)
+                if (m0 + i0 + i < M) dst[static_cast<int64_t>(i) * N] = __float2bfloat16_rn(sum[i]);
+            }
           }
         }
         named_bar(1, 128);
