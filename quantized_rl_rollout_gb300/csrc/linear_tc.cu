@@ -81,7 +81,10 @@ struct Cfg {
   static constexpr bool SC_TMA = BK >= 256;  // block scales staged by TMA (16 B per row)
   static constexpr int S_BYTES = SC_TMA ? 128 * (BK / 16) : 0;
   static constexpr int STAGE = X_BYTES + C_BYTES + S_BYTES;
-  static constexpr int STAGES_RAW = (200 * 1024) / STAGE;
+  // as many stages as fit in shared memory (227 KB per CTA, less the
+  // alignment slack and the control block): the ring is what covers the L2
+  // and HBM latency of the x tiles
+  static constexpr int STAGES_RAW = (224 * 1024 - 2048) / STAGE;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int DBUF = BN <= 128 ? 2 : 1;  // accumulator buffers in TMEM
   static constexpr int D_COLS = BN < 32 ? 32 : BN;
@@ -91,12 +94,14 @@ struct Cfg {
   static constexpr int ACH = BK < 128 ? BK : 128;  // K per A chunk
   static constexpr int ACOLS = ACH / 2;
   static constexpr int CPS = BK / ACH;             // A chunks per stage
-  // A slot of chunk c is rewritten for chunk c + AST once the stage of chunk
-  // c has been released; that stage must still be in the shared-memory ring
-  // (at most STAGES stages back) for its barrier phase to be unambiguous
+  // A slot of chunk c is rewritten for chunk c + AST once the MMAs of chunk c
+  // are done.  While the TMEM ring is no deeper than the shared-memory ring,
+  // the release of chunk c's stage says so (its barrier phase is still
+  // unambiguous, at most STAGES stages back); a deeper TMEM ring gets one
+  // release barrier per slot, at the price of a second commit per chunk.
   static constexpr int AST_FIT = (512 - A_COL) / ACOLS;
-  static constexpr int AST_RAW = AST_FIT < CPS * STAGES ? AST_FIT : CPS * STAGES;
-  static constexpr int AST = (AST_RAW > 8 ? 8 : AST_RAW) / G * G;
+  static constexpr bool SLOT_BARS = AST_FIT > CPS * STAGES;
+  static constexpr int AST = (AST_FIT > 8 ? 8 : AST_FIT) / G * G;
   static constexpr int THREADS = 32 * (2 + 4 + 4 * G);
   // registers per thread for one resident CTA: each of the SM's four
   // sub-partitions holds 16K registers and ceil(warps / 4) of the warps, in
@@ -107,13 +112,14 @@ struct Cfg {
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr size_t SMEM = 1024 + static_cast<size_t>(STAGES) * STAGE + 1024;
   static_assert(STAGES >= 2, "shared memory ring too small");
+  static_assert(SMEM <= 227 * 1024, "shared memory per CTA exceeded");
   static_assert(AST >= 2 * G, "TMEM ring too small");
   static_assert(A_COL + AST * ACOLS <= 512, "TMEM overflow");
 };
 
 struct SharedCtl {
   uint64_t full[8], full_x[8], empty[8];  // full: codes + scales landed; full_x: x (or t') landed
-  uint64_t a_full[8];  // per A chunk slot
+  uint64_t a_full[8], a_empty[8];  // per A chunk slot (a_empty: only with SLOT_BARS)
   uint64_t d_full[2], d_empty[2];
   uint64_t done;
   uint32_t next_chunk[4];  // next A chunk to take, per TMEM lane quarter
@@ -146,14 +152,18 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   return r;
 }
 
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 
-__device__ __forceinline__ float f16_lo_to_f32(uint32_t h2) { return __half2float(__ushort_as_half(h2 & 0xFFFFu)); }
-__device__ __forceinline__ float f16_hi_to_f32(uint32_t h2) { return __half2float(__ushort_as_half(h2 >> 16)); }
 
 // 64 codes (8 words) + their 4 block scales (one word) -> 32 words of A.
 template <bool F16>
@@ -173,16 +183,25 @@ __device__ __forceinline__ void dequant64(const uint32_t* w, uint32_t scales4, u
         for (int b = 0; b < 4; ++b) out[8 * g + 4 * q + b] = hmul2(h[b], sg[g]);
       }
   } else {
+    // The E2M1 values come out of the hardware conversion as f16, where only
+    // the top mantissa bit can be set.  Moving each half's exponent and
+    // mantissa fields down by three bits re-reads them as the bf16 of
+    // v 2^-112 (an f16 exponent field under the bf16 bias, 127 - 15 = 112;
+    // the three mantissa bits shifted out are zero, zero stays zero), and
+    // one bf16x2 multiply by s_b 2^112 returns v s_b exactly: both factors
+    // and the product are normal bf16 numbers, the product has at most six
+    // significant bits.
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-      const float sv = e4m3_to_f32((scales4 >> (8 * g)) & 0xFFu);
+      const float sv = e4m3_to_f32((scales4 >> (8 * g)) & 0xFFu) * 0x1p112f;
+      const uint32_t s2 = pack_bf16x2(sv, sv);
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         uint32_t h[4];
         f16x2x4_from_e2m1x8(w[2 * g + q], h);
 #pragma unroll
         for (int b = 0; b < 4; ++b)
-          out[8 * g + 4 * q + b] = pack_bf16x2(f16_lo_to_f32(h[b]) * sv, f16_hi_to_f32(h[b]) * sv);
+          out[8 * g + 4 * q + b] = bmul2(((h[b] & 0x7FFF7FFFu) >> 3) | (h[b] & 0x80008000u), s2);
       }
     }
   }
@@ -219,7 +238,10 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
       mbar_init(&sh.full_x[s], 1);
       mbar_init(&sh.empty[s], 1 + 4 * C::CPS);  // MMA commit + 4 dequant warps per A chunk
     }
-    for (int s = 0; s < C::AST; ++s) mbar_init(&sh.a_full[s], 4);
+    for (int s = 0; s < C::AST; ++s) {
+      mbar_init(&sh.a_full[s], 4);
+      mbar_init(&sh.a_empty[s], 1);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.d_full[b], 1);
       mbar_init(&sh.d_empty[b], 4);
@@ -391,6 +413,7 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
               mma8_ts(dcol, a0, bd, idesc, acc);
             else
               mma4_ts(dcol, a0, bd, idesc, acc);
+            if constexpr (C::SLOT_BARS) mma_commit(&sh.a_empty[at.idx]);
             QRR_STAMP(1, 1, chunks);
             ++chunks;
           }
@@ -607,12 +630,16 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
             if (c < nk) scw[0] = __ldg(reinterpret_cast<const uint32_t*>(srow + (c0 + c) * (BK / 16)));
           }
           // the slot was last written for chunk - AST; its MMAs are done once
-          // the stage that chunk belonged to has been released (one commit per
-          // stage, no per-chunk commits on the tensor pipe)
+          // the slot's own release barrier or (shallow ring) the stage that
+          // chunk belonged to has been released
           bool free = true;
           if (chunk >= static_cast<uint32_t>(C::AST)) {
-            const uint32_t prev = (chunk - C::AST) / C::CPS;  // stage sequence number
-            free = mbar_wait(&sh.empty[prev % C::STAGES], (prev / C::STAGES) & 1, abort, p.status);
+            if constexpr (C::SLOT_BARS) {
+              free = mbar_wait(&sh.a_empty[slot], (chunk / C::AST - 1) & 1, abort, p.status);
+            } else {
+              const uint32_t prev = (chunk - C::AST) / C::CPS;  // stage sequence number
+              free = mbar_wait(&sh.empty[prev % C::STAGES], (prev / C::STAGES) & 1, abort, p.status);
+            }
           }
           if (q == 2 && lane == 0) QRR_STAMP(4, 3, chunk);
           if (!free || !mbar_wait(&sh.full[sidx], (sseq / C::STAGES) & 1, abort, p.status)) break;

@@ -99,6 +99,29 @@ def test_closed_forms(q):
     _assert_close(y, _ref(xr, zc, zs, zt, A, B, alpha), "W=0")
 
 
+@pytest.mark.parametrize("m", [64, 100, 300])
+def test_one_hot_tokens_bit_exact(q, m):
+    """Token m is +-e_{k_m}: y[m] is then +-W_hat[:, k_m] scaled once by s_t
+    in fp32 and rounded to bf16, with no sum to round, so every output is
+    fixed to the bit (the f16 decode tiles at 64 tokens, the bf16 prefill
+    tiles of 128 and 256 tokens with a ragged last tile)."""
+    n, k = 384, 2048
+    W, codes, scales, ts, _, _, _ = _layer(q, n, k, 0, "onehot")
+    g = np.random.default_rng(m)
+    cols = g.choice(k, m, replace=False)
+    sign = np.where(g.random(m) < 0.5, -1.0, 1.0)
+    xh = np.zeros((m, k), np.float32)
+    xh[np.arange(m), cols] = sign
+    x = torch.from_numpy(xh).to(torch.bfloat16).to(DEV)
+    y = q.linear_nvfp4_lora(x, codes, scales, ts, None, None, 0.0)
+    torch.cuda.synchronize()
+    w_hat = oracle.nvfp4.dequantize(codes.cpu().numpy(), scales.cpu().numpy(), np.float32(ts.item()))
+    want = oracle.formats.bf16_rne(np.float32(w_hat[:, cols].T * sign[:, None]))
+    got = y.float().cpu().numpy()
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{len(bad)} outputs differ, first {bad[:3].tolist()}"
+
+
 def test_empty_tokens(q):
     W, codes, scales, ts, A, B, alpha = _layer(q, 128, 256, 8, "empty")
     x = torch.zeros(0, 256, dtype=torch.bfloat16, device=DEV)
