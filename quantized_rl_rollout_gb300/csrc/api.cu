@@ -54,6 +54,7 @@ struct LinIn {
 // workspace carve-up.  Every layer of a call shares the token count M.
 struct LinPlan {
   bool f16;
+  bool pair;  // 256-token tiles on CTA pairs (2-CTA clusters), each pair two 128-row tiles
   int bn, bk, m_tiles, count;
   struct Layer {
     int n_tiles, splits, kcps, lora_chunks, lora_ks, lora_slice;
@@ -86,6 +87,11 @@ LinPlan plan_linear(int64_t M, const LinIn* in, int count) {
     p.l[j].splits = 1;
     p.l[j].kcps = kc[j];
   }
+  // Prefill tiles of 256 tokens run on CTA pairs when every layer has an even
+  // number of 128-row tiles: the pair's MMA reads each CTA's half of the
+  // token tile, so each SM streams half of x.
+  p.pair = !decode && p.bn == 256;
+  for (int j = 0; j < count; ++j) p.pair = p.pair && p.l[j].n_tiles % 2 == 0;
   if (decode) {
     // Cost model in pipeline stages: a unit costs its K stages plus its
     // epilogue (about half a stage, or three when it writes a split-K partial
@@ -223,7 +229,8 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
     W4Layer& L = p.layer[p.count++];
     const void* xsrc = pl.f16 ? static_cast<const void*>(x16) : a.x;
     const CUtensorMapDataType xt = pl.f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    if (!make_tmap_2d(&L.tx, xsrc, xt, M, a.K, a.K * 2, pl.bn, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    const uint32_t box_m = pl.pair ? pl.bn / 2 : pl.bn;  // token rows one CTA loads
+    if (!make_tmap_2d(&L.tx, xsrc, xt, M, a.K, a.K * 2, box_m, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_2d(&L.tcodes, a.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.N, a.K / 2, a.K / 2, 128, pl.bk / 2,
                       pl.bk == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B) ||
         !make_tmap_2d(&L.tscales, a.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.N, a.K / 16, a.K / 16, 128, 16,
@@ -231,7 +238,7 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
       return QRR_ERR_CUDA;
     if (a.r > 0) {
       if (!make_tmap_2d(&L.tt, tbuf, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, M, 64 * pj.lora_chunks,
-                        64 * pj.lora_chunks * 2, pl.bn, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+                        64 * pj.lora_chunks * 2, box_m, 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return QRR_ERR_CUDA;
     } else {
       L.tt = L.tx;  // never read without an adapter
@@ -257,7 +264,7 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
   if (p.count == 0) return QRR_OK;
   if (any_split && cudaMemsetAsync(ws + pl.cnt_begin, 0, pl.cnt_bytes, s) != cudaSuccess) return QRR_ERR_CUDA;
   if (lb.count > 0 && launch_lora_down_tc(lb, s) != cudaSuccess) return QRR_ERR_CUDA;
-  return from_cuda(launch_w4a16_tc(p, pl.bn, pl.f16, lb.count > 0, s));
+  return from_cuda(launch_w4a16_tc(p, pl.bn, pl.f16, pl.pair, lb.count > 0, s));
 }
 
 LinIn make_in(const void* x, int64_t N, int64_t K, const uint8_t* codes, const uint8_t* scales, const float* ts,

@@ -17,9 +17,9 @@ namespace qrr {
 constexpr int kMaxW4Layers = 8;
 
 struct W4Layer {
-  CUtensorMap tx;      // x (bf16) or its f16 image [M, K], box [BN, 64], 128 B swizzle
+  CUtensorMap tx;      // x (bf16) or its f16 image [M, K], box [BN (BN/2 for a CTA pair), 64], 128 B swizzle
   CUtensorMap tcodes;  // packed codes u8 [N, K/2], box [128, 32]
-  CUtensorMap tt;      // LoRA t' bf16 [M, 64 * lora_chunks], box [BN, 64], 128 B swizzle
+  CUtensorMap tt;      // LoRA t' bf16 [M, 64 * lora_chunks], box as tx, 128 B swizzle
   CUtensorMap tscales;  // block scales u8 [N, K/16], box [128, 16] (256-wide K stages)
   const uint8_t* scales;
   const float* tensor_scale;
@@ -71,7 +71,9 @@ cudaError_t launch_lora_down_tc(LoraDownBatch& b, cudaStream_t stream);
 
 int w4_bn_for(int64_t M);
 int w4_bk_for(int64_t M);
-cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, bool after_prologue, cudaStream_t stream);
+// pair: 256-token tiles run on 2-CTA clusters, each cluster two adjacent
+// 128-row tiles (every layer's n_tiles even; x / t' maps with 128-row boxes).
+cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, bool pair, bool after_prologue, cudaStream_t stream);
 
 struct Fp8GemmArgs {
   const uint8_t* qa;  // [M, K]

@@ -71,10 +71,12 @@ __device__ unsigned long long qrr_trace_buf[8][4][256];
 
 namespace {
 
-template <int BN, int BK, int G>
+template <int BN, int BK, int G, bool PAIR = false>
 struct Cfg {
   static constexpr int KSUB = BK / 64;     // 64-wide sub-chunks per stage
-  static constexpr int X_SUB = BN * 128;   // one [BN x 64] 128-byte-swizzled sub-tile
+  // token rows of x held by this CTA: a CTA pair splits its BN tokens
+  static constexpr int BNL = PAIR ? BN / 2 : BN;
+  static constexpr int X_SUB = BNL * 128;  // one [BNL x 64] 128-byte-swizzled sub-tile
   static constexpr int X_BYTES = KSUB * X_SUB;
   static constexpr int C_ROW = BK / 2;     // packed code bytes per weight row per stage
   static constexpr int C_BYTES = 128 * C_ROW;
@@ -115,6 +117,7 @@ struct Cfg {
   static_assert(SMEM <= 227 * 1024, "shared memory per CTA exceeded");
   static_assert(AST >= 2 * G, "TMEM ring too small");
   static_assert(A_COL + AST * ACOLS <= 512, "TMEM overflow");
+  static_assert(!PAIR || (BN == 256 && !SLOT_BARS), "CTA pairs: 256-token tiles, stage-released A slots");
 };
 
 struct SharedCtl {
@@ -222,15 +225,32 @@ struct Ring {
 
 }  // namespace
 
-template <int BN, int BK, bool F16, int G>
-__global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __grid_constant__ W4Params p) {
-  using C = Cfg<BN, BK, G>;
+template <int BN, int BK, bool F16, int G, bool PAIR>
+__global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(const __grid_constant__ W4Params p) {
+  using C = Cfg<BN, BK, G, PAIR>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   SharedCtl& sh = *reinterpret_cast<SharedCtl*>(tiles + C::STAGES * C::STAGE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &sh.abort;
   constexpr int KSUB = C::KSUB;
+  // CTA pairs (2-CTA clusters): both CTAs walk the same units, the even one
+  // (rank 0) issues the pair's MMAs and holds the barriers the pair meets on
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
+  const int ustart = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int ustep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  // Every wait acquires at CTA scope, which keeps the SM's L1 contents valid
+  // across it: what the peer CTA of a pair hands over through a barrier is
+  // tensor-memory state, TMA bytes or tensor-core completion, none of it
+  // generic memory.
+  auto wait = [&](uint64_t* bar, uint32_t parity) { return mbar_wait(bar, parity, abort, p.status); };
+  // arrive on the even CTA's copy of a barrier (this CTA's own when unpaired)
+  auto arrive_leader = [&](uint64_t* bar) {
+    if (PAIR && rank != 0)
+      mbar_arrive_cluster(cluster_addr(bar, 0));
+    else
+      mbar_arrive(bar);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -239,12 +259,12 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
       mbar_init(&sh.empty[s], 1 + 4 * C::CPS);  // MMA commit + 4 dequant warps per A chunk
     }
     for (int s = 0; s < C::AST; ++s) {
-      mbar_init(&sh.a_full[s], 4);
+      mbar_init(&sh.a_full[s], PAIR ? 8 : 4);  // the dequant warps of both CTAs of a pair
       mbar_init(&sh.a_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh.d_full[b], 1);
-      mbar_init(&sh.d_empty[b], 4);
+      mbar_init(&sh.d_empty[b], PAIR ? 8 : 4);
     }
     mbar_init(&sh.done, 1);
     for (int i = 0; i < 4; ++i) sh.next_chunk[i] = 0;
@@ -256,9 +276,15 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
   // warp holds up its whole A chunk), then the four epilogue warps, then the
   // TMA and MMA issuers
   constexpr int kEpi = 4 * G, kTma = 4 * G + 4, kMma = 4 * G + 5;
-  if (warp == kMma) tmem_alloc(&sh.tmem, C::TMEM_COLS);
+  if (warp == kMma) {
+    if constexpr (PAIR)
+      tmem_alloc_pair(&sh.tmem, C::TMEM_COLS);
+    else
+      tmem_alloc(&sh.tmem, C::TMEM_COLS);
+  }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // the peer's barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem = sh.tmem;
 
@@ -268,14 +294,16 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
     while (j + 1 < p.count && p.layer[j + 1].first_unit <= u) ++j;
     const W4Layer& L = p.layer[j];
     const int local = u - L.first_unit;
-    nt = local % L.n_tiles;
-    const int rest = local / L.n_tiles;
+    const int n_units = PAIR ? L.n_tiles / 2 : L.n_tiles;  // a pair takes two adjacent 128-row tiles
+    nt = local % n_units;
+    const int rest = local / n_units;
     mt = rest % L.m_tiles;
     sp = rest / L.m_tiles;
     c0 = sp * L.kcps;
     const int kc = L.K / BK;
     nk = min(c0 + L.kcps, kc) - c0;
     nl = (L.r > 0 && sp == L.splits - 1) ? (L.lora_chunks + KSUB - 1) / KSUB : 0;
+    if constexpr (PAIR) nt = 2 * nt + static_cast<int>(rank);
   };
 
   if (warp == kTma) {
@@ -291,8 +319,7 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
       auto next = [&](Cursor& k) {  // advance to the next stage of the CTA; false past the last
         if (k.u >= 0 && ++k.c < k.nk + k.nl) return true;
         k.c = 0;
-        for (k.u = k.u < 0 ? static_cast<int>(blockIdx.x) : k.u + static_cast<int>(gridDim.x); k.u < p.total_units;
-             k.u += gridDim.x) {
+        for (k.u = k.u < 0 ? ustart : k.u + ustep; k.u < p.total_units; k.u += ustep) {
           locate(k.u, k.j, k.nt, k.mt, k.sp, k.c0, k.nk, k.nl);
           if (k.nk + k.nl > 0) return true;
         }
@@ -311,20 +338,25 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
           mbar_arrive(fb);  // LoRA stage: no codes
         }
       };
+      // x (or t') rows of this CTA; in a pair each CTA loads its half of the
+      // tile's tokens and both halves count on the even CTA's barrier
       auto issue_x = [&](const Cursor& k, int idx) {
         uint64_t* fb = &sh.full_x[idx];
         uint8_t* xs = tiles + idx * C::STAGE;
-        mbar_arrive_expect_tx(fb, C::X_BYTES);
-        if (k.c < k.nk) {
-          const int kb = (k.c0 + k.c) * BK;
+        const int row0 = k.mt * BN + static_cast<int>(rank) * C::BNL;
+        const CUtensorMap* map = k.c < k.nk ? &p.layer[k.j].tx : &p.layer[k.j].tt;
+        // column of the first sub-tile: K offset, or the LoRA sub-tile (past
+        // the tensor's width reads as zeros)
+        const int col0 = k.c < k.nk ? (k.c0 + k.c) * BK : (k.c - k.nk) * KSUB * 64;
+        if constexpr (PAIR) {
+          if (rank == 0) mbar_arrive_expect_tx(fb, 2 * C::X_BYTES);
+          const uint32_t fbc = cluster_addr(fb, 0);
 #pragma unroll
-          for (int q = 0; q < KSUB; ++q) tma_load_2d(&p.layer[k.j].tx, fb, xs + q * C::X_SUB, kb + 64 * q, k.mt * BN);
+          for (int q = 0; q < KSUB; ++q) tma_load_2d_pair(map, fbc, xs + q * C::X_SUB, col0 + 64 * q, row0);
         } else {
-          // LoRA stage: t' sub-tiles past the tensor's width read as zeros
-          const int lsub = (k.c - k.nk) * KSUB;
+          mbar_arrive_expect_tx(fb, C::X_BYTES);
 #pragma unroll
-          for (int q = 0; q < KSUB; ++q)
-            tma_load_2d(&p.layer[k.j].tt, fb, xs + q * C::X_SUB, (lsub + q) * 64, k.mt * BN);
+          for (int q = 0; q < KSUB; ++q) tma_load_2d(map, fb, xs + q * C::X_SUB, col0 + 64 * q, row0);
         }
       };
       Cursor kw, kx;
@@ -345,7 +377,7 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
       while (ok && next(kw)) {
         next(kx);
         const uint32_t idx = nw % C::STAGES, use = nw / C::STAGES;
-        if (!mbar_wait(&sh.empty[idx], (use - 1) & 1, abort, p.status)) {
+        if (!wait(&sh.empty[idx], (use - 1) & 1)) {
           ok = false;
           break;
         }
@@ -355,34 +387,45 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
         ++nw;
       }
       // drain: the last loads of every stage have landed before the CTA exits
+      // (a pair's x halves all count on the even CTA, which the odd one
+      // waits for at the closing cluster barrier)
       volatile int no_abort = 0;
       for (uint32_t k = 0; k < static_cast<uint32_t>(C::STAGES) && k < nw; ++k) {
         const uint32_t i = nw - 1 - k;
         mbar_wait(&sh.full[i % C::STAGES], (i / C::STAGES) & 1, &no_abort, p.status);
-        mbar_wait(&sh.full_x[i % C::STAGES], (i / C::STAGES) & 1, &no_abort, p.status);
+        if (!PAIR || rank == 0) mbar_wait(&sh.full_x[i % C::STAGES], (i / C::STAGES) & 1, &no_abort, p.status);
       }
     }
   } else if (warp == kMma) {
     // ------------------------------ MMA ------------------------------
     // Per stage: the x (or t') tile has landed; per A chunk: its dequant
     // warps have stored it to TMEM.
-    if (elect_one()) {
-      constexpr uint32_t id_main = make_idesc(F16 ? kFmtF16 : kFmtBF16, F16 ? kFmtF16 : kFmtBF16, 128, BN);
-      constexpr uint32_t id_lora = make_idesc(kFmtBF16, kFmtBF16, 128, BN);
+    // In a CTA pair only the even CTA issues: M = 256 rows (128 in each
+    // CTA's TMEM), and every commit reaches the barrier in both CTAs.
+    if (elect_one() && (!PAIR || rank == 0)) {
+      constexpr uint32_t MM = PAIR ? 256 : 128;
+      constexpr uint32_t id_main = make_idesc(F16 ? kFmtF16 : kFmtBF16, F16 ? kFmtF16 : kFmtBF16, MM, BN);
+      constexpr uint32_t id_lora = make_idesc(kFmtBF16, kFmtBF16, MM, BN);
+      auto commit = [&](uint64_t* bar) {
+        if constexpr (PAIR)
+          mma_commit_pair(bar, 0x3);
+        else
+          mma_commit(bar);
+      };
       Ring st, at;
       uint32_t units = 0, chunks = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x, ++units) {
+      for (int u = ustart; u < p.total_units && ok; u += ustep, ++units) {
         int j, nt, mt, sp, c0, nk, nl;
         locate(u, j, nt, mt, sp, c0, nk, nl);
         const int db = units % C::DBUF;
         const uint32_t duse = units / C::DBUF;
         QRR_STAMP(1, 2, units);
-        if (duse > 0 && !mbar_wait(&sh.d_empty[db], (duse - 1) & 1, abort, p.status)) break;
+        if (duse > 0 && !wait(&sh.d_empty[db], (duse - 1) & 1)) break;
         QRR_STAMP(1, 3, units);
         const uint32_t dcol = tmem + db * C::D_COLS;
         for (int c = 0; c < nk + nl && ok; ++c, st.next<C::STAGES>()) {
-          if (!mbar_wait(&sh.full_x[st.idx], st.use & 1, abort, p.status)) {
+          if (!wait(&sh.full_x[st.idx], st.use & 1)) {
             ok = false;
             break;
           }
@@ -393,7 +436,7 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
 #pragma unroll
           for (int hc = 0; hc < C::CPS; ++hc, at.next<C::AST>()) {
             QRR_STAMP(2, 2, chunks);
-            if (!mbar_wait(&sh.a_full[at.idx], at.use & 1, abort, p.status)) {
+            if (!wait(&sh.a_full[at.idx], at.use & 1)) {
               ok = false;
               break;
             }
@@ -409,23 +452,30 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
               bd[k] = bdesc + static_cast<uint64_t>(((kk >> 2) * C::X_SUB + 32 * (kk & 3)) >> 4);
             }
             const uint32_t acc = (c > 0 || hc > 0) ? 1u : 0u;
-            if constexpr (NK == 8)
+            if constexpr (PAIR) {
+              static_assert(!PAIR || NK == 4, "CTA pairs use 64-wide K chunks");
+              mma4_ts_pair(dcol, a0, bd, idesc, acc);
+            } else if constexpr (NK == 8) {
               mma8_ts(dcol, a0, bd, idesc, acc);
-            else
+            } else {
               mma4_ts(dcol, a0, bd, idesc, acc);
-            if constexpr (C::SLOT_BARS) mma_commit(&sh.a_empty[at.idx]);
+            }
+            if constexpr (C::SLOT_BARS) commit(&sh.a_empty[at.idx]);
             QRR_STAMP(1, 1, chunks);
             ++chunks;
           }
           QRR_STAMP(2, 0, chunks / C::CPS);
-          if (ok) mma_commit(&sh.empty[st.idx]);
+          if (ok) commit(&sh.empty[st.idx]);
           QRR_STAMP(2, 1, chunks / C::CPS);
         }
         if (!ok) break;
-        mma_commit(&sh.d_full[db]);
+        commit(&sh.d_full[db]);
         QRR_STAMP(2, 3, units);
       }
-      mma_commit(&sh.done);
+      if constexpr (PAIR)
+        mma_commit_pair(&sh.done, 0x1);
+      else
+        mma_commit(&sh.done);
       volatile int no_abort = 0;
       mbar_wait(&sh.done, 0, &no_abort, p.status);
     }
@@ -438,7 +488,7 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
     griddep_wait();  // the per-token exponents come from the prologue kernel
     uint32_t units = 0;
-    for (int u = blockIdx.x; u < p.total_units; u += gridDim.x, ++units) {
+    for (int u = ustart; u < p.total_units; u += ustep, ++units) {
       int j, nt, mt, sp, c0, nk, nl;
       locate(u, j, nt, mt, sp, c0, nk, nl);
       const int M = p.layer[j].M, N = p.layer[j].N, splits = p.layer[j].splits, n_tiles = p.layer[j].n_tiles;
@@ -450,7 +500,7 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
       const int n = nt * 128 + 32 * q + lane;
       const int db = units % C::DBUF;
       if (warp == kEpi && lane == 0) QRR_STAMP(3, 0, units);
-      if (!mbar_wait(&sh.d_full[db], (units / C::DBUF) & 1, abort, p.status)) break;
+      if (!wait(&sh.d_full[db], (units / C::DBUF) & 1)) break;
       if (warp == kEpi && lane == 0) QRR_STAMP(3, 1, units);
       tc_fence_after();
       const float g = st > 0.0f ? st : 1.0f;
@@ -513,7 +563,7 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.d_empty[db]);
+      if (lane == 0) arrive_leader(&sh.d_empty[db]);
       if (warp == kEpi && lane == 0) QRR_STAMP(3, 2, units);
       if (F16 && part != nullptr) {
         // all 128 epilogue threads have written their partials; one thread
@@ -591,12 +641,12 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
     const int rot = BK == 256 ? (row & 7) : ((row >> 2) & 1);
     // this CTA's A chunks: its units in order, (nk + nl) stages of CPS chunks
     uint32_t total = 0;
-    for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+    for (int u = ustart; u < p.total_units; u += ustep) {
       int j, nt, mt, sp, c0, nk, nl;
       locate(u, j, nt, mt, sp, c0, nk, nl);
       total += static_cast<uint32_t>((nk + nl) * C::CPS);
     }
-    int u = static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x);
+    int u = ustart - ustep;
     uint32_t ubeg = 0, uend = 0;  // chunk range of unit u
     int j = 0, nt = 0, mt = 0, sp = 0, c0 = 0, nk = 0, nl = 0;
     while (true) {
@@ -605,7 +655,7 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
       chunk = __shfl_sync(0xFFFFFFFFu, chunk, 0);
       if (chunk >= total) break;
       while (chunk >= uend) {  // claims only grow: move forward to the chunk's unit
-        u += gridDim.x;
+        u += ustep;
         locate(u, j, nt, mt, sp, c0, nk, nl);
         ubeg = uend;
         uend += static_cast<uint32_t>((nk + nl) * C::CPS);
@@ -635,10 +685,10 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
           bool free = true;
           if (chunk >= static_cast<uint32_t>(C::AST)) {
             if constexpr (C::SLOT_BARS) {
-              free = mbar_wait(&sh.a_empty[slot], (chunk / C::AST - 1) & 1, abort, p.status);
+              free = wait(&sh.a_empty[slot], (chunk / C::AST - 1) & 1);
             } else {
               const uint32_t prev = (chunk - C::AST) / C::CPS;  // stage sequence number
-              free = mbar_wait(&sh.empty[prev % C::STAGES], (prev / C::STAGES) & 1, abort, p.status);
+              free = wait(&sh.empty[prev % C::STAGES], (prev / C::STAGES) & 1);
             }
           }
           if (q == 2 && lane == 0) QRR_STAMP(4, 3, chunk);
@@ -647,7 +697,10 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
           // the prologue kernel wrote
           if (c >= nk) {
             griddep_wait();
-            if (!mbar_wait(&sh.full_x[sidx], (sseq / C::STAGES) & 1, abort, p.status)) break;
+            // the f16 path rescales the t' tile in shared memory: it must
+            // have landed
+            if constexpr (F16)
+              if (!mbar_wait(&sh.full_x[sidx], (sseq / C::STAGES) & 1, abort, p.status)) break;
           }
           if (q == 2 && lane == 0) QRR_STAMP(4, 1, chunk);
           if (q != 2 && lane == 0) QRR_STAMP(5 + (q == 3 ? 2 : q), 1, chunk);
@@ -732,7 +785,7 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(&sh.a_full[slot]);
+            arrive_leader(&sh.a_full[slot]);
             mbar_arrive(&sh.empty[sidx]);
           }
         }
@@ -741,9 +794,15 @@ __global__ void __maxnreg__((Cfg<BN, BK, G>::MAXNREG)) w4a16_tc_kernel(const __g
   }
   tc_fence_before();
   __syncthreads();
+  // a pair ends together: no remote arrive or x half may reach a CTA that
+  // has exited, and the pair's TMEM is released by both
+  if constexpr (PAIR) cluster_sync();
   if (warp == kMma) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem, C::TMEM_COLS);
+    else
+      tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
@@ -757,27 +816,41 @@ namespace {
 #endif
 constexpr int kDecodeGroups = QRR_DECODE_GROUPS;
 
-template <int BN, int BK, bool F16, int G>
+// grid: CTAs for units one at a time; a paired launch runs min(units,
+// co-resident 2-CTA clusters) clusters instead.
+template <int BN, int BK, bool F16, int G, bool PAIR = false>
 cudaError_t launch_bn(const W4Params& p, int grid, bool after_prologue, cudaStream_t stream) {
-  using C = Cfg<BN, BK, G>;
+  using C = Cfg<BN, BK, G, PAIR>;
+  auto kernel = w4a16_tc_kernel<BN, BK, F16, G, PAIR>;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(w4a16_tc_kernel<BN, BK, F16, G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM));
     if (e != cudaSuccess) return e;
     attr = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
-  cudaLaunchAttribute la[1];
+  cudaLaunchAttribute la[2];
   la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   la[0].val.programmaticStreamSerializationAllowed = after_prologue ? 1 : 0;
+  la[1].id = cudaLaunchAttributeClusterDimension;
+  la[1].val.clusterDim.x = PAIR ? 2 : 1;
+  la[1].val.clusterDim.y = 1;
+  la[1].val.clusterDim.z = 1;
   cfg.attrs = la;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<BN, BK, F16, G>, p);
+  cfg.numAttrs = PAIR ? 2 : 1;
+  if (PAIR) {
+    cfg.gridDim = dim3(2);
+    int clusters = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorLaunchOutOfResources;
+    grid = 2 * (grid < clusters ? grid : clusters);
+  }
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 }  // namespace
@@ -796,11 +869,11 @@ int w4_bk_for(int64_t M) { return M <= 64 ? 256 : 64; }
 
 // after_prologue: the previous kernel in the stream is the prologue that
 // writes x16 / pexp / t'; this launch may then start before it completes.
-cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, bool after_prologue, cudaStream_t stream) {
+cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, bool pair, bool after_prologue, cudaStream_t stream) {
   int units = 0;
   for (int j = 0; j < p.count; ++j) {
     p.layer[j].first_unit = units;
-    units += p.layer[j].n_tiles * p.layer[j].m_tiles * p.layer[j].splits;
+    units += (pair ? p.layer[j].n_tiles / 2 : p.layer[j].n_tiles) * p.layer[j].m_tiles * p.layer[j].splits;
   }
   p.total_units = units;
   if (units == 0) return cudaSuccess;
@@ -814,8 +887,9 @@ cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, bool after_prologue, 
       default: return launch_bn<64, 256, true, kDecodeGroups>(p, grid, after_prologue, stream);
     }
   }
-  return bn == 128 ? launch_bn<128, 64, false, 2>(p, grid, after_prologue, stream)
-                   : launch_bn<256, 64, false, 2>(p, grid, after_prologue, stream);
+  if (bn == 128) return launch_bn<128, 64, false, 2>(p, grid, after_prologue, stream);
+  if (pair) return launch_bn<256, 64, false, 3, true>(p, units, after_prologue, stream);
+  return launch_bn<256, 64, false, 2>(p, grid, after_prologue, stream);
 }
 
 }  // namespace qrr

@@ -264,6 +264,26 @@ __device__ __forceinline__ void mma8_ts(uint32_t d_tmem, uint32_t a_tmem, const 
       : "memory");
 }
 
+// The same four MMAs for a CTA pair (cta_group::2, M = 256): issued by one
+// thread of the even CTA of a 2-CTA cluster; A is read from both CTAs' TMEM
+// at a_tmem (128 rows each), B from both CTAs' shared memory at each
+// descriptor's address (the even CTA holds rows [0, N/2) of B, the odd CTA
+// rows [N/2, N)), and each CTA's TMEM at d_tmem receives its 128 rows of D
+// over all N columns.
+__device__ __forceinline__ void mma4_ts_pair(uint32_t d_tmem, uint32_t a_tmem, const uint64_t (&b)[4], uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b32 a1, a2, a3;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 q, %6, %6;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %7, p;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [a1], %3, %7, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [a2], %4, %7, q;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [a3], %5, %7, q;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(accumulate), "r"(idesc)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] x B[smem]^T, kind::f8f6f4 (E4M3 operands).
 __device__ __forceinline__ void mma_fp8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                            uint32_t accumulate) {
@@ -278,6 +298,74 @@ __device__ __forceinline__ void mma_fp8_ss(uint32_t d_tmem, uint64_t a_desc, uin
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+
+// Arrive on `bar` (same shared-memory offset) in each CTA of `cta_mask`
+// once every cta_group::2 MMA this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// ---- CTA pairs (2-CTA clusters) --------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of every CTA of the cluster; orders shared-memory writes
+// (release) before the peer's later reads (acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier given by its cluster address (this CTA's or a
+// peer's) with relaxed ordering.  A release at cluster scope would make the
+// arriving thread wait until all its earlier memory operations are visible to
+// the whole cluster (measured: about a thousand cycles per arrive, which
+// halved the dequant rate of a CTA pair); the hand-offs that use this one
+// carry tensor-memory state only, completed by tcgen05.wait::st / ::ld and
+// ordered by tcgen05.fence::before_thread_sync before the arrive, and the
+// waiter orders its own tcgen05 work after the wait with
+// tcgen05.fence::after_thread_sync.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+// TMEM allocation shared by a CTA pair: one warp of each CTA executes it,
+// and each CTA gets the same columns of its own TMEM.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// 2-D tile load into this CTA's shared memory whose completion is counted on
+// an mbarrier given by its cluster address, which may sit in the peer CTA of
+// the pair.
+__device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap* map, uint32_t bar_cluster, void* dst, int32_t x,
+                                                 int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
 }
 
 __device__ __forceinline__ uint32_t elect_one() {

@@ -99,13 +99,15 @@ def test_closed_forms(q):
     _assert_close(y, _ref(xr, zc, zs, zt, A, B, alpha), "W=0")
 
 
+@pytest.mark.parametrize("n", [384, 512])
 @pytest.mark.parametrize("m", [64, 100, 300])
-def test_one_hot_tokens_bit_exact(q, m):
+def test_one_hot_tokens_bit_exact(q, m, n):
     """Token m is +-e_{k_m}: y[m] is then +-W_hat[:, k_m] scaled once by s_t
     in fp32 and rounded to bf16, with no sum to round, so every output is
     fixed to the bit (the f16 decode tiles at 64 tokens, the bf16 prefill
-    tiles of 128 and 256 tokens with a ragged last tile)."""
-    n, k = 384, 2048
+    tiles of 128 and 256 tokens with a ragged last tile, on single CTAs for
+    an odd number of 128-row tiles and on CTA pairs for an even one)."""
+    k = 2048
     W, codes, scales, ts, _, _, _ = _layer(q, n, k, 0, "onehot")
     g = np.random.default_rng(m)
     cols = g.choice(k, m, replace=False)
@@ -148,11 +150,13 @@ def test_decode_8b_layer_set_sampled(q, m):
         del W, codes, scales
 
 
-@pytest.mark.parametrize("m", [1, 8, 64, 300])
+@pytest.mark.parametrize("m", [1, 8, 64, 200, 300])
 def test_grouped_layer_set(q, m):
     """The grouped call over a mixed layer set (different N, K, ranks, one
     layer without adapter) matches the oracle layer by layer."""
     shapes = [(384, 1024, 32), (128, 256, 8), (256, 2048, 0), (512, 768, 64)]
+    if m == 200:  # an even tile count in every layer: the prefill tiles run on CTA pairs
+        shapes = [(256, 1024, 32), (512, 256, 8), (256, 2048, 0), (768, 768, 64)]
     layers = []
     for i, (n, k, r) in enumerate(shapes):
         W, codes, scales, ts, A, B, alpha = _layer(q, n, k, r, f"grp{i}")
@@ -188,6 +192,30 @@ def test_grouped_8b_decode_sampled(q, m):
         y_ref = _ref(d["x"], d["codes"], d["scales"], d["tensor_scale"], d["lora_A"], d["lora_B"], d["alpha"],
                      rows=rows)
         _assert_close(y[:, torch.from_numpy(rows).to(DEV)], y_ref, f"grouped 8B {layer.name} m={m}")
+
+
+def test_grouped_8b_prefill_sampled(q):
+    """The 8B-class layer set at 4096 tokens in one grouped call, the bench's
+    prefill launch (256-token tiles on CTA pairs, LoRA r = 32): all 4096
+    tokens of sampled output columns, at least one column in every 128-row
+    tile, so both CTAs of every pair and every token tile are checked."""
+    c = configs.PREFILL_8B
+    m, r = c["tokens"], c["r"]
+    g = np.random.default_rng(10)
+    layers = []
+    for layer in configs.LAYERS_8B:
+        W, codes, scales, ts, A, B, alpha = _layer(q, layer.n, layer.k, r, f"p8b/{layer.name}")
+        x = inputs.activations(m, layer.k, inputs.derive_seed(0, "p8b-x", layer.name), device=DEV)
+        layers.append(dict(x=x, codes=codes, scales=scales, tensor_scale=ts, lora_A=A, lora_B=B, alpha=alpha))
+        del W
+    ys = q.linear_nvfp4_lora_grouped(layers)
+    torch.cuda.synchronize()
+    for layer, d, y in zip(configs.LAYERS_8B, layers, ys):
+        tiles = np.arange(layer.n // 128) * 128
+        rows = np.unique(np.concatenate([[0, layer.n - 1], tiles + g.integers(0, 128, tiles.size)]))
+        y_ref = _ref(d["x"], d["codes"], d["scales"], d["tensor_scale"], d["lora_A"], d["lora_B"], d["alpha"],
+                     rows=rows)
+        _assert_close(y[:, torch.from_numpy(rows).to(DEV)], y_ref, f"grouped 8B prefill {layer.name}")
 
 
 @pytest.mark.parametrize("mode", [0, 1])
