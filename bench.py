@@ -31,6 +31,8 @@ same workload per step, on the host's cores) and prints the same line with
 """
 
 import argparse
+import csv
+import hashlib
 import json
 import os
 import statistics
@@ -55,6 +57,67 @@ PREFILL_TOKENS = 4096
 R = 32
 ALPHA = 2.0 * R
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# DRAM traffic per launch of each phase's main kernel, from an ncu launch list
+# (dram__bytes_read.sum + dram__bytes_write.sum).  It is recorded together with
+# a hash of the CUDA sources and reported only while the sources are unchanged.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+PHASE_KERNELS = {  # phase -> (kernel name prefix, template arguments as ncu prints them)
+    "prefill": ("w4a16_tc_kernel", "<256, 64, 0, 3, 1>"),
+    "decode_m1": ("w4a16_tc_kernel", "<16, 256, 1, 3, 0>"),
+    "decode_m8": ("w4a16_tc_kernel", "<16, 256, 1, 3, 0>"),
+    "decode_m64": ("w4a16_tc_kernel", "<64, 256, 1, 3, 0>"),
+    "requant": ("nvfp4_encode_kernel", ""),
+    "fp8_quant": ("fp8_w128_kernel", ""),
+    "fp8_gemm": ("fp8_gemm_tc_kernel", ""),
+}
+
+
+def source_hash():
+    h = hashlib.sha256()
+    src = os.path.join(ROOT, "quantized_rl_rollout_gb300", "csrc")
+    for name in sorted(os.listdir(src)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            h.update(open(os.path.join(src, name), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "qrr.h"), "rb").read())
+    return h.hexdigest()
+
+
+def record_traffic(csv_path):
+    """Median DRAM bytes per launch of each phase kernel in an ncu CSV launch
+    list, written to profiles/traffic.json with the current source hash."""
+    per = {}
+    with open(csv_path) as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    rows = list(csv.DictReader(lines))
+    launches = {}
+    for r in rows:
+        launches.setdefault(r["ID"], {"name": r["Kernel Name"]})[r["Metric Name"]] = float(
+            r["Metric Value"].replace(",", ""))
+    for phase, (prefix, targs) in PHASE_KERNELS.items():
+        vals = [v["dram__bytes_read.sum"] + v["dram__bytes_write.sum"] for v in launches.values()
+                if prefix in v["name"] and targs.replace(" ", "") in v["name"].replace(" ", "")
+                and "dram__bytes_read.sum" in v and "dram__bytes_write.sum" in v]
+        if vals:
+            per[phase] = {"kernel": prefix + targs, "dram_bytes_per_launch": statistics.median(vals),
+                          "launches": len(vals)}
+    out = {"source_sha256": source_hash(), "from": os.path.basename(csv_path), "phases": per}
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(out, f, indent=1)
+    print(json.dumps(out, indent=1))
+
+
+def load_traffic(phase):
+    try:
+        d = json.load(open(TRAFFIC_FILE))
+    except (OSError, ValueError):
+        return None
+    if d.get("source_sha256") != source_hash():
+        return None
+    e = d.get("phases", {}).get(phase)
+    return e["dram_bytes_per_launch"] if e else None
 
 
 def load_peaks():
@@ -420,12 +483,17 @@ def max_over_ranks(dist, value):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--phases", default=",".join(PHASES))
     ap.add_argument("--skip-extras", action="store_true", help="no e2e or CPU-oracle legs (for profiler runs)")
+    ap.add_argument("--record-traffic", metavar="NCU_CSV",
+                    help="write profiles/traffic.json from an ncu launch list (dram bytes) and exit")
     args = ap.parse_args()
+    if args.record_traffic:
+        record_traffic(args.record_traffic)
+        return
     warmup = max(3, args.warmup)
     rank, world, local, dist = dist_setup(args.gpus)
 
@@ -534,6 +602,7 @@ def main():
         roof = {"bound": "tensor", "achieved": d["TFLOP/s"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": d["TFLOP/s"] / peaks["bf16_tflops"], "traffic": None, "kernel_phase": dom}
     roof["peak_source"] = peaks["source"]
+    roof["traffic"] = load_traffic(dom)
 
     e2e = None
     cpu = None

@@ -14,15 +14,19 @@
 // bf16 and in f16, so the tensor core forms every product exactly and sums in
 // fp32; s_t is applied once in the epilogue.
 //
-//   warps 0..4G-1  G dequant warpgroups taking the A chunks in turn: thread =
-//               weight row (its TMEM lane); codes and scales from shared
-//               memory, stored to a TMEM ring of A chunks
-//   warps 4G..4G+3  epilogue: D out of TMEM (double-buffered when it fits),
-//               scale, store y or a split-K partial
-//   warp 4G+4   TMA: per BK-wide K stage, x [BN x BK] (128 B swizzle, in
+//   warp 0      TMA: per BK-wide K stage, x [BN x BK] (128 B swizzle, in
 //               64-wide sub-tiles), the packed codes [128 x BK/2 B] and, for
 //               BK = 256, the block scales [128 x 16 B] into an S-stage ring
-//   warp 4G+5   MMA: BK/16 x tcgen05.mma (M128 x BN x K16) per stage, A from TMEM
+//   warp 1      MMA: BK/16 x tcgen05.mma (M128 x BN x K16) per stage, A from TMEM
+//   warps 2, 3, 4G+4, 4G+5  epilogue: D out of TMEM (double-buffered when it
+//               fits), scale, store y or a split-K partial
+//   warps 4..4G+3  G dequant warpgroups taking the A chunks in turn: thread =
+//               weight row (its TMEM lane); codes and scales from shared
+//               memory, stored to a TMEM ring of A chunks
+//
+// Prefill tiles of 256 tokens run on CTA pairs (2-CTA clusters): the even
+// CTA issues cta_group::2 MMAs (M = 256, 128 weight rows in each CTA's TMEM)
+// and each CTA stages only its half of the token tile.
 //
 // LoRA is folded into the same accumulator as extra K columns: the prologue
 // writes t' = (alpha/r) t / g (t = x . A^T, g = s_t or 1) as interleaved bf16
@@ -271,11 +275,14 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
     sh.abort = 0;
     fence_barrier_init();
   }
-  // warp roles: the dequant warpgroups take the lowest warp numbers (the
-  // schedulers favour them when a sub-partition is busy, and a lagging dequant
-  // warp holds up its whole A chunk), then the four epilogue warps, then the
-  // TMA and MMA issuers
-  constexpr int kEpi = 4 * G, kTma = 4 * G + 4, kMma = 4 * G + 5;
+  // warp roles: the TMA and MMA issuers take the lowest warp numbers, which
+  // the schedulers favour on a busy sub-partition (an MMA issuer sharing its
+  // sub-partition with three busy dequant warps otherwise slows to about 70
+  // cycles per MMA); then two epilogue warps (lane quarters 2, 3), the
+  // dequant warpgroups, and the other two epilogue warps (quarters 0, 1).
+  // Every warp w that touches TMEM serves lane quarter w % 4.
+  constexpr int kTma = 0, kMma = 1, kEpi = 2, kDqEnd = 4 + 4 * G;
+  const bool epi_warp = warp == 2 || warp == 3 || warp >= kDqEnd;
   if (warp == kMma) {
     if constexpr (PAIR)
       tmem_alloc_pair(&sh.tmem, C::TMEM_COLS);
@@ -309,9 +316,10 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
   if (warp == kTma) {
     // ------------------------------ TMA ------------------------------
     // The weight stream does not depend on the prologue kernel that writes
-    // the f16 x and t' (this kernel may start while it runs, as its
-    // programmatic dependent): the first ring of stages gets its codes and
-    // scales at once, then x waits for the prologue to complete.
+    // t' (and, on the f16 path, the f16 x): this kernel may start while it
+    // runs, as its programmatic dependent.  The first ring of stages gets its
+    // codes and scales at once; f16 x waits for the prologue to complete,
+    // bf16 x does not, and t' (the LoRA stages) always does.
     if (elect_one()) {
       struct Cursor {
         int u = -1, c = 0, j = 0, nt = 0, mt = 0, sp = 0, c0 = 0, nk = 0, nl = 0;
@@ -348,6 +356,7 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
         // column of the first sub-tile: K offset, or the LoRA sub-tile (past
         // the tensor's width reads as zeros)
         const int col0 = k.c < k.nk ? (k.c0 + k.c) * BK : (k.c - k.nk) * KSUB * 64;
+        if (!F16 && k.c >= k.nk) griddep_wait();  // t' is the prologue's
         if constexpr (PAIR) {
           if (rank == 0) mbar_arrive_expect_tx(fb, 2 * C::X_BYTES);
           const uint32_t fbc = cluster_addr(fb, 0);
@@ -366,7 +375,7 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
         issue_w(kw, static_cast<int>(nw));
         ++nw;
       }
-      griddep_wait();
+      if constexpr (F16) griddep_wait();
       uint32_t nx = 0;
       bool ok = true;
       while (nx < nw) {
@@ -479,14 +488,14 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
       volatile int no_abort = 0;
       mbar_wait(&sh.done, 0, &no_abort, p.status);
     }
-  } else if (warp >= kEpi) {
+  } else if (epi_warp) {
     // ------------------------------ epilogue ------------------------------
     // Layer fields are copied to registers once per unit: read through the
     // parameter reference they would be re-read after every store (the
     // compiler cannot rule out aliasing), each a dependent memory round trip.
     const int q = warp & 3;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
-    griddep_wait();  // the per-token exponents come from the prologue kernel
+    if constexpr (F16) griddep_wait();  // the per-token exponents come from the prologue kernel
     uint32_t units = 0;
     for (int u = ustart; u < p.total_units; u += ustep, ++units) {
       int j, nt, mt, sp, c0, nk, nl;
