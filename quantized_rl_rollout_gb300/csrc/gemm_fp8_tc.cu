@@ -142,13 +142,28 @@ __global__ void __launch_bounds__(THREADS, 1) fp8_gemm_tc_kernel(const __grid_co
       const float f = __fmul_rn(sa, sw);
       if (!mbar_wait(&sh.tfull[buf], buse & 1, abort, p.status)) break;
       tc_fence_after();
+      // promotion acc += f P on the paired fp32 pipe (each half an ordinary
+      // correctly rounded fp32 FMA), two TMEM loads in flight
+      uint64_t f2;
+      asm("mov.b64 %0, {%1, %1};" : "=l"(f2) : "f"(f));
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_addr + buf * BN + 128 * h + 32 * c, r);
+      for (int c = 0; c < 4; c += 2) {
+        uint32_t r[2][32];
+        tmem_ld32(tmem + lane_addr + buf * BN + 128 * h + 32 * c, r[0]);
+        tmem_ld32(tmem + lane_addr + buf * BN + 128 * h + 32 * (c + 1), r[1]);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(f, __uint_as_float(r[j]), acc[32 * c + j]);
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            float& a0 = acc[32 * (c + u) + j];
+            float& a1 = acc[32 * (c + u) + j + 1];
+            uint64_t a2, p2;
+            asm("mov.b64 %0, {%1, %2};" : "=l"(a2) : "f"(a0), "f"(a1));
+            asm("mov.b64 %0, {%1, %2};" : "=l"(p2) : "r"(r[u][j]), "r"(r[u][j + 1]));
+            asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a2) : "l"(f2), "l"(p2));
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a2));
+          }
       }
       tc_fence_before();
       __syncwarp();

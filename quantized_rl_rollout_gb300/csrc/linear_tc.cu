@@ -63,6 +63,14 @@ namespace qrr {
 // compile every stamp away.
 #ifdef QRR_TRACE_BUILD
 __device__ unsigned long long qrr_trace_buf[8][4][256];
+// global-timer stamps per CTA: start, x stream released, first MMA, end
+__device__ unsigned long long qrr_gtrace_buf[256][4];
+#define QRR_GSTAMP(ev)                                               \
+  do {                                                               \
+    unsigned long long t_;                                           \
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));           \
+    if (blockIdx.x < 256) qrr_gtrace_buf[blockIdx.x][ev] = t_;       \
+  } while (0)
 #define QRR_STAMP(role, ev, idx) \
   do {                                                                  \
     if (blockIdx.x == 0 && (idx) < 256) qrr_trace_buf[role][ev][idx] = clock64(); \
@@ -70,6 +78,9 @@ __device__ unsigned long long qrr_trace_buf[8][4][256];
 #else
 #define QRR_STAMP(role, ev, idx) \
   do {                           \
+  } while (0)
+#define QRR_GSTAMP(ev) \
+  do {                 \
   } while (0)
 #endif
 
@@ -238,6 +249,7 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &sh.abort;
   constexpr int KSUB = C::KSUB;
+  if (threadIdx.x == 0) QRR_GSTAMP(0);
   // CTA pairs (2-CTA clusters): both CTAs walk the same units, the even one
   // (rank 0) issues the pair's MMAs and holds the barriers the pair meets on
   const uint32_t rank = PAIR ? cluster_rank() : 0u;
@@ -376,6 +388,7 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
         ++nw;
       }
       if constexpr (F16) griddep_wait();
+      QRR_GSTAMP(1);
       uint32_t nx = 0;
       bool ok = true;
       while (nx < nw) {
@@ -471,6 +484,7 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
             }
             if constexpr (C::SLOT_BARS) commit(&sh.a_empty[at.idx]);
             QRR_STAMP(1, 1, chunks);
+            if (chunks == 0) QRR_GSTAMP(2);
             ++chunks;
           }
           QRR_STAMP(2, 0, chunks / C::CPS);
@@ -803,6 +817,7 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) QRR_GSTAMP(3);
   // a pair ends together: no remote arrive or x half may reach a CTA that
   // has exited, and the pair's TMEM is released by both
   if constexpr (PAIR) cluster_sync();
@@ -907,8 +922,12 @@ cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, bool pair, bool after
 extern "C" int qrr_trace_read(unsigned long long* host) {
   return static_cast<int>(cudaMemcpyFromSymbol(host, qrr::qrr_trace_buf, sizeof(qrr::qrr_trace_buf)));
 }
+extern "C" int qrr_gtrace_read(unsigned long long* host) {
+  return static_cast<int>(cudaMemcpyFromSymbol(host, qrr::qrr_gtrace_buf, sizeof(qrr::qrr_gtrace_buf)));
+}
 extern "C" int qrr_trace_clear(void) {
   static unsigned long long zeros[8 * 4 * 256] = {};
+  cudaMemcpyToSymbol(qrr::qrr_gtrace_buf, zeros, sizeof(qrr::qrr_gtrace_buf));
   return static_cast<int>(cudaMemcpyToSymbol(qrr::qrr_trace_buf, zeros, sizeof(zeros)));
 }
 #endif
