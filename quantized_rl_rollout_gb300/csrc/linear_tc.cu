@@ -575,8 +575,18 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
         } else {
           __nv_bfloat16* const dst = y + static_cast<int64_t>(mb) * N + n;
           if (cnt >= CW) {
+            // Token pairs: lanes n (even) and n + 1 swap one value, so each
+            // lane holds two adjacent outputs of one token and writes them as
+            // one word (the even lane token i, the odd lane token i + 1): one
+            // packed conversion and one store per two outputs.
+            const int odd = lane & 1;
+            uint32_t* const dstw = reinterpret_cast<uint32_t*>(dst - odd);
 #pragma unroll
-            for (int i = 0; i < CW; ++i) dst[static_cast<int64_t>(i) * N] = __float2bfloat16_rn(v[i]);
+            for (int i = 0; i < CW; i += 2) {
+              const float recv = __shfl_xor_sync(0xFFFFFFFFu, odd ? v[i] : v[i + 1], 1);
+              const uint32_t w = odd ? pack_bf16x2(recv, v[i + 1]) : pack_bf16x2(v[i], recv);
+              dstw[static_cast<int64_t>(i + odd) * (N / 2)] = w;
+            }
           } else {
 #pragma unroll
             for (int i = 0; i < CW; ++i)
