@@ -170,6 +170,46 @@ def test_grouped_layer_set(q, m):
 
 
 @pytest.mark.parametrize("m", [1, 8, 64])
+def test_grouped_call_in_cuda_graph(q, m):
+    """The grouped call captured in a CUDA graph (workspace and outputs
+    supplied, so the call allocates nothing) replays to the same bits as a
+    direct call, also after the captured x buffers are refilled."""
+    shapes = [(384, 1024, 32), (256, 2048, 0), (512, 768, 64)]
+    layers = []
+    for i, (n, k, r) in enumerate(shapes):
+        W, codes, scales, ts, A, B, alpha = _layer(q, n, k, r, f"graph{i}")
+        x = inputs.activations(m, k, inputs.derive_seed(0, "graph-x", i, m), device=DEV)
+        y = torch.empty(m, n, dtype=torch.bfloat16, device=DEV)
+        layers.append(dict(x=x, codes=codes, scales=scales, tensor_scale=ts, lora_A=A, lora_B=B, alpha=alpha, y=y))
+    ws = torch.empty(q.linear_nvfp4_lora_grouped_workspace_bytes(layers), dtype=torch.uint8, device=DEV)
+    q.linear_nvfp4_lora_grouped(layers, workspace=ws)
+    torch.cuda.synchronize()
+    direct = [d["y"].clone() for d in layers]
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        q.linear_nvfp4_lora_grouped(layers, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        q.linear_nvfp4_lora_grouped(layers, workspace=ws)
+    for d in layers:
+        d["y"].zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    for i, d in enumerate(layers):
+        assert torch.equal(d["y"], direct[i]), f"replay differs, layer {i}"
+    for i, d in enumerate(layers):
+        d["x"].copy_(inputs.activations(m, d["x"].shape[1], inputs.derive_seed(1, "graph-x", i, m), device=DEV))
+    graph.replay()
+    torch.cuda.synchronize()
+    for i, d in enumerate(layers):
+        _assert_close(d["y"], _ref(d["x"], d["codes"], d["scales"], d["tensor_scale"], d["lora_A"], d["lora_B"],
+                                   d["alpha"]), f"graph replay, new x, layer {i} m={m}")
+
+
+@pytest.mark.parametrize("m", [1, 8, 64])
 def test_grouped_8b_decode_sampled(q, m):
     """The 8B-class layer set in one grouped call, the bench's launch
     configuration: every CTA runs several units, so accumulator reuse, issuer
