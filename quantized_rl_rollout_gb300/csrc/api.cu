@@ -134,9 +134,11 @@ LinPlan plan_linear(int64_t M, const LinIn* in, int count) {
     if (p.f16) off += round_up(static_cast<size_t>(M) * 4);
     L.part_off = off;
     if (L.splits > 1) off += round_up(static_cast<size_t>(L.splits) * M * in[j].N * 4);
-    // decode LoRA down projection: fp32 partials over 512-wide K slices (many
-    // CTAs in one wave; each reads a short slice of x and A)
-    L.lora_slice = 512;
+    // decode LoRA down projection: fp32 partials over K slices.  Short slices
+    // give many CTAs in one wave, each reading a short slice of x and A; the
+    // last CTA of a token tile then sums M r partials per slice, so the slices
+    // grow with the token count to keep that sum off the critical path.
+    L.lora_slice = M <= 8 ? 512 : M <= 32 ? 1024 : 2048;
     L.lora_ks = static_cast<int>((in[j].K + L.lora_slice - 1) / L.lora_slice);
     L.tpart_off = off;
     if (in[j].r > 0 && p.f16) off += round_up(static_cast<size_t>((L.lora_ks + 3) & ~3) * M * in[j].r * 4);
