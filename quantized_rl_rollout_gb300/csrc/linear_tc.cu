@@ -844,11 +844,10 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
 
 namespace {
 
-// dequant warpgroups of the decode (f16) kernels
-#ifndef QRR_DECODE_GROUPS
-#define QRR_DECODE_GROUPS 3
-#endif
-constexpr int kDecodeGroups = QRR_DECODE_GROUPS;
+// dequant warpgroups of the decode (f16) kernels: three per lane quarter
+// (measured: two are about 6% slower at 1 and 8 tokens, and four do not fit
+// the TMEM ring beside double-buffered 64-column accumulators)
+constexpr int kDecodeGroups = 3;
 
 // grid: CTAs for units one at a time; a paired launch runs min(units,
 // co-resident 2-CTA clusters) clusters instead.
