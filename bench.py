@@ -502,11 +502,20 @@ def dist_setup(n_gpus):
 
 
 def max_over_ranks(dist, value):
+    """The largest of every rank's value (NCCL on GPU ranks, gloo on CPU)."""
     if dist is None:
         return value
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job(dist, world, bytes_per_rank, ms_per_rank):
+    """Replicas: every rank moves the same bytes; the job's throughput is
+    all ranks' bytes over the slowest rank's time (GB/s), or None."""
+    ms = max_over_ranks(dist, ms_per_rank)
+    return world * bytes_per_rank / ms / 1e6 if ms else None
 
 
 def main():
@@ -615,8 +624,7 @@ def main():
 
     step_ms = sum(med.values())
     step_ms = max_over_ranks(dist, step_ms)
-    dec_ms_all = max_over_ranks(dist, dec_ms) if dec_ms else 0.0
-    value = world * dec_bytes / dec_ms_all / 1e6 if dec_ms_all else None
+    value = whole_job(dist, world, dec_bytes, dec_ms) if dec_ms else None
 
     # dominant phase -> roofline object
     dom = max(phases, key=lambda p: med[p])
