@@ -33,7 +33,7 @@ def _rank(rank, world, port, out):
 
 def test_replicas_two_gloo_ranks():
     world = 2
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_rank, args=(world, _free_port(), out), nprocs=world, join=True)
         res = dict(out)
