@@ -10,13 +10,23 @@ tokens.  One step is one pass of the whole hot path over that layer set:
   decode   W4A16 + LoRA linear of all 7 layers at M = 1, 8 and 64 (one
            grouped call per token count)
   prefill  the same linears at M = 4096 (activations with 1% x10 channels)
-  fp8      FP8 path at M = 4096: activation 1x128 quantize, 128x128 weight
-           re-quantize, blockwise-scaled GEMM
+  fp8      FP8 path at M = 4096: 128x128 weight re-quantize (fp8_requant),
+           activation 1x128 quantize (fp8_act_quant), blockwise-scaled GEMM
 
-On request (--phases ...,decode32b,requant32b) the 32B-class stack (64 layers
-of hidden 5120, LoRA r = 64) is measured too: decode at M = 64 (one grouped
-call per layer) and the full bf16 -> NVFP4 re-quantization of its 31.2 G
-weight elements.  It is another configuration, not part of the step.
+Re-quantization follows a training step: the bf16 masters alternate between W
+and W' = bf16(W + N(0, 1e-4)) from step to step, so every step recalibrates
+new weights.
+
+After the step, in a timed region of its own, the 32B-class stack (64 layers
+of hidden 5120, LoRA r = 64) is measured too (unless --no-32b): the full bf16
+-> NVFP4 re-quantization of its 31.2 G weight elements and decode at M = 64
+(one grouped call per layer).  It is another configuration, not part of the
+step, and is reported in ``breakdown`` beside the step's phases.
+
+Roofline fractions are given against the measured peaks (``MEASURED_PEAKS.json``;
+the FP8 dense peak is measured in the same run with torch._scaled_mm) and, as a
+second figure, against GB300's published dense numbers (8 TB/s HBM, 2.25
+PFLOP/s bf16, 4.5 PFLOP/s FP8).
 
 Each phase is timed with CUDA events on the launching stream after an L2
 flush (a 512 MB write), so no phase reads its weights from L2 left by the
@@ -57,6 +67,8 @@ PREFILL_TOKENS = 4096
 R = 32
 ALPHA = 2.0 * R
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+# GB300's published dense figures (per GPU), reported beside the measured peaks
+SPEC_PEAKS = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0, "fp8_tflops": 4500.0}
 
 
 # DRAM traffic per launch of each phase's main kernel, from an ncu launch list
@@ -69,7 +81,8 @@ PHASE_KERNELS = {  # phase -> (kernel name prefix, template arguments as ncu pri
     "decode_m8": ("w4a16_tc_kernel", "<16, 256, 1, 3, 0>"),
     "decode_m64": ("w4a16_tc_kernel", "<64, 256, 1, 3, 0>"),
     "requant": ("nvfp4_encode_kernel", ""),
-    "fp8_quant": ("fp8_w128_kernel", ""),
+    "fp8_requant": ("fp8_w128_kernel", ""),
+    "fp8_act_quant": ("fp8_a1x128_kernel", ""),
     "fp8_gemm": ("fp8_gemm_tc_kernel", ""),
 }
 
@@ -164,64 +177,145 @@ def fp8_quant_bytes(layers, m):
     return w, a
 
 
+def fp8_gemm_flops(layers, m):
+    return sum(2 * m * l.n * l.k for l in layers)
+
+
+def measure_fp8_peak(device, n=8192, reps=10):
+    """Dense E4M3 GEMM throughput of torch._scaled_mm (cuBLASLt) at n^3 on this
+    GPU: best of `reps` back-to-back launches, TFLOP/s; None if unsupported."""
+    try:
+        a = torch.randn(n, n, device=device).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=device).to(torch.float8_e4m3fn).t()  # column-major operand
+        one = torch.ones((), device=device, dtype=torch.float32)
+        for _ in range(3):
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            e1.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        del a, b
+        return 2.0 * n ** 3 / best / 1e9
+    except Exception:  # noqa: BLE001 - an unsupported op leaves the nominal ratio in place
+        return None
+
+
 # ---------------------------------------------------------------------------
 
 
 class Clocks:
-    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    """SM clock, power and throttle reasons sampled DURING a region, read-only.
 
+    Polls NVML directly (libnvidia-ml through ctypes) every 10 ms, so even a
+    timed region of a few tens of milliseconds gets several samples; falls back
+    to ``nvidia-smi -lms 200`` when NVML cannot be loaded.  Nothing here changes
+    a setting of the GPU."""
+
+    # clocks-event-reason bits of NVML
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
     FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown," \
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown," \
              "clocks_event_reasons.sw_power_cap"
 
-    def __init__(self, index):
+    def __init__(self, index, period_s=0.01):
         self.index = index
+        self.period = period_s
+        self.samples = []  # (sm_mhz, max_mhz, reasons bitmask or names)
         self.proc = None
-        self.lines = []
         self.thread = None
+        self.stop_evt = threading.Event()
+        self.source = None
+
+    def _nvml_handle(self):
+        import ctypes
+
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        bus = None
+        try:
+            props = torch.cuda.get_device_properties(self.index)
+            bus = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+        except (AttributeError, RuntimeError):
+            bus = None
+        if bus is None or nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+        return nv, h
+
+    def _poll_nvml(self, nv, h):
+        import ctypes
+
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop_evt.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and get_reasons(h, ctypes.byref(rs)) == 0:
+                self.samples.append((float(clk.value), float(mx.value), int(rs.value)))
+            time.sleep(self.period)
 
     def start(self):
+        try:
+            nv, h = self._nvml_handle()
+            self.source = "nvml 10 ms"
+            self.thread = threading.Thread(target=self._poll_nvml, args=(nv, h), daemon=True)
+            self.thread.start()
+            return
+        except OSError:
+            pass
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.source = "nvidia-smi 200 ms"
+            self.thread = threading.Thread(target=self._read_smi, daemon=True)
             self.thread.start()
         except OSError:
             self.proc = None
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
-    def stop(self):
-        if self.proc is None:
-            return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        if self.thread:
-            self.thread.join(timeout=2)
-        sm, mx, reasons = [], [], set()
+    def _read_smi(self):
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.strip().split(",")]
             if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                sm, mx = float(parts[0]), float(parts[1])
             except ValueError:
                 continue
-            for name, val in zip(names, parts[4:8]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
+            self.samples.append((sm, mx, [n for n, v in zip(names, parts[4:8]) if v.lower() == "active"]))
+
+    def stop(self):
+        self.stop_evt.set()
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        if not self.samples:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        reasons = set()
+        for _, _, r in self.samples:
+            if isinstance(r, int):
+                reasons.update(name for bit, name in self.REASONS.items() if r & bit)
+            else:
+                reasons.update(r)
+        sm = [a for a, _, _ in self.samples]
+        return {"sm_mhz": statistics.median(sm), "sm_mhz_min": min(sm), "sm_max_mhz": max(b for _, b, _ in self.samples),
+                "samples": len(sm), "source": self.source, "reasons": sorted(reasons)}
 
 
 class Workload:
@@ -233,6 +327,10 @@ class Workload:
         self.layers = configs.LAYERS_8B
         L = self.layers
         self.W = [inputs.weight(l.n, l.k, inputs.derive_seed(seed, "8b", l.name, "W"), device=device) for l in L]
+        # the trainer's N(0, 1e-4) update of every master: successive steps
+        # re-quantize W and W' in turn, so each re-quantization sees new weights
+        self.Wu = [inputs.updated(w, inputs.derive_seed(seed, "8b", l.name, "update")) for w, l in zip(self.W, L)]
+        self.masters = self.W
         self.lora = [inputs.lora(R, l.k, l.n, inputs.derive_seed(seed, "8b", l.name, "lora"), device=device)[:2]
                      for l in L]
         self.nv = [(torch.empty(l.n, l.k // 2, dtype=torch.uint8, device=device),
@@ -258,9 +356,12 @@ class Workload:
         self.flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
         self.launches = 0
 
+    def next_step(self):
+        self.masters = self.Wu if self.masters is self.W else self.W
+
     # each phase returns the number of library kernels it launched
     def requant(self):
-        self.q.requantize_weights(self.W, self.nv, self.q.FORMAT_NVFP4, workspace=self.rq_ws)
+        self.q.requantize_weights(self.masters, self.nv, self.q.FORMAT_NVFP4, workspace=self.rq_ws)
         return 2
 
     def _group(self, xs, ys):
@@ -280,11 +381,14 @@ class Workload:
         self.q.linear_nvfp4_lora_grouped(self.gp, workspace=self.ws)
         return 2
 
-    def fp8_quant(self):
-        self.q.requantize_weights(self.W, self.f8w, self.q.FORMAT_FP8_W128)
+    def fp8_requant(self):
+        self.q.requantize_weights(self.masters, self.f8w, self.q.FORMAT_FP8_W128)
+        return 1
+
+    def fp8_act_quant(self):
         for i, _ in enumerate(self.layers):
             self.q.quantize_fp8_a1x128(self.xp[i], q=self.f8a[i][0], scales=self.f8a[i][1])
-        return 1 + len(self.layers)
+        return len(self.layers)
 
     def fp8_gemm(self):
         for i, _ in enumerate(self.layers):
@@ -338,9 +442,9 @@ class Workload:
 
 
 # one step over the 8B-class workload; the 32B-class stack (another
-# configuration, ~85 GB resident) is measured only when asked for by --phases
-PHASES = ["requant", "decode_m1", "decode_m8", "decode_m64", "prefill", "fp8_quant", "fp8_gemm"]
-EXTRA_PHASES = ["decode32b", "requant32b"]
+# configuration, ~85 GB resident) is timed after it, in a region of its own
+PHASES = ["requant", "decode_m1", "decode_m8", "decode_m64", "prefill", "fp8_requant", "fp8_act_quant", "fp8_gemm"]
+EXTRA_PHASES = ["requant32b", "decode32b"]
 
 
 def run_phase(w, name):
@@ -350,8 +454,10 @@ def run_phase(w, name):
         return w.decode(int(name[len("decode_m"):]))
     if name == "prefill":
         return w.prefill()
-    if name == "fp8_quant":
-        return w.fp8_quant()
+    if name == "fp8_requant":
+        return w.fp8_requant()
+    if name == "fp8_act_quant":
+        return w.fp8_act_quant()
     if name == "decode32b":
         return w.decode32()
     if name == "requant32b":
@@ -365,6 +471,7 @@ def timed_steps(w, steps, phases):
     times = {p: [] for p in phases}
     launches = 0
     for _ in range(steps):
+        w.next_step()
         for p in phases:
             w.do_flush()
             e0 = torch.cuda.Event(enable_timing=True)
@@ -478,6 +585,56 @@ def oracle_decode_sample(seconds_target):
     return bytes_done / secs / 1e9, secs, desc
 
 
+def oracle_phase_rates(seconds_each=3.0):
+    """The oracle's rate on each other phase of the step, on bounded samples
+    (each repeated until about `seconds_each`): NVFP4 quantization and FP8
+    128x128 quantization of one 4096x4096 weight (GB/s of bf16 read), FP8
+    1x128 quantization of 256 tokens x 4096, and the float64 blockwise FP8 GEMM
+    for 16 tokens of a 4096x4096 layer (GFLOP/s).  Single process."""
+    import oracle
+
+    g = np.random.default_rng(1)
+    n = k = 4096
+    w = oracle.formats.bf16_rne(g.standard_normal((n, k)).astype(np.float32) * np.float32(0.02))
+    x = oracle.formats.bf16_rne(g.standard_normal((256, k)).astype(np.float32))
+
+    def rate(fn, units):
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            out = fn()
+            reps += 1
+            if time.perf_counter() - t0 >= seconds_each:
+                break
+        return units * reps / (time.perf_counter() - t0), reps, out
+
+    out = {}
+    r, reps, _ = rate(lambda: oracle.nvfp4.quantize(w), 2.0 * n * k / 1e9)
+    out["nvfp4_quantize"] = {"value": r, "unit": "GB/s", "sample": f"one {n}x{k} weight, {reps} reps"}
+    r, reps, (qw, sw) = rate(lambda: oracle.fp8.quantize_w128x128(w), 2.0 * n * k / 1e9)
+    out["fp8_w128_quantize"] = {"value": r, "unit": "GB/s", "sample": f"one {n}x{k} weight, {reps} reps"}
+    r, reps, (qa, sa) = rate(lambda: oracle.fp8.quantize_a1x128(x), 2.0 * x.size / 1e9)
+    out["fp8_a1x128_quantize"] = {"value": r, "unit": "GB/s", "sample": f"256x{k} activations, {reps} reps"}
+    r, reps, _ = rate(lambda: oracle.fp8.gemm_blockwise(qa[:16], sa[:16], qw, sw), 2.0 * 16 * n * k / 1e9)
+    out["fp8_gemm"] = {"value": r, "unit": "GFLOP/s", "sample": f"16 tokens x {n}x{k} layer, {reps} reps"}
+    return out
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:  # noqa: BLE001 - threadpoolctl is optional
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return None
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -526,6 +683,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--phases", default=",".join(PHASES))
     ap.add_argument("--skip-extras", action="store_true", help="no e2e or CPU-oracle legs (for profiler runs)")
+    ap.add_argument("--no-32b", action="store_true", help="do not build or time the 32B-class stack")
     ap.add_argument("--record-traffic", metavar="NCU_CSV",
                     help="write profiles/traffic.json from an ncu launch list (dram bytes) and exit")
     args = ap.parse_args()
@@ -562,11 +720,17 @@ def main():
     qrr.lib()
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    phases = [p for p in args.phases.split(",") if p]
+    phases = [p for p in args.phases.split(",") if p and p not in EXTRA_PHASES]
+    extra = [p for p in args.phases.split(",") if p in EXTRA_PHASES]
+    if not args.no_32b:
+        extra = extra or list(EXTRA_PHASES)
+    peaks = load_peaks()
+    fp8_meas = measure_fp8_peak(device)
     w = Workload(qrr, device)
     w.requant()  # valid NVFP4 weights for every phase, whichever phases run
     # warm-up (untimed)
     for _ in range(warmup):
+        w.next_step()
         for p in phases:
             run_phase(w, p)
     torch.cuda.synchronize()
@@ -584,60 +748,89 @@ def main():
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
 
+    # the 32B-class stack: another configuration, timed in a region of its own
+    # after the step (same protocol: warm-up, L2 flush before every phase)
+    per_extra, clk32, wall32 = {}, None, None
+    if extra:
+        for p in extra:  # builds the stack on first use
+            run_phase(w, p)
+        for _ in range(max(1, warmup - 2)):
+            for p in extra:
+                run_phase(w, p)
+        torch.cuda.synchronize()
+        clocks32 = Clocks(local)
+        clocks32.start()
+        t0 = time.perf_counter()
+        per_extra, l32 = timed_steps(w, args.steps, extra)
+        torch.cuda.synchronize()
+        wall32 = time.perf_counter() - t0
+        clk32 = clocks32.stop()
+
     med = {p: statistics.median(v) for p, v in per_phase.items()}
+    med_extra = {p: statistics.median(v) for p, v in per_extra.items()}
     L = configs.LAYERS_8B
-    peaks = load_peaks()
-    fp8_peak = 2.0 * peaks["bf16_tflops"]  # nominal FP8:BF16 dense ratio of 2
+    fp8_peak = fp8_meas if fp8_meas else 2.0 * peaks["bf16_tflops"]
+    fp8_peak_source = "measured in this run (torch._scaled_mm E4M3 8192^3, best of 10)" if fp8_meas else \
+        "2 x measured bf16 (nominal FP8:BF16 ratio)"
+
+    def hbm(ms, b):
+        return {"ms": ms, "GB/s": b / ms / 1e6, "frac_hbm": b / ms / 1e6 / peaks["hbm_gbs"],
+                "frac_hbm_spec": b / ms / 1e6 / SPEC_PEAKS["hbm_gbs"], "bytes": b}
+
     breakdown = {}
     dec_bytes = 0
     dec_ms = 0.0
-    for p in phases:
-        ms = med[p]
+    for p, ms in list(med.items()) + list(med_extra.items()):
         if p.startswith("decode_m"):
             m = int(p[len("decode_m"):])
             b = decode_bytes(L, m, R)
             dec_bytes += b
             dec_ms += ms
-            breakdown[p] = {"ms": ms, "GB/s": b / ms / 1e6, "frac_hbm": b / ms / 1e6 / peaks["hbm_gbs"],
-                            "bytes": b}
+            breakdown[p] = hbm(ms, b)
         elif p == "requant":
-            b = requant_nvfp4_bytes(L)
-            breakdown[p] = {"ms": ms, "GB/s": b / ms / 1e6, "frac_hbm": b / ms / 1e6 / peaks["hbm_gbs"], "bytes": b}
+            breakdown[p] = hbm(ms, requant_nvfp4_bytes(L))
         elif p == "prefill":
             f = linear_flops(L, PREFILL_TOKENS, R)
             breakdown[p] = {"ms": ms, "TFLOP/s": f / ms / 1e9, "frac_bf16": f / ms / 1e9 / peaks["bf16_tflops"],
-                            "flops": f}
-        elif p == "fp8_quant":
-            bw, ba = fp8_quant_bytes(L, PREFILL_TOKENS)
-            breakdown[p] = {"ms": ms, "GB/s": (bw + ba) / ms / 1e6, "frac_hbm": (bw + ba) / ms / 1e6 / peaks["hbm_gbs"],
-                            "bytes": bw + ba}
+                            "frac_bf16_sustained": f / ms / 1e9 / peaks["bf16_tflops_sustained"],
+                            "frac_bf16_spec": f / ms / 1e9 / SPEC_PEAKS["bf16_tflops"], "flops": f}
+        elif p == "fp8_requant":
+            breakdown[p] = hbm(ms, fp8_quant_bytes(L, PREFILL_TOKENS)[0])
+        elif p == "fp8_act_quant":
+            breakdown[p] = hbm(ms, fp8_quant_bytes(L, PREFILL_TOKENS)[1])
+        elif p == "fp8_gemm":
+            f = fp8_gemm_flops(L, PREFILL_TOKENS)
+            breakdown[p] = {"ms": ms, "TFLOP/s": f / ms / 1e9, "frac_fp8": f / ms / 1e9 / fp8_peak,
+                            "frac_fp8_spec": f / ms / 1e9 / SPEC_PEAKS["fp8_tflops"], "flops": f,
+                            "scale_mode": "fp32"}
         elif p == "decode32b":
             c32 = configs.DECODE_32B
-            b = c32["depth"] * decode_bytes(configs.LAYERS_32B, c32["tokens"], c32["r"])
-            breakdown[p] = {"ms": ms, "GB/s": b / ms / 1e6, "frac_hbm": b / ms / 1e6 / peaks["hbm_gbs"], "bytes": b}
+            breakdown[p] = hbm(ms, c32["depth"] * decode_bytes(configs.LAYERS_32B, c32["tokens"], c32["r"]))
+            breakdown[p]["region"] = "separate (after the step)"
         elif p == "requant32b":
-            b = configs.DECODE_32B["depth"] * requant_nvfp4_bytes(configs.LAYERS_32B)
-            breakdown[p] = {"ms": ms, "GB/s": b / ms / 1e6, "frac_hbm": b / ms / 1e6 / peaks["hbm_gbs"], "bytes": b}
-        elif p == "fp8_gemm":
-            f = sum(2 * PREFILL_TOKENS * l.n * l.k for l in L)
-            breakdown[p] = {"ms": ms, "TFLOP/s": f / ms / 1e9, "frac_fp8_nominal": f / ms / 1e9 / fp8_peak, "flops": f}
+            breakdown[p] = hbm(ms, configs.DECODE_32B["depth"] * requant_nvfp4_bytes(configs.LAYERS_32B))
+            breakdown[p]["region"] = "separate (after the step)"
 
     step_ms = sum(med.values())
     step_ms = max_over_ranks(dist, step_ms)
     value = whole_job(dist, world, dec_bytes, dec_ms) if dec_ms else None
 
-    # dominant phase -> roofline object
+    # dominant phase of the step -> roofline object
     dom = max(phases, key=lambda p: med[p])
     d = breakdown[dom]
     if "GB/s" in d:
         roof = {"bound": "hbm", "achieved": d["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": d["GB/s"] / peaks["hbm_gbs"], "traffic": None, "kernel_phase": dom}
+                "frac": d["GB/s"] / peaks["hbm_gbs"], "peak_spec": SPEC_PEAKS["hbm_gbs"],
+                "frac_spec": d["GB/s"] / SPEC_PEAKS["hbm_gbs"]}
     elif dom == "fp8_gemm":
         roof = {"bound": "tensor", "achieved": d["TFLOP/s"], "peak": fp8_peak, "unit": "TFLOP/s",
-                "frac": d["TFLOP/s"] / fp8_peak, "traffic": None, "kernel_phase": dom}
+                "frac": d["TFLOP/s"] / fp8_peak, "peak_spec": SPEC_PEAKS["fp8_tflops"],
+                "frac_spec": d["TFLOP/s"] / SPEC_PEAKS["fp8_tflops"]}
     else:
         roof = {"bound": "tensor", "achieved": d["TFLOP/s"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": d["TFLOP/s"] / peaks["bf16_tflops"], "traffic": None, "kernel_phase": dom}
+                "frac": d["TFLOP/s"] / peaks["bf16_tflops"], "peak_spec": SPEC_PEAKS["bf16_tflops"],
+                "frac_spec": d["TFLOP/s"] / SPEC_PEAKS["bf16_tflops"]}
+    roof["kernel_phase"] = dom
     roof["peak_source"] = peaks["source"]
     roof["traffic"] = load_traffic(dom)
 
@@ -649,18 +842,26 @@ def main():
         e2e = {"value": e_bytes / e_ms / 1e6, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms,
                "mode": "grouped C-ABI calls; pinned-host copies on a copy stream, overlapped with the other token counts"}
-        v, s, desc = oracle_decode_sample(seconds_target=12.0)
-        cpu = {"value": v, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc, "seconds": s}
+        v, s, desc = oracle_decode_sample(seconds_target=10.0)
+        bt = blas_threads()
+        cpu = {"value": v, "unit": "GB/s", "cores": bt or cpu_cores(), "kind": "oracle", "sample": desc, "seconds": s,
+               "blas_threads": bt, "host_cores": cpu_cores(),
+               "process": "single process; elementwise numpy on one core, float64 matmul on the BLAS threads",
+               "phases": oracle_phase_rates(seconds_each=2.5)}
 
+    if clk and clk.get("sm_mhz"):
+        clk["step_ms_x_sm_mhz"] = step_ms * clk["sm_mhz"]
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
                 "warmup": warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "nvfp4xbf16", "data": "synthetic",
                 "config": {"workload": WORKLOAD, "phases": phases, "l2": "flushed (512 MB write) before every phase",
-                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                           "separately_timed": extra},
                 "roofline": roof, "breakdown": breakdown, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": launches, "clocks": clk, "wall_s_timed": wall,
-                "peaks": peaks}
+                "gpu_launches": launches, "clocks": clk, "clocks_32b_region": clk32, "wall_s_timed": wall,
+                "wall_s_timed_32b": wall32,
+                "peaks": dict(peaks, fp8_tflops=fp8_peak, fp8_source=fp8_peak_source, spec=SPEC_PEAKS)}
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()

@@ -39,7 +39,8 @@
  *    orientation W[N = out][K = in], y = x . W^T; LoRA uses A[r][K], B[N][r].
  *  - bf16 / fp32 / byte pointers must be 16-byte aligned.
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
- *    legacy default stream) and never synchronizes with the host.  The tensor
+ *    legacy default stream) and never synchronizes with the host, except
+ *    qrr_get_last_device_status, the one explicit sync point.  The tensor
  *    scale stays on the device, so quantize -> linear never round-trips.
  *  - Return value: QRR_OK, or an error detected on the host before anything
  *    is launched (invalid argument, unsupported shape, misalignment, small
@@ -48,8 +49,8 @@
  *    OR-ed into it (QRR_DEV_NONFINITE: a non-finite input was seen; the
  *    outputs are then unspecified; QRR_DEV_TIMEOUT: a tensor-core pipeline
  *    wait gave up after its bounded time and the kernel ended early).  The
- *    library never clears it; the caller
- *    zeroes it and reads it when it chooses.
+ *    library never clears it; the caller zeroes it and reads it when it
+ *    chooses (qrr_get_last_device_status).
  */
 #ifndef QRR_H_
 #define QRR_H_
@@ -110,7 +111,9 @@ qrr_status qrr_quantize_nvfp4(const void* W, int64_t N, int64_t K, uint8_t* code
  * Key Features: NVFP4 weight path, activations/logits in higher precision;
  * "QeRL: Beyond Efficiency", abstract: NVFP4 with LoRA):
  *   y = x . W_hat^T + (alpha / r) . (x . A^T) . B^T,  y in bf16
- *   x            bf16 [M][K], M >= 0, K a multiple of 256
+ *   x            bf16 [M][K], M >= 0, K a multiple of 256 (the block-scale
+ *                rows, K/16 bytes, are fetched by TMA, whose row pitch must be
+ *                a multiple of 16 bytes)
  *   codes/scales/tensor_scale: an NVFP4 weight [N][K] as qrr_quantize_nvfp4 writes it
  *   lora_A       bf16 [r][K] or NULL;  lora_B bf16 [N][r] or NULL
  *   r            LoRA rank, 0..64 and a multiple of 8 when the adapter is on;
@@ -131,11 +134,10 @@ qrr_status qrr_linear_nvfp4_lora(const void* x, int64_t M, int64_t K, const uint
 /* ------------------------------------------------------------------------ */
 /* W4A16 + LoRA linear that allocates nothing.  The pages have no counterpart
  * to this call; it exists for callers that cannot get device memory of their
- * own: code that holds only the input and output buffers it was handed (a
- * plugin or FFI binding inside a host framework that owns every device
- * allocation, or a serving process that reserved its whole HBM budget up
- * front), and code that runs while a CUDA graph is being captured, where
- * cudaMalloc is not allowed.
+ * own: code that holds only the input and output buffers it was handed, such
+ * as a plugin or FFI binding inside a host framework that owns every device
+ * allocation and hands out no scratch, or a serving process that reserved its
+ * whole HBM budget up front and has none left to give.
  *
  * Same arguments, contract and result as qrr_linear_nvfp4_lora, minus the
  * workspace.  Its scratch is a fixed block of QRR_NOALLOC_SCRATCH_BYTES of
@@ -145,7 +147,10 @@ qrr_status qrr_linear_nvfp4_lora(const void* x, int64_t M, int64_t K, const uint
  *    r)) exceeds QRR_NOALLOC_SCRATCH_BYTES return QRR_ERR_WORKSPACE and launch
  *    nothing.
  *  - The first call on each device looks up the block's device address (with
- *    that device current); make that first call before any stream capture.
+ *    that device current) and keeps it for the life of the process; make that
+ *    first call before any stream capture.  The address is kept per device
+ *    number, so a device reset (cudaDeviceReset, or tearing down the primary
+ *    context) while the library stays loaded is not supported.
  *  - Every call shares the block and it keeps the last call's contents (what
  *    must start at zero is cleared on the stream).  Calls that overlap on the
  *    GPU, on different streams or different host threads, race on it: order
@@ -237,6 +242,45 @@ size_t qrr_requantize_workspace_bytes(int32_t count);
 qrr_status qrr_requantize_weights(const qrr_weight_desc* descs, int32_t count, int32_t format,
                                   int32_t scale_mode, void* workspace, size_t workspace_bytes,
                                   int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* The explicit sync point for device-detected conditions: copies the status
+ * word `dev_status` (device int32, as passed to the calls above) into
+ * `*host_out` once every call queued on `stream` before it has finished, then
+ * returns.  It blocks the calling host thread on `stream` (the only call of
+ * the library that does) and does not clear the word.  QRR_ERR_INVALID_ARG for
+ * a NULL pointer, QRR_ERR_CUDA when the copy or the stream fails (an error of
+ * an earlier kernel on the stream surfaces here). */
+qrr_status qrr_get_last_device_status(int32_t* host_out, const int32_t* dev_status, void* stream);
+
+/* One query for every call's scratch need, by operation:
+ *   QRR_OP_QUANTIZE_NVFP4      (sizes unused)
+ *   QRR_OP_LINEAR_NVFP4_LORA   M tokens, N outputs, K inputs, LoRA rank r
+ *   QRR_OP_REQUANTIZE_WEIGHTS  M = number of descriptors
+ *   QRR_OP_QUANTIZE_FP8, QRR_OP_GEMM_FP8: no scratch (0)
+ * It returns the same value as the per-call query; 0 for an unknown op or
+ * invalid sizes. */
+typedef enum qrr_op {
+  QRR_OP_QUANTIZE_NVFP4 = 0,
+  QRR_OP_LINEAR_NVFP4_LORA = 1,
+  QRR_OP_REQUANTIZE_WEIGHTS = 2,
+  QRR_OP_QUANTIZE_FP8 = 3,
+  QRR_OP_GEMM_FP8 = 4
+} qrr_op;
+size_t qrr_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t r);
+
+/* Probe of the bounded-wait path.  Every tensor-core pipeline wait of the
+ * library gives up after a bounded time (about 2 s), raises QRR_DEV_TIMEOUT,
+ * lets its CTA drain its copies, free its tensor memory and exit, so a broken
+ * pipeline ends the kernel instead of hanging the GPU.  This launches one CTA
+ * that allocates tensor memory and waits, through that same bounded wait, on
+ * a barrier with a give-up time of `limit_cycles` SM clock cycles
+ * (1 .. about 4e9).  arrive = 0: nothing arrives, so the wait runs out and
+ * QRR_DEV_TIMEOUT is OR-ed into *dev_status; arrive = 1: the barrier is
+ * completed first and nothing is flagged.  `cycles` (nullable, device int64)
+ * receives the wait's duration in SM cycles.  The context stays usable
+ * either way. */
+qrr_status qrr_wait_probe(int64_t limit_cycles, int32_t arrive, int32_t* dev_status, int64_t* cycles, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Conformance probe: the library's own float32 -> E2M1 / E4M3 rounding

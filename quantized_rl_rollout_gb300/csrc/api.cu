@@ -1,6 +1,7 @@
 // C ABI of the library (include/qrr.h): host-side validation, workspace
-// carving and dispatch to the kernels.  Nothing here allocates device memory
-// or synchronizes with the host.
+// carving and dispatch to the kernels.  Nothing here allocates device memory,
+// and only qrr_get_last_device_status (the explicit sync point) synchronizes
+// with the host.
 #include <stdlib.h>
 #include <string.h>
 
@@ -515,6 +516,40 @@ qrr_status qrr_requantize_weights(const qrr_weight_desc* descs, int32_t count, i
     if (e != cudaSuccess) return QRR_ERR_CUDA;
   }
   return QRR_OK;
+}
+
+qrr_status qrr_get_last_device_status(int32_t* host_out, const int32_t* dev_status, void* stream) {
+  if (!host_out || !dev_status) return QRR_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(dev_status) & 3u) return QRR_ERR_MISALIGNED;
+  if (injected_cuda_fault()) return QRR_ERR_CUDA;
+  cudaStream_t s = as_stream(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, dev_status, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return QRR_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return QRR_ERR_CUDA;
+  *host_out = v;
+  return QRR_OK;
+}
+
+size_t qrr_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t r) {
+  switch (op) {
+    case QRR_OP_QUANTIZE_NVFP4: return qrr_quantize_nvfp4_workspace_bytes();
+    case QRR_OP_LINEAR_NVFP4_LORA: return qrr_linear_nvfp4_lora_workspace_bytes(M, N, K, r);
+    case QRR_OP_REQUANTIZE_WEIGHTS:
+      return M < 0 || M > INT32_MAX ? 0 : qrr_requantize_workspace_bytes(static_cast<int32_t>(M));
+    case QRR_OP_QUANTIZE_FP8:
+    case QRR_OP_GEMM_FP8: return 0;
+    default: return 0;
+  }
+}
+
+qrr_status qrr_wait_probe(int64_t limit_cycles, int32_t arrive, int32_t* dev_status, int64_t* cycles, void* stream) {
+  if (limit_cycles <= 0 || limit_cycles > kWaitLimitCycles || (arrive != 0 && arrive != 1)) return QRR_ERR_INVALID_ARG;
+  if (!dev_status) return QRR_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(dev_status) & 3u) || (reinterpret_cast<uintptr_t>(cycles) & 7u))
+    return QRR_ERR_MISALIGNED;
+  if (injected_cuda_fault()) return QRR_ERR_CUDA;
+  return from_cuda(launch_wait_probe(limit_cycles, arrive, dev_status, reinterpret_cast<long long*>(cycles),
+                                     as_stream(stream)));
 }
 
 qrr_status qrr_round_probe(const float* in, int64_t n, int32_t fmt, uint8_t* out, void* stream) {

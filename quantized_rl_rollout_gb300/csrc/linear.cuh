@@ -86,4 +86,9 @@ struct Fp8GemmArgs {
 
 cudaError_t launch_fp8_gemm_tc(const Fp8GemmArgs& a, int32_t* status, cudaStream_t stream);
 
+// ---- probe of the bounded-wait path (probe.cu) ----
+// limit: give-up time of the wait in SM clock cycles; arrive: complete the
+// barrier before waiting; cycles (nullable, device): the wait's duration.
+cudaError_t launch_wait_probe(long long limit, int arrive, int32_t* status, long long* cycles, cudaStream_t stream);
+
 }  // namespace qrr

@@ -74,8 +74,10 @@ constexpr uint32_t kWaitSliceNs = 1u << 20;  // about 1 ms per parked try
 
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false (and raises the abort flag) on timeout or when another wait of the
-// CTA already timed out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* status) {
+// CTA already timed out.  `limit` is the give-up time in SM clock cycles; the
+// pipelines use the default, a test of the timeout path passes a short one.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* status,
+                                          long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   // the SM cycle counter is cheap to read (a global timer read costs about a
   // microsecond, which would add that much latency to every hand-off)
@@ -84,10 +86,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 #ifdef QRR_WAIT_SPIN
     if (mbar_try_wait(bar, parity)) return true;
 #else
-    if (mbar_try_wait_sleep(bar, parity, kWaitSliceNs)) return true;
+    if (mbar_try_wait_sleep(bar, parity, limit < kWaitLimitCycles ? 1000u : kWaitSliceNs)) return true;
 #endif
     if (*abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       *abort = 1;
       flag(status, kDevTimeout);
       return false;

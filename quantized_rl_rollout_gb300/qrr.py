@@ -21,6 +21,12 @@ SCALE_POW2 = 1
 FORMAT_NVFP4 = 0
 FORMAT_FP8_W128 = 1
 DEV_NONFINITE = 0x1
+DEV_TIMEOUT = 0x2
+OP_QUANTIZE_NVFP4 = 0
+OP_LINEAR_NVFP4_LORA = 1
+OP_REQUANTIZE_WEIGHTS = 2
+OP_QUANTIZE_FP8 = 3
+OP_GEMM_FP8 = 4
 
 _c_i64 = ctypes.c_int64
 _c_i32 = ctypes.c_int32
@@ -66,6 +72,9 @@ SIGNATURES = {
     "qrr_requantize_weights": (ctypes.c_int, [ctypes.POINTER(WeightDesc), _c_i32, _c_i32, _c_i32, _c_p, _c_sz, _c_p,
                                               _c_p]),
     "qrr_round_probe": (ctypes.c_int, [_c_p, _c_i64, _c_i32, _c_p, _c_p]),
+    "qrr_get_last_device_status": (ctypes.c_int, [_c_p, _c_p, _c_p]),
+    "qrr_workspace_bytes": (_c_sz, [_c_i32, _c_i64, _c_i64, _c_i64, _c_i32]),
+    "qrr_wait_probe": (ctypes.c_int, [_c_i64, _c_i32, _c_p, _c_p, _c_p]),
 }
 
 _lib = None
@@ -273,3 +282,25 @@ def round_probe(values, fmt, out=None, stream=None):
     _check(lib().qrr_round_probe(_ptr(values), values.numel(), int(fmt), _ptr(out), _stream(stream)),
            "qrr_round_probe")
     return out
+
+
+def get_last_device_status(dev_status, stream=None) -> int:
+    """Host copy of the device status word once the stream's earlier work is done."""
+    _need(dev_status, torch.int32, "dev_status")
+    out = ctypes.c_int32(0)
+    _check(lib().qrr_get_last_device_status(ctypes.addressof(out), _ptr(dev_status), _stream(stream)),
+           "qrr_get_last_device_status")
+    return int(out.value)
+
+
+def workspace_bytes(op, M=0, N=0, K=0, r=0) -> int:
+    return int(lib().qrr_workspace_bytes(int(op), int(M), int(N), int(K), int(r)))
+
+
+def wait_probe(limit_cycles, arrive, dev_status, cycles=None, stream=None):
+    """Run the bounded-wait probe (see ``qrr_wait_probe``)."""
+    _need(dev_status, torch.int32, "dev_status")
+    if cycles is not None:
+        _need(cycles, torch.int64, "cycles")
+    _check(lib().qrr_wait_probe(int(limit_cycles), int(arrive), _ptr(dev_status), _ptr(cycles), _stream(stream)),
+           "qrr_wait_probe")

@@ -124,3 +124,27 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(qrr, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         qrr.lib()
+
+
+def test_status_sync_and_probe_validation(lib):
+    """Argument checks of the sync point and the wait probe (host side only)."""
+    assert lib.qrr_get_last_device_status(None, FAKE, None) == 1
+    assert lib.qrr_get_last_device_status(FAKE, None, None) == 1
+    assert lib.qrr_get_last_device_status(FAKE, FAKE + 2, None) == 3
+    assert lib.qrr_wait_probe(0, 0, FAKE, None, None) == 1  # no limit
+    assert lib.qrr_wait_probe(1 << 40, 0, FAKE, None, None) == 1  # above the pipelines' own limit
+    assert lib.qrr_wait_probe(1000, 2, FAKE, None, None) == 1
+    assert lib.qrr_wait_probe(1000, 0, None, None, None) == 1
+    assert lib.qrr_wait_probe(1000, 0, FAKE, FAKE + 4, None) == 3
+
+
+def test_generic_workspace_query_matches_per_call_queries(lib):
+    from quantized_rl_rollout_gb300 import qrr
+
+    assert lib.qrr_workspace_bytes(qrr.OP_QUANTIZE_NVFP4, 0, 0, 0, 0) == lib.qrr_quantize_nvfp4_workspace_bytes()
+    for m, n, k, r in [(1, 4096, 4096, 32), (64, 14336, 4096, 32), (4096, 1024, 4096, 0), (3, 128, 256, 8)]:
+        assert lib.qrr_workspace_bytes(qrr.OP_LINEAR_NVFP4_LORA, m, n, k, r) == \
+            lib.qrr_linear_nvfp4_lora_workspace_bytes(m, n, k, r)
+    assert lib.qrr_workspace_bytes(qrr.OP_REQUANTIZE_WEIGHTS, 7, 0, 0, 0) == lib.qrr_requantize_workspace_bytes(7)
+    assert lib.qrr_workspace_bytes(qrr.OP_GEMM_FP8, 4096, 4096, 4096, 0) == 0
+    assert lib.qrr_workspace_bytes(99, 1, 1, 1, 1) == 0
