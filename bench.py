@@ -12,6 +12,8 @@ tokens.  One step is one pass of the whole hot path over that layer set:
   prefill  the same linears at M = 4096 (activations with 1% x10 channels)
   fp8      FP8 path at M = 4096: 128x128 weight re-quantize (fp8_requant),
            activation 1x128 quantize (fp8_act_quant), blockwise-scaled GEMM
+           with fp32 scales (fp8_gemm, promotion) and with power-of-two scales
+           (fp8_gemm_pow2, native block-scaled MMA)
 
 Re-quantization follows a training step: the bf16 masters alternate between W
 and W' = bf16(W + N(0, 1e-4)) from step to step, so every step recalibrates
@@ -84,6 +86,7 @@ PHASE_KERNELS = {  # phase -> (kernel name prefix, template arguments as ncu pri
     "fp8_requant": ("fp8_w128_kernel", ""),
     "fp8_act_quant": ("fp8_a1x128_kernel", ""),
     "fp8_gemm": ("fp8_gemm_tc_kernel", ""),
+    "fp8_gemm_pow2": ("fp8_gemm_mx_kernel", ""),
 }
 
 
@@ -347,6 +350,9 @@ class Workload:
         self.f8a = [(torch.empty(PREFILL_TOKENS, l.k, dtype=torch.uint8, device=device),
                      torch.empty(PREFILL_TOKENS, l.k // 128, dtype=torch.float32, device=device)) for l in L]
         self.yf = [torch.empty(PREFILL_TOKENS, l.n, dtype=torch.bfloat16, device=device) for l in L]
+        # power-of-two-scale operands for the native block-scaled GEMM
+        self.f8w2 = [qrr.quantize_fp8_w128x128(w, qrr.SCALE_POW2) for w in self.W]
+        self.f8a2 = [qrr.quantize_fp8_a1x128(x, qrr.SCALE_POW2) for x in self.xp]
         self.gd = {m: self._group(self.xd[m], self.yd[m]) for m in DECODE_TOKENS}
         self.gp = self._group(self.xp, self.yp)
         ws = max([qrr.linear_nvfp4_lora_grouped_workspace_bytes(self.gd[m]) for m in DECODE_TOKENS] +
@@ -397,6 +403,13 @@ class Workload:
             self.q.gemm_fp8_blockwise(qa, sa, qw, sw, y=self.yf[i])
         return len(self.layers)
 
+    def fp8_gemm_pow2(self):
+        for i, _ in enumerate(self.layers):
+            qa, sa = self.f8a2[i]
+            qw, sw = self.f8w2[i]
+            self.q.gemm_fp8_blockwise(qa, sa, qw, sw, self.q.SCALE_POW2, y=self.yf[i])
+        return len(self.layers)
+
     def do_flush(self):
         self.flush.fill_(self.launches & 0xFF)
 
@@ -443,7 +456,8 @@ class Workload:
 
 # one step over the 8B-class workload; the 32B-class stack (another
 # configuration, ~85 GB resident) is timed after it, in a region of its own
-PHASES = ["requant", "decode_m1", "decode_m8", "decode_m64", "prefill", "fp8_requant", "fp8_act_quant", "fp8_gemm"]
+PHASES = ["requant", "decode_m1", "decode_m8", "decode_m64", "prefill", "fp8_requant", "fp8_act_quant", "fp8_gemm",
+          "fp8_gemm_pow2"]
 EXTRA_PHASES = ["requant32b", "decode32b"]
 
 
@@ -462,6 +476,8 @@ def run_phase(w, name):
         return w.decode32()
     if name == "requant32b":
         return w.requant32()
+    if name == "fp8_gemm_pow2":
+        return w.fp8_gemm_pow2()
     return w.fp8_gemm()
 
 
@@ -798,11 +814,12 @@ def main():
             breakdown[p] = hbm(ms, fp8_quant_bytes(L, PREFILL_TOKENS)[0])
         elif p == "fp8_act_quant":
             breakdown[p] = hbm(ms, fp8_quant_bytes(L, PREFILL_TOKENS)[1])
-        elif p == "fp8_gemm":
+        elif p in ("fp8_gemm", "fp8_gemm_pow2"):
             f = fp8_gemm_flops(L, PREFILL_TOKENS)
             breakdown[p] = {"ms": ms, "TFLOP/s": f / ms / 1e9, "frac_fp8": f / ms / 1e9 / fp8_peak,
                             "frac_fp8_spec": f / ms / 1e9 / SPEC_PEAKS["fp8_tflops"], "flops": f,
-                            "scale_mode": "fp32"}
+                            "scale_mode": "fp32 (promotion)" if p == "fp8_gemm" else
+                            "pow2 (native block-scaled MMA, UE8M0)"}
         elif p == "decode32b":
             c32 = configs.DECODE_32B
             breakdown[p] = hbm(ms, c32["depth"] * decode_bytes(configs.LAYERS_32B, c32["tokens"], c32["r"]))
@@ -822,7 +839,7 @@ def main():
         roof = {"bound": "hbm", "achieved": d["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": d["GB/s"] / peaks["hbm_gbs"], "peak_spec": SPEC_PEAKS["hbm_gbs"],
                 "frac_spec": d["GB/s"] / SPEC_PEAKS["hbm_gbs"]}
-    elif dom == "fp8_gemm":
+    elif dom in ("fp8_gemm", "fp8_gemm_pow2"):
         roof = {"bound": "tensor", "achieved": d["TFLOP/s"], "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": d["TFLOP/s"] / fp8_peak, "peak_spec": SPEC_PEAKS["fp8_tflops"],
                 "frac_spec": d["TFLOP/s"] / SPEC_PEAKS["fp8_tflops"]}

@@ -74,6 +74,9 @@ typedef enum qrr_status {
 /* Bits OR-ed into the optional device status word. */
 #define QRR_DEV_NONFINITE 0x1 /* a non-finite input value was seen */
 #define QRR_DEV_TIMEOUT 0x2   /* a pipeline wait gave up after its time limit; outputs unspecified */
+#define QRR_DEV_SCALE_RANGE 0x4 /* QRR_SCALE_POW2 GEMM: a scale was not a power of two (or zero), or the
+                                   exponents of one 128-K block spread wider than the native MMA's scale
+                                   bytes can carry exactly; outputs are then inexact */
 
 typedef enum qrr_scale_mode {
   QRR_SCALE_FP32 = 0, /* s = fp32(amax / 448); codes e4m3_rne(x / s) */
@@ -209,10 +212,18 @@ qrr_status qrr_quantize_fp8_a1x128(const void* x, int64_t M, int64_t K, uint8_t*
  *   y[m][n] = sum_kb sa[m][kb] * sw[n/128][kb] * sum_{k in kb} qa[m][k] * qw[n][k]
  *   qa uint8 [M][K], sa fp32 [M][K/128], qw uint8 [N][K], sw fp32 [ceil(N/128)][K/128]
  *   y  bf16 [M][N] (out); K a multiple of 128, N a multiple of 128.
- *   scale_mode  QRR_SCALE_POW2 promises that every scale is a power of two
- *               (or zero); the result is the same either way.
- * The E4M3 products are exact; each 128-wide block sum is fp32 before the
- * scales are applied. */
+ *   scale_mode  QRR_SCALE_FP32: any non-negative scales.  Each 128-wide block
+ *               sum is formed by the tensor core in fp32, then multiplied by
+ *               sa * sw and added in fp32 on the CUDA cores (promotion).
+ *               QRR_SCALE_POW2: every scale is a power of two or zero (as
+ *               QRR_SCALE_POW2 quantization writes them).  The product sa * sw
+ *               is then applied by the tensor core itself: tcgen05.mma
+ *               kind::mxf8f6f4 with one UE8M0 scale byte per 32 K of each row,
+ *               and the whole K loop accumulates in one fp32 accumulator.  A
+ *               scale that breaks the promise, or exponents within one 128-K
+ *               block of a 128 x 256 output tile spread over more than 254
+ *               binades, raise QRR_DEV_SCALE_RANGE (outputs then inexact).
+ * The E4M3 products are exact; sums are fp32. */
 qrr_status qrr_gemm_fp8_blockwise(const uint8_t* qa, const float* sa, const uint8_t* qw,
                                   const float* sw, int64_t M, int64_t N, int64_t K, void* y,
                                   int32_t scale_mode, int32_t* dev_status, void* stream);

@@ -458,6 +458,9 @@ qrr_status qrr_gemm_fp8_blockwise(const uint8_t* qa, const float* sa, const uint
   cudaStream_t s = as_stream(stream);
   if (K == 0) return from_cuda(cudaMemsetAsync(y, 0, static_cast<size_t>(M * N) * 2, s));
   Fp8GemmArgs a{qa, sa, qw, sw, y, M, N, K};
+  // power-of-two scales run on the native block-scaled MMA (UE8M0 scale
+  // bytes, no promotion); FP32 scales promote each 128-K block sum in fp32
+  if (scale_mode == QRR_SCALE_POW2) return from_cuda(launch_fp8_gemm_mx(a, dev_status, s));
   return from_cuda(launch_fp8_gemm_tc(a, dev_status, s));
 }
 

@@ -85,6 +85,8 @@ struct Fp8GemmArgs {
 };
 
 cudaError_t launch_fp8_gemm_tc(const Fp8GemmArgs& a, int32_t* status, cudaStream_t stream);
+// power-of-two scales on the native block-scaled MMA (gemm_fp8_mx.cu)
+cudaError_t launch_fp8_gemm_mx(const Fp8GemmArgs& a, int32_t* status, cudaStream_t stream);
 
 // ---- probe of the bounded-wait path (probe.cu) ----
 // limit: give-up time of the wait in SM clock cycles; arrive: complete the

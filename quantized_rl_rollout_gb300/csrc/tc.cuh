@@ -169,6 +169,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 32 lanes x 4 columns of 32-bit from registers.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+
 // 32 lanes x 8 columns of 32-bit from registers.
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile(
@@ -294,6 +301,35 @@ __device__ __forceinline__ void mma_fp8_ss(uint32_t d_tmem, uint64_t a_desc, uin
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// D[tmem] (+)= A[smem] x B[smem]^T, kind::mxf8f6f4 with block scaling
+// (E4M3 operands, one UE8M0 scale per 32 K of each row of A and of B): the
+// scale bytes come from tensor memory at `sfa` / `sfb`, the byte within each
+// 32-bit cell chosen by the scale ids of `idesc` (see make_idesc_mx).
+// Layout for M = 128, cta_group::1 (measured on GB300 with a probe of
+// encoded scale bytes): the scale of row m of A is lane m, column
+// sfa + m / 32; the scale of row n of B is column sfb + n / 32, lane
+// n % 32 of the lane quarter of the output row being formed, so every lane
+// quarter holds a copy.
+__device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with UE8M0 scales: E4M3 A and B,
+// both K-major, D fp32, shape M x N; a_sf / b_sf pick the scale byte (0..3)
+// of each 32-bit tensor-memory cell.  Bits: B scale id [4,6), A format
+// [7,10), B format [10,13), N >> 3 [17,23), scale type [23] (1 = UE8M0),
+// M >> 4 [24,29), A scale id [29,31).
+__host__ __device__ constexpr uint32_t make_idesc_mx(uint32_t m, uint32_t n, uint32_t a_sf, uint32_t b_sf) {
+  return (b_sf << 4) | (kFmtE4M3 << 7) | (kFmtE4M3 << 10) | ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24) |
+         (a_sf << 29);
 }
 
 // Arrive on `bar` once every MMA this thread issued so far has completed.

@@ -22,6 +22,7 @@ FORMAT_NVFP4 = 0
 FORMAT_FP8_W128 = 1
 DEV_NONFINITE = 0x1
 DEV_TIMEOUT = 0x2
+DEV_SCALE_RANGE = 0x4
 OP_QUANTIZE_NVFP4 = 0
 OP_LINEAR_NVFP4_LORA = 1
 OP_REQUANTIZE_WEIGHTS = 2
