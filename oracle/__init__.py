@@ -18,7 +18,9 @@ written in numpy:
   activation row blocks; FP32 or power-of-two scales) and the blockwise-scaled
   GEMM in float64;
 * ``requant``  -- re-quantization of every weight of a layer set after a
-  training step.
+  training step;
+* ``rollout_is`` -- token log-probabilities from a row of logits and the
+  token-level importance-sampling weights between rollout and trainer.
 
 Sources.  The pages describe QeRL ("QeRL: Beyond Efficiency -- Quantization-
 enhanced Reinforcement Learning for LLMs", abstract; "NVIDIA and MIT Collaborate
@@ -35,4 +37,4 @@ float32 arithmetic (correctly rounded, subnormals kept) produces it; sums of
 products are formed in float64.
 """
 
-from . import formats, nvfp4, fp8, linear, requant  # noqa: F401
+from . import formats, nvfp4, fp8, linear, requant, rollout_is  # noqa: F401
