@@ -14,6 +14,8 @@ tokens.  One step is one pass of the whole hot path over that layer set:
            activation 1x128 quantize (fp8_act_quant), blockwise-scaled GEMM
            with fp32 scales (fp8_gemm, promotion) and with power-of-two scales
            (fp8_gemm_pow2, native block-scaled MMA)
+  is       token log-probabilities and importance-sampling weights of 4096
+           tokens over a 128256-entry vocabulary (rollout_is)
 
 Re-quantization follows a training step: the bf16 masters alternate between W
 and W' = bf16(W + N(0, 1e-4)) from step to step, so every step recalibrates
@@ -68,6 +70,7 @@ DECODE_TOKENS = (1, 8, 64)
 PREFILL_TOKENS = 4096
 R = 32
 ALPHA = 2.0 * R
+IS_TOKENS, IS_VOCAB, IS_CAP = 4096, 128256, 5.0  # importance-sampling phase: tokens x 8B-class vocabulary
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 # GB300's published dense figures (per GPU), reported beside the measured peaks
 SPEC_PEAKS = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0, "fp8_tflops": 4500.0}
@@ -87,6 +90,7 @@ PHASE_KERNELS = {  # phase -> (kernel name prefix, template arguments as ncu pri
     "fp8_act_quant": ("fp8_a1x128_kernel", ""),
     "fp8_gemm": ("fp8_gemm_tc_kernel", ""),
     "fp8_gemm_pow2": ("fp8_gemm_mx_kernel", ""),
+    "rollout_is": ("token_logprob_is_kernel", ""),
 }
 
 
@@ -350,6 +354,12 @@ class Workload:
         self.f8a = [(torch.empty(PREFILL_TOKENS, l.k, dtype=torch.uint8, device=device),
                      torch.empty(PREFILL_TOKENS, l.k // 128, dtype=torch.float32, device=device)) for l in L]
         self.yf = [torch.empty(PREFILL_TOKENS, l.n, dtype=torch.bfloat16, device=device) for l in L]
+        # token log-probabilities / importance weights over an 8B-class vocabulary
+        self.lg = inputs.logits(IS_TOKENS, IS_VOCAB, inputs.derive_seed(seed, "is", "logits"), device=device)
+        self.tok = inputs.sampled_tokens(self.lg, inputs.derive_seed(seed, "is", "tokens"))
+        self.rlp = inputs.jitter(torch.full((IS_TOKENS,), -2.0, device=device), inputs.derive_seed(seed, "is", "r"), 1.0)
+        self.lp = torch.empty(IS_TOKENS, dtype=torch.float32, device=device)
+        self.iw = torch.empty(IS_TOKENS, dtype=torch.float32, device=device)
         # power-of-two-scale operands for the native block-scaled GEMM
         self.f8w2 = [qrr.quantize_fp8_w128x128(w, qrr.SCALE_POW2) for w in self.W]
         self.f8a2 = [qrr.quantize_fp8_a1x128(x, qrr.SCALE_POW2) for x in self.xp]
@@ -410,6 +420,10 @@ class Workload:
             self.q.gemm_fp8_blockwise(qa, sa, qw, sw, self.q.SCALE_POW2, y=self.yf[i])
         return len(self.layers)
 
+    def rollout_is(self):
+        self.q.token_logprobs_is(self.lg, self.tok, self.rlp, IS_CAP, logp=self.lp, w=self.iw)
+        return 1
+
     def do_flush(self):
         self.flush.fill_(self.launches & 0xFF)
 
@@ -457,7 +471,7 @@ class Workload:
 # one step over the 8B-class workload; the 32B-class stack (another
 # configuration, ~85 GB resident) is timed after it, in a region of its own
 PHASES = ["requant", "decode_m1", "decode_m8", "decode_m64", "prefill", "fp8_requant", "fp8_act_quant", "fp8_gemm",
-          "fp8_gemm_pow2"]
+          "fp8_gemm_pow2", "rollout_is"]
 EXTRA_PHASES = ["requant32b", "decode32b"]
 
 
@@ -478,6 +492,8 @@ def run_phase(w, name):
         return w.requant32()
     if name == "fp8_gemm_pow2":
         return w.fp8_gemm_pow2()
+    if name == "rollout_is":
+        return w.rollout_is()
     return w.fp8_gemm()
 
 
@@ -820,6 +836,9 @@ def main():
                             "frac_fp8_spec": f / ms / 1e9 / SPEC_PEAKS["fp8_tflops"], "flops": f,
                             "scale_mode": "fp32 (promotion)" if p == "fp8_gemm" else
                             "pow2 (native block-scaled MMA, UE8M0)"}
+        elif p == "rollout_is":
+            breakdown[p] = hbm(ms, IS_TOKENS * IS_VOCAB * 2 + IS_TOKENS * 16)
+            breakdown[p]["workload"] = f"{IS_TOKENS} tokens x {IS_VOCAB} vocabulary, bf16 logits"
         elif p == "decode32b":
             c32 = configs.DECODE_32B
             breakdown[p] = hbm(ms, c32["depth"] * decode_bytes(configs.LAYERS_32B, c32["tokens"], c32["r"]))

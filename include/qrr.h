@@ -77,6 +77,7 @@ typedef enum qrr_status {
 #define QRR_DEV_SCALE_RANGE 0x4 /* QRR_SCALE_POW2 GEMM: a scale was not a power of two (or zero), or the
                                    exponents of one 128-K block spread wider than the native MMA's scale
                                    bytes can carry exactly; outputs are then inexact */
+#define QRR_DEV_BAD_INDEX 0x8   /* an index read on the device (a token id) was out of range */
 
 typedef enum qrr_scale_mode {
   QRR_SCALE_FP32 = 0, /* s = fp32(amax / 448); codes e4m3_rne(x / s) */
@@ -253,6 +254,28 @@ size_t qrr_requantize_workspace_bytes(int32_t count);
 qrr_status qrr_requantize_weights(const qrr_weight_desc* descs, int32_t count, int32_t format,
                                   int32_t scale_mode, void* workspace, size_t workspace_bytes,
                                   int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Token log-probabilities and token-level importance-sampling weights
+ * ("NVIDIA NeMo RL behaalt 48% ...", the paragraph on importance sampling in
+ * "Waarom dit belangrijk is voor AI-economie": the shift between the
+ * generation engine's and the trainer's token distributions is corrected
+ * token by token):
+ *   logp[t] = logits[t][tok[t]] - log(sum_v exp(logits[t][v]))
+ *   w[t]    = min(exp(logp[t] - rollout_logp[t]), cap)   (cap <= 0: no cap)
+ *   logits        bf16 [T][V] row-major (V >= 1); read once
+ *   tokens        int32 [T]; a negative id marks padding (logp = w = 0); an id
+ *                 >= V also gives 0 and raises QRR_DEV_BAD_INDEX
+ *   rollout_logp  fp32 [T] (the rollout engine's log-probabilities) or NULL
+ *   logp          fp32 [T] (out)
+ *   w             fp32 [T] (out; only written when rollout_logp is given)
+ * The sums are fp32; exp and log are the hardware base-2 approximations
+ * (relative error about 2^-22).  A NaN or +inf logit raises
+ * QRR_DEV_NONFINITE.  Pointers 16-byte aligned (logits; 4-byte for the
+ * others); V % 8 == 0 takes 16-byte loads, any other V element loads. */
+qrr_status qrr_token_logprobs_is(const void* logits, int64_t T, int64_t V, const int32_t* tokens,
+                                 const float* rollout_logp, float cap, float* logp, float* w, int32_t* dev_status,
+                                 void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* The explicit sync point for device-detected conditions: copies the status

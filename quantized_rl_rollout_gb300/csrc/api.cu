@@ -521,6 +521,18 @@ qrr_status qrr_requantize_weights(const qrr_weight_desc* descs, int32_t count, i
   return QRR_OK;
 }
 
+qrr_status qrr_token_logprobs_is(const void* logits, int64_t T, int64_t V, const int32_t* tokens,
+                                 const float* rollout_logp, float cap, float* logp, float* w, int32_t* dev_status,
+                                 void* stream) {
+  if (T < 0 || V < 1) return QRR_ERR_INVALID_ARG;
+  if (T > 0 && (!logits || !tokens || !logp || (rollout_logp && !w))) return QRR_ERR_INVALID_ARG;
+  auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  if (!aligned16(logits) || !a4(tokens) || !a4(logp) || !a4(rollout_logp) || !a4(w)) return QRR_ERR_MISALIGNED;
+  if (injected_cuda_fault()) return QRR_ERR_CUDA;
+  return from_cuda(
+      launch_token_logprob_is(logits, T, V, tokens, rollout_logp, cap, logp, w, dev_status, as_stream(stream)));
+}
+
 qrr_status qrr_get_last_device_status(int32_t* host_out, const int32_t* dev_status, void* stream) {
   if (!host_out || !dev_status) return QRR_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(dev_status) & 3u) return QRR_ERR_MISALIGNED;

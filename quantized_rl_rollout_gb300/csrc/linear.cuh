@@ -88,6 +88,11 @@ cudaError_t launch_fp8_gemm_tc(const Fp8GemmArgs& a, int32_t* status, cudaStream
 // power-of-two scales on the native block-scaled MMA (gemm_fp8_mx.cu)
 cudaError_t launch_fp8_gemm_mx(const Fp8GemmArgs& a, int32_t* status, cudaStream_t stream);
 
+// ---- token log-probabilities and importance-sampling weights (rollout_is.cu) ----
+cudaError_t launch_token_logprob_is(const void* logits, int64_t T, int64_t V, const int32_t* tokens,
+                                    const float* rollout_logp, float cap, float* logp, float* w, int32_t* status,
+                                    cudaStream_t stream);
+
 // ---- probe of the bounded-wait path (probe.cu) ----
 // limit: give-up time of the wait in SM clock cycles; arrive: complete the
 // barrier before waiting; cycles (nullable, device): the wait's duration.

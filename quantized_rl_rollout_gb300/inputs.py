@@ -14,7 +14,10 @@ Recipe (workload shapes follow an 8B-class and a 32B-class decoder layer set):
 * prefill / FP8 activations: ``N(0, 1)`` with 1% of the K channels (columns)
   multiplied by 10, in bf16;
 * LoRA factors: A [r, K] and B [N, r] ``N(0, 0.01)`` in bf16, alpha = 2 r;
-* weight update after a training step: ``W' = bf16(W + N(0, 1e-4))``.
+* weight update after a training step: ``W' = bf16(W + N(0, 1e-4))``;
+* logits of a vocabulary row: ``N(0, 2)`` in bf16; the sampled token of a row
+  by the Gumbel-max rule; the rollout engine's log-probabilities as the
+  trainer's plus ``N(0, 0.02)`` (a second engine's numbers).
 
 Every tensor has its own stream: ``torch.Generator`` seeded with
 ``derive_seed(seed, *labels)``.  Draws are made on the device the tensor is
@@ -72,6 +75,26 @@ def lora(r: int, k: int, n: int, seed: int, device="cpu", std: float = 0.01):
     a = (torch.randn(r, k, generator=g, device=device, dtype=torch.float32) * std).to(torch.bfloat16)
     b = (torch.randn(n, r, generator=g, device=device, dtype=torch.float32) * std).to(torch.bfloat16)
     return a, b, float(2 * r)
+
+
+def logits(t: int, v: int, seed: int, device="cpu", std: float = 2.0) -> torch.Tensor:
+    """bf16 [t, v] logits ~N(0, std)."""
+    g = _gen(device, seed)
+    return (torch.randn(t, v, generator=g, device=device, dtype=torch.float32) * std).to(torch.bfloat16)
+
+
+def sampled_tokens(lg: torch.Tensor, seed: int) -> torch.Tensor:
+    """int32 [t]: one token per row drawn from softmax(row) by the Gumbel-max
+    rule (the token a sampling rollout would emit)."""
+    g = _gen(lg.device, seed)
+    u = torch.rand(lg.shape, generator=g, device=lg.device, dtype=torch.float32).clamp_(1e-20, 1.0)
+    return (lg.float() - torch.log(-torch.log(u))).argmax(dim=-1).to(torch.int32)
+
+
+def jitter(x: torch.Tensor, seed: int, std: float) -> torch.Tensor:
+    """x + N(0, std) in fp32 (a second engine's slightly different numbers)."""
+    g = _gen(x.device, seed)
+    return x.float() + torch.randn(x.shape, generator=g, device=x.device, dtype=torch.float32) * std
 
 
 def updated(w: torch.Tensor, seed: int, std: float = 1e-4) -> torch.Tensor:

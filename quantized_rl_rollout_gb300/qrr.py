@@ -23,6 +23,7 @@ FORMAT_FP8_W128 = 1
 DEV_NONFINITE = 0x1
 DEV_TIMEOUT = 0x2
 DEV_SCALE_RANGE = 0x4
+DEV_BAD_INDEX = 0x8
 OP_QUANTIZE_NVFP4 = 0
 OP_LINEAR_NVFP4_LORA = 1
 OP_REQUANTIZE_WEIGHTS = 2
@@ -74,6 +75,8 @@ SIGNATURES = {
                                               _c_p]),
     "qrr_round_probe": (ctypes.c_int, [_c_p, _c_i64, _c_i32, _c_p, _c_p]),
     "qrr_get_last_device_status": (ctypes.c_int, [_c_p, _c_p, _c_p]),
+    "qrr_token_logprobs_is": (ctypes.c_int, [_c_p, _c_i64, _c_i64, _c_p, _c_p, ctypes.c_float, _c_p, _c_p, _c_p,
+                                             _c_p]),
     "qrr_workspace_bytes": (_c_sz, [_c_i32, _c_i64, _c_i64, _c_i64, _c_i32]),
     "qrr_wait_probe": (ctypes.c_int, [_c_i64, _c_i32, _c_p, _c_p, _c_p]),
 }
@@ -305,3 +308,20 @@ def wait_probe(limit_cycles, arrive, dev_status, cycles=None, stream=None):
         _need(cycles, torch.int64, "cycles")
     _check(lib().qrr_wait_probe(int(limit_cycles), int(arrive), _ptr(dev_status), _ptr(cycles), _stream(stream)),
            "qrr_wait_probe")
+
+
+def token_logprobs_is(logits, tokens, rollout_logp=None, cap=0.0, logp=None, w=None, dev_status=None, stream=None):
+    """Token log-probabilities (and, given the rollout's, importance weights).
+
+    Returns ``logp`` or ``(logp, w)`` when ``rollout_logp`` is given."""
+    _need(logits, torch.bfloat16, "logits")
+    _need(tokens, torch.int32, "tokens")
+    t, v = logits.shape
+    logp = torch.empty(t, dtype=torch.float32, device=logits.device) if logp is None else logp
+    if rollout_logp is not None:
+        _need(rollout_logp, torch.float32, "rollout_logp")
+        w = torch.empty(t, dtype=torch.float32, device=logits.device) if w is None else w
+    _check(lib().qrr_token_logprobs_is(_ptr(logits), t, v, _ptr(tokens), _ptr(rollout_logp), float(cap), _ptr(logp),
+                                       _ptr(w) if rollout_logp is not None else None, _ptr(dev_status),
+                                       _stream(stream)), "qrr_token_logprobs_is")
+    return logp if rollout_logp is None else (logp, w)
