@@ -20,7 +20,9 @@ written in numpy:
 * ``requant``  -- re-quantization of every weight of a layer set after a
   training step;
 * ``rollout_is`` -- token log-probabilities from a row of logits and the
-  token-level importance-sampling weights between rollout and trainer.
+  token-level importance-sampling weights between rollout and trainer;
+* ``aqn``      -- adaptive quantization noise: counter-based noise added to the
+  masters before re-quantization, with its schedule.
 
 Sources.  The pages describe QeRL ("QeRL: Beyond Efficiency -- Quantization-
 enhanced Reinforcement Learning for LLMs", abstract; "NVIDIA and MIT Collaborate
@@ -37,4 +39,4 @@ float32 arithmetic (correctly rounded, subnormals kept) produces it; sums of
 products are formed in float64.
 """
 
-from . import formats, nvfp4, fp8, linear, requant, rollout_is  # noqa: F401
+from . import formats, nvfp4, fp8, linear, requant, rollout_is, aqn  # noqa: F401
