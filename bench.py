@@ -6,7 +6,9 @@ Workload (the decode configuration the headline metric is quoted on): an
 outliers -- in NVFP4 with LoRA r = 32 (alpha = 64), decoding 1, 8 and 64
 tokens.  One step is one pass of the whole hot path over that layer set:
 
-  requant  re-quantize all 7 bf16 weights to NVFP4 (absmax sweep + encode)
+  requant  re-quantize all 7 bf16 weights to NVFP4 (absmax sweep + encode);
+           requant_aqn the same with adaptive quantization noise added to the
+           masters (Philox noise regenerated in both sweeps)
   decode   W4A16 + LoRA linear of all 7 layers at M = 1, 8 and 64 (one
            grouped call per token count)
   prefill  the same linears at M = 4096 (activations with 1% x10 channels)
@@ -86,6 +88,7 @@ PHASE_KERNELS = {  # phase -> (kernel name prefix, template arguments as ncu pri
     "decode_m8": ("w4a16_tc_kernel", "<16, 256, 1, 3, 0>"),
     "decode_m64": ("w4a16_tc_kernel", "<64, 256, 1, 3, 0>"),
     "requant": ("nvfp4_encode_kernel", ""),
+    "requant_aqn": ("nvfp4_encode_kernel", ""),
     "fp8_requant": ("fp8_w128_kernel", ""),
     "fp8_act_quant": ("fp8_a1x128_kernel", ""),
     "fp8_gemm": ("fp8_gemm_tc_kernel", ""),
@@ -420,6 +423,13 @@ class Workload:
             self.q.gemm_fp8_blockwise(qa, sa, qw, sw, self.q.SCALE_POW2, y=self.yf[i])
         return len(self.layers)
 
+    def requant_aqn(self):
+        # step-dependent noise strength of a geometric schedule over 100 steps
+        self.aqn_step = getattr(self, "aqn_step", 0) + 1
+        sigma = self.q.aqn_sigma(self.aqn_step % 100, 100, 1e-2, 5e-4)
+        self.q.requantize_weights_aqn(self.masters, self.nv, sigma, 0x5EED, self.aqn_step, workspace=self.rq_ws)
+        return 2
+
     def rollout_is(self):
         self.q.token_logprobs_is(self.lg, self.tok, self.rlp, IS_CAP, logp=self.lp, w=self.iw)
         return 1
@@ -470,8 +480,8 @@ class Workload:
 
 # one step over the 8B-class workload; the 32B-class stack (another
 # configuration, ~85 GB resident) is timed after it, in a region of its own
-PHASES = ["requant", "decode_m1", "decode_m8", "decode_m64", "prefill", "fp8_requant", "fp8_act_quant", "fp8_gemm",
-          "fp8_gemm_pow2", "rollout_is"]
+PHASES = ["requant", "requant_aqn", "decode_m1", "decode_m8", "decode_m64", "prefill", "fp8_requant", "fp8_act_quant",
+          "fp8_gemm", "fp8_gemm_pow2", "rollout_is"]
 EXTRA_PHASES = ["requant32b", "decode32b"]
 
 
@@ -494,6 +504,8 @@ def run_phase(w, name):
         return w.fp8_gemm_pow2()
     if name == "rollout_is":
         return w.rollout_is()
+    if name == "requant_aqn":
+        return w.requant_aqn()
     return w.fp8_gemm()
 
 
@@ -819,7 +831,7 @@ def main():
             dec_bytes += b
             dec_ms += ms
             breakdown[p] = hbm(ms, b)
-        elif p == "requant":
+        elif p in ("requant", "requant_aqn"):
             breakdown[p] = hbm(ms, requant_nvfp4_bytes(L))
         elif p == "prefill":
             f = linear_flops(L, PREFILL_TOKENS, R)

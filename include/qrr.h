@@ -317,6 +317,40 @@ size_t qrr_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t 
 qrr_status qrr_wait_probe(int64_t limit_cycles, int32_t arrive, int32_t* dev_status, int64_t* cycles, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Re-quantization with adaptive quantization noise ("QeRL: Beyond Efficiency
+ * -- Quantization-enhanced Reinforcement Learning for LLMs", Abstract: noise
+ * in the quantized policy raises its entropy and helps exploration; the
+ * Adaptive Quantization Noise mechanism adjusts it during training).  The
+ * page gives no formula; this library's reading: each master is made noisy
+ * before it is quantized,
+ *   W'[e] = bf16_rn(fp32(W[e]) + fp32(sigma * z[e]))
+ * and W' is quantized exactly as qrr_requantize_weights would (same formats,
+ * scale modes, workspace, grouping).  z[e] is a standardized sum of four
+ * uniforms (mean 0, variance 1, within +-2 sqrt 3) drawn from Philox4x32-10
+ * (Salmon et al., SC'11) at counter (e / 2 low word, e / 2 high word,
+ * descriptor index j, step), key (seed low word, seed high word): the four
+ * 16-bit halves k_i of words r0, r1 (even e) or r2, r3 (odd e) give
+ * z = fp32((k1 + k2 + k3 + k4 - 131070) / 65536) * fp32(sqrt 3).  e is the
+ * element's row-major index in its tensor.  Every step is integer or one
+ * correctly rounded fp32 operation, so the result is reproducible bit for bit.
+ * The noise is regenerated from its counter in every pass: nothing noisy is
+ * stored.  sigma >= 0 and finite (0: plain re-quantization), step >= 0. */
+qrr_status qrr_requantize_weights_aqn(const qrr_weight_desc* descs, int32_t count, int32_t format,
+                                      int32_t scale_mode, float sigma, uint64_t seed, int32_t step, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* The noise strength of a training step under a geometric schedule from
+ * sigma_start (step 0) to sigma_end (step steps - 1 and later):
+ *   sigma_start * (sigma_end / sigma_start) ^ (step / (steps - 1)),
+ * computed in double precision and rounded to fp32.  Host only. */
+float qrr_aqn_sigma(int32_t step, int32_t steps, double sigma_start, double sigma_end);
+
+/* Conformance probe of the noise: z of elements start .. start + n - 1 of
+ * descriptor index `tensor` at `step` with `seed`, written to out fp32 [n]. */
+qrr_status qrr_aqn_noise_probe(float* out, int64_t n, int64_t start, uint64_t seed, int32_t tensor, int32_t step,
+                               void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Conformance probe: the library's own float32 -> E2M1 / E4M3 rounding
  * primitive applied to n values (fmt 0 = E2M1 code in the low 4 bits,
  * fmt 1 = E4M3 byte).  in fp32 [n], out uint8 [n]; n >= 0.  The quantizers

@@ -2,6 +2,7 @@
 // carving and dispatch to the kernels.  Nothing here allocates device memory,
 // and only qrr_get_last_device_status (the explicit sync point) synchronizes
 // with the host.
+#include <math.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -358,7 +359,7 @@ qrr_status qrr_quantize_nvfp4(const void* W, int64_t N, int64_t K, uint8_t* code
   if (injected_cuda_fault()) return QRR_ERR_CUDA;
   Nvfp4Batch batch{};
   batch.count = 1;
-  batch.job[0] = Nvfp4Job{static_cast<const uint16_t*>(W), codes, scales, tensor_scale, N, K, 0, 0};
+  batch.job[0] = Nvfp4Job{static_cast<const uint16_t*>(W), codes, scales, tensor_scale, N, K, 0, 0, 0u};
   batch.amax_bits = static_cast<uint32_t*>(workspace);
   batch.status = dev_status;
   return from_cuda(launch_nvfp4(batch, as_stream(stream)));
@@ -428,7 +429,7 @@ qrr_status qrr_quantize_fp8_w128x128(const void* W, int64_t N, int64_t K, uint8_
   batch.count = 1;
   batch.mode = scale_mode;
   batch.status = dev_status;
-  batch.job[0] = Fp8WJob{static_cast<const uint16_t*>(W), q, scales, N, K, 0};
+  batch.job[0] = Fp8WJob{static_cast<const uint16_t*>(W), q, scales, N, K, 0, 0u};
   return from_cuda(launch_fp8_w128(batch, as_stream(stream)));
 }
 
@@ -464,8 +465,9 @@ qrr_status qrr_gemm_fp8_blockwise(const uint8_t* qa, const float* sa, const uint
   return from_cuda(launch_fp8_gemm_tc(a, dev_status, s));
 }
 
-qrr_status qrr_requantize_weights(const qrr_weight_desc* descs, int32_t count, int32_t format, int32_t scale_mode,
-                                  void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+static qrr_status requantize(const qrr_weight_desc* descs, int32_t count, int32_t format, int32_t scale_mode,
+                             const AqnParams& aqn, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                             void* stream) {
   if (count < 0 || (count > 0 && !descs)) return QRR_ERR_INVALID_ARG;
   if (format != QRR_FORMAT_NVFP4 && format != QRR_FORMAT_FP8_W128) return QRR_ERR_INVALID_ARG;
   if (format == QRR_FORMAT_FP8_W128 && !is_fp8_mode(scale_mode)) return QRR_ERR_INVALID_ARG;
@@ -499,10 +501,11 @@ qrr_status qrr_requantize_weights(const qrr_weight_desc* descs, int32_t count, i
       batch.count = n;
       batch.amax_bits = static_cast<uint32_t*>(workspace);
       batch.status = dev_status;
+      batch.aqn = aqn;
       for (int i = 0; i < n; ++i) {
         const qrr_weight_desc& d = descs[g + i];
         batch.job[i] = Nvfp4Job{static_cast<const uint16_t*>(d.W), d.codes, static_cast<uint8_t*>(d.scales),
-                                d.tensor_scale, d.N, d.K, 0, 0};
+                                d.tensor_scale, d.N, d.K, 0, 0, static_cast<uint32_t>(g + i)};
       }
       e = launch_nvfp4(batch, s);
     } else {
@@ -510,9 +513,11 @@ qrr_status qrr_requantize_weights(const qrr_weight_desc* descs, int32_t count, i
       batch.count = n;
       batch.mode = scale_mode;
       batch.status = dev_status;
+      batch.aqn = aqn;
       for (int i = 0; i < n; ++i) {
         const qrr_weight_desc& d = descs[g + i];
-        batch.job[i] = Fp8WJob{static_cast<const uint16_t*>(d.W), d.codes, static_cast<float*>(d.scales), d.N, d.K, 0};
+        batch.job[i] = Fp8WJob{static_cast<const uint16_t*>(d.W), d.codes, static_cast<float*>(d.scales), d.N, d.K, 0,
+                               static_cast<uint32_t>(g + i)};
       }
       e = launch_fp8_w128(batch, s);
     }
@@ -565,6 +570,35 @@ qrr_status qrr_wait_probe(int64_t limit_cycles, int32_t arrive, int32_t* dev_sta
   if (injected_cuda_fault()) return QRR_ERR_CUDA;
   return from_cuda(launch_wait_probe(limit_cycles, arrive, dev_status, reinterpret_cast<long long*>(cycles),
                                      as_stream(stream)));
+}
+
+qrr_status qrr_requantize_weights(const qrr_weight_desc* descs, int32_t count, int32_t format, int32_t scale_mode,
+                                  void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return requantize(descs, count, format, scale_mode, AqnParams{0.0f, 0u, 0ull}, workspace, workspace_bytes,
+                    dev_status, stream);
+}
+
+qrr_status qrr_requantize_weights_aqn(const qrr_weight_desc* descs, int32_t count, int32_t format,
+                                      int32_t scale_mode, float sigma, uint64_t seed, int32_t step, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (!(sigma >= 0.0f) || sigma == INFINITY || step < 0) return QRR_ERR_INVALID_ARG;
+  return requantize(descs, count, format, scale_mode, AqnParams{sigma, static_cast<uint32_t>(step), seed}, workspace,
+                    workspace_bytes, dev_status, stream);
+}
+
+float qrr_aqn_sigma(int32_t step, int32_t steps, double sigma_start, double sigma_end) {
+  if (steps <= 1 || step >= steps - 1) return static_cast<float>(sigma_end);
+  if (step <= 0) return static_cast<float>(sigma_start);
+  return static_cast<float>(sigma_start * pow(sigma_end / sigma_start, static_cast<double>(step) / (steps - 1)));
+}
+
+qrr_status qrr_aqn_noise_probe(float* out, int64_t n, int64_t start, uint64_t seed, int32_t tensor, int32_t step,
+                               void* stream) {
+  if (n < 0 || start < 0 || tensor < 0 || step < 0 || (n > 0 && !out)) return QRR_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(out) & 3u) return QRR_ERR_MISALIGNED;
+  if (injected_cuda_fault()) return QRR_ERR_CUDA;
+  return from_cuda(launch_aqn_noise_probe(out, n, start, static_cast<uint32_t>(tensor),
+                                          AqnParams{1.0f, static_cast<uint32_t>(step), seed}, as_stream(stream)));
 }
 
 qrr_status qrr_round_probe(const float* in, int64_t n, int32_t fmt, uint8_t* out, void* stream) {

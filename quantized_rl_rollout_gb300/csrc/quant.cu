@@ -60,6 +60,7 @@ __device__ __forceinline__ bool stream_issue(StreamRing& r, uint8_t* ring, int64
 // patterns; `amax_bits[j]` must be zero before the launch.  Each warp keeps a
 // running max over its chunks and publishes it with one atomic per tensor it
 // leaves (same-address atomics serialize in L2).
+template <bool NOISE>
 __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __grid_constant__ Nvfp4Batch batch) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* ring = smem_raw;
@@ -67,12 +68,15 @@ __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __grid_constant__
   __shared__ int64_t s_first[kMaxJobs + 1];
   __shared__ int64_t s_bytes[kMaxJobs];
   __shared__ const uint8_t* s_src[kMaxJobs];
+  __shared__ uint32_t s_tensor[kMaxJobs];
   const int count = batch.count;
   const int64_t chunks = batch.total_amax_chunks;
+  const AqnParams aqn = batch.aqn;
   for (int j = threadIdx.x; j < count; j += blockDim.x) {
     s_first[j] = batch.job[j].first_amax_chunk;
     s_bytes[j] = batch.job[j].N * batch.job[j].K * 2;
     s_src[j] = reinterpret_cast<const uint8_t*>(batch.job[j].W);
+    s_tensor[j] = batch.job[j].tensor;
   }
   if (threadIdx.x == 0) {
     s_first[count] = chunks;
@@ -121,10 +125,15 @@ __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __grid_constant__
     const int64_t left = s_bytes[j] - (c - s_first[j]) * kStreamChunk;
     const int nvec = static_cast<int>((left < kStreamChunk ? left : kStreamChunk) / 16);
     const uint4* v = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * kStreamChunk);
+    const int64_t e0 = (c - s_first[j]) * (kStreamChunk / 2);  // first element of the chunk
 #pragma unroll
     for (int u = 0; u < kStreamChunk / 16 / 256; ++u) {
       const int e = u * 256 + threadIdx.x;
-      if (e < nvec) run = max(run, absmax_bits8(v[e]));
+      if (e < nvec) {
+        uint4 x = v[e];
+        if constexpr (NOISE) x = aqn_noisy8(x, e0 + 8 * e, s_tensor[j], aqn);
+        run = max(run, absmax_bits8(x));
+      }
     }
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&r.empty[s]);
@@ -144,6 +153,7 @@ __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __grid_constant__
 // each (the encode is arithmetic-heavy: more warps hide its latency).  The
 // chunks run in the reverse of the absmax pass's order, so the first ones
 // read what that pass read last, while it is still in L2.
+template <bool NOISE>
 __global__ void __launch_bounds__(512, 3) nvfp4_encode_kernel(const __grid_constant__ Nvfp4Batch batch) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* ring = smem_raw;
@@ -156,9 +166,12 @@ __global__ void __launch_bounds__(512, 3) nvfp4_encode_kernel(const __grid_const
   __shared__ float* s_ts[kMaxJobs];
   __shared__ float s_st[kMaxJobs];
   __shared__ SharedDivisor s_six[kMaxJobs];  // the per-tensor divisor 6 s_t of every block's absmax
+  __shared__ uint32_t s_tensor[kMaxJobs];
   const int count = batch.count;
   const int64_t chunks = batch.total_encode_chunks;
+  const AqnParams aqn = batch.aqn;
   for (int j = threadIdx.x; j < count; j += blockDim.x) {
+    s_tensor[j] = batch.job[j].tensor;
     s_first[j] = batch.job[j].first_encode_chunk;
     s_bytes[j] = batch.job[j].N * batch.job[j].K * 2;
     s_src[j] = reinterpret_cast<const uint8_t*>(batch.job[j].W);
@@ -204,11 +217,15 @@ __global__ void __launch_bounds__(512, 3) nvfp4_encode_kernel(const __grid_const
     if (b0 == 0 && threadIdx.x == 0) *s_ts[j] = s_t;
     if (!mbar_wait(&r.full[s], (i / kEncodeStages) & 1, &r.abort, status)) break;
     const uint4* v = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * kStreamChunk);
-    const uint4 x0 = v[2 * threadIdx.x], x1 = v[2 * threadIdx.x + 1];
+    uint4 x0 = v[2 * threadIdx.x], x1 = v[2 * threadIdx.x + 1];
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&r.empty[s]);
     const int64_t b = b0 + threadIdx.x;
     if (b >= nb) continue;
+    if constexpr (NOISE) {
+      x0 = aqn_noisy8(x0, 16 * b, s_tensor[j], aqn);
+      x1 = aqn_noisy8(x1, 16 * b + 8, s_tensor[j], aqn);
+    }
     uint32_t sb = 0;
     uint2 packed = make_uint2(0u, 0u);
     if (s_t > 0.0f) {
@@ -299,6 +316,7 @@ __global__ void __launch_bounds__(256) fp8_a1x128_kernel(const uint16_t* __restr
 // reads two full 256-byte tile rows), so the tile's absmax is reduced in
 // registers, then encoded without re-reading HBM.
 
+template <bool NOISE>
 __global__ void __launch_bounds__(256) fp8_w128_kernel(const __grid_constant__ Fp8WBatch batch) {
   __shared__ uint32_t warp_max[8];
   __shared__ int64_t s_first[kMaxJobs + 1];  // job table in shared memory (see the NVFP4 kernels)
@@ -327,6 +345,7 @@ __global__ void __launch_bounds__(256) fp8_w128_kernel(const __grid_constant__ F
       const int64_t row = row0 + u * 16 + (threadIdx.x >> 4);
       if (row < N) {
         v[u] = __ldg(reinterpret_cast<const uint4*>(W + row * K + tc * 128) + cchunk);
+        if constexpr (NOISE) v[u] = aqn_noisy8(v[u], row * K + tc * 128 + 8 * cchunk, batch.job[j].tensor, batch.aqn);
         m = max(m, absmax_bits8(v[u]));
       } else {
         v[u] = make_uint4(0, 0, 0, 0);
@@ -419,14 +438,24 @@ cudaError_t launch_nvfp4(Nvfp4Batch& batch, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   static bool attr = false;
   if (!attr) {
-    err = cudaFuncSetAttribute(nvfp4_amax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kNvfp4Smem);
+    err = cudaFuncSetAttribute(nvfp4_amax_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kNvfp4Smem);
     if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(nvfp4_encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kEncodeSmem);
+      err = cudaFuncSetAttribute(nvfp4_amax_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kNvfp4Smem);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(nvfp4_encode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEncodeSmem);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(nvfp4_encode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEncodeSmem);
     if (err != cudaSuccess) return err;
     attr = true;
   }
-  if (amax_chunks > 0) nvfp4_amax_kernel<<<grid_for(amax_chunks, 2), 256, kNvfp4Smem, stream>>>(batch);
-  nvfp4_encode_kernel<<<grid_for(enc_chunks, 3), 512, kEncodeSmem, stream>>>(batch);
+  // sigma 0 adds exactly nothing (W + 0 z = W), so it takes the plain kernels
+  if (batch.aqn.sigma != 0.0f) {
+    if (amax_chunks > 0) nvfp4_amax_kernel<true><<<grid_for(amax_chunks, 2), 256, kNvfp4Smem, stream>>>(batch);
+    nvfp4_encode_kernel<true><<<grid_for(enc_chunks, 3), 512, kEncodeSmem, stream>>>(batch);
+  } else {
+    if (amax_chunks > 0) nvfp4_amax_kernel<false><<<grid_for(amax_chunks, 2), 256, kNvfp4Smem, stream>>>(batch);
+    nvfp4_encode_kernel<false><<<grid_for(enc_chunks, 3), 512, kEncodeSmem, stream>>>(batch);
+  }
   return cudaGetLastError();
 }
 
@@ -447,7 +476,28 @@ cudaError_t launch_fp8_w128(Fp8WBatch& batch, cudaStream_t stream) {
   }
   batch.total_tiles = tiles;
   if (tiles == 0) return cudaSuccess;
-  fp8_w128_kernel<<<grid_for(tiles, 6), 256, 0, stream>>>(batch);
+  if (batch.aqn.sigma != 0.0f)
+    fp8_w128_kernel<true><<<grid_for(tiles, 6), 256, 0, stream>>>(batch);
+  else
+    fp8_w128_kernel<false><<<grid_for(tiles, 6), 256, 0, stream>>>(batch);
+  return cudaGetLastError();
+}
+
+__global__ void aqn_noise_probe_kernel(float* __restrict__ out, int64_t n, int64_t start, uint32_t tensor,
+                                       AqnParams a) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = start + i;
+    float z0, z1;
+    aqn_z2(static_cast<uint64_t>(e) >> 1, tensor, a, z0, z1);
+    out[i] = (e & 1) ? z1 : z0;
+  }
+}
+
+cudaError_t launch_aqn_noise_probe(float* out, int64_t n, int64_t start, uint32_t tensor, const AqnParams& a,
+                                   cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  aqn_noise_probe_kernel<<<grid_for((n + 255) / 256, 8), 256, 0, stream>>>(out, n, start, tensor, a);
   return cudaGetLastError();
 }
 

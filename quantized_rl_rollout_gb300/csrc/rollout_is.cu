@@ -10,10 +10,11 @@
 //
 // HBM-bound: every logit is read once.  One CTA (256 threads) per token row;
 // each thread streams its share of the row with 16-byte loads, four in
-// flight, and keeps a running (max, sum of exp(x - max)) in fp32, rescaling
-// the sum once per 32 values; the CTA then merges the 256 pairs.  Exponent
-// and logarithm use the base-2 hardware approximations (relative error about
-// 2^-22) on log2(e)-scaled values.
+// flight, and keeps a running (max, sum of exp(x - max)) in fp32: the max of
+// each 32 values by packed bf16 max, then one FMA, one exp2 and one add per
+// value; the CTA then merges the 256 pairs.  Exponent and logarithm use the
+// base-2 hardware approximations (relative error about 2^-22).  A NaN or +inf
+// logit is detected from the final log-sum-exp, not per value.
 #include <cuda_bf16.h>
 
 #include "linear.cuh"
@@ -68,72 +69,98 @@ struct Lse {
 
 }  // namespace
 
+// Largest of the 16 bf16 pairs in q[4] as an fp32 value (packed bf16 max).
+__device__ __forceinline__ float bf16_max32(const uint4 (&q)[4]) {
+  uint32_t w[16] = {q[0].x, q[0].y, q[0].z, q[0].w, q[1].x, q[1].y, q[1].z, q[1].w,
+                    q[2].x, q[2].y, q[2].z, q[2].w, q[3].x, q[3].y, q[3].z, q[3].w};
+#pragma unroll
+  for (int n = 8; n >= 1; n >>= 1)
+#pragma unroll
+    for (int i = 0; i < n; ++i) asm("max.bf16x2 %0, %1, %2;" : "=r"(w[i]) : "r"(w[i]), "r"(w[i + n]));
+  return fmaxf(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xFFFF0000u));
+}
+
 template <bool VEC>
-__global__ void __launch_bounds__(kThreads) token_logprob_is_kernel(const uint16_t* __restrict__ logits, int64_t T,
-                                                                    int64_t V, const int32_t* __restrict__ tokens,
-                                                                    const float* __restrict__ rollout_logp, float cap,
-                                                                    float* __restrict__ logp, float* __restrict__ w,
-                                                                    int32_t* status) {
+__global__ void __launch_bounds__(kThreads, 6) token_logprob_is_kernel(const uint16_t* __restrict__ logits, int64_t T,
+                                                                       int64_t V, const int32_t* __restrict__ tokens,
+                                                                       const float* __restrict__ rollout_logp,
+                                                                       float cap, float* __restrict__ logp,
+                                                                       float* __restrict__ w, int32_t* status) {
   __shared__ float red_m[kThreads / 32], red_s[kThreads / 32];
-  __shared__ int bad_val;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x == 0) bad_val = 0;
-  __syncthreads();
   for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
     const int tok = __ldg(tokens + t);
     const bool live = tok >= 0 && tok < V;
-    Lse st;
-    uint32_t nonfinite = 0;  // any +inf / NaN seen (bf16 exponent all ones, not -inf)
+    // running state: xm = max of the raw logits seen, s = sum of e^(x - xm)
+    float xm = -INFINITY, s = 0.0f;
     if (live) {
       const uint16_t* row = logits + t * V;
       if constexpr (VEC) {
         const uint4* rv = reinterpret_cast<const uint4*>(row);
         const int64_t nvec = V / 8;
+        const uint4 pad = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);  // bf16 -inf
         for (int64_t base = threadIdx.x; base < nvec; base += 4 * kThreads) {
           uint4 q[4];
-          int cnt = 0;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int64_t i = base + u * kThreads;
-            if (i < nvec) {
-              q[u] = __ldcs(rv + i);  // streamed once: no reuse, evict first
-              ++cnt;
-            }
+            q[u] = i < nvec ? __ldcs(rv + i) : pad;  // streamed once: evict first
           }
-          float v[32];
-          float bmax = -INFINITY;
+          const float bmax = bf16_max32(q);
+          if (!(bmax > -INFINITY)) {
+            // all -inf, or NaN beside -inf (the packed max skips NaN): a NaN
+            // poisons the sum so that the final check reports it
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t wd[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if ((wd[e] & 0x7FFFu) > 0x7F80u || (wd[e] & 0x7FFF0000u) > 0x7F800000u) s = __int_as_float(0x7FC00000);
+            }
+            continue;
+          }
+          if (bmax > xm) {
+            s = xm == -INFINITY ? 0.0f : s * ex2((xm - bmax) * kLog2e);
+            xm = bmax;
+          }
+          const float nm = -xm * kLog2e;
+          float acc0 = 0.0f, acc1 = 0.0f;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const uint32_t wd[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const uint32_t lo = wd[e] << 16, hi = wd[e] & 0xFFFF0000u;
-              nonfinite |= (u < cnt) && (((lo & 0x7F800000u) == 0x7F800000u && lo != 0xFF800000u) ||
-                                         ((hi & 0x7F800000u) == 0x7F800000u && hi != 0xFF800000u));
-              v[8 * u + 2 * e] = u < cnt ? __uint_as_float(lo) * kLog2e : -INFINITY;
-              v[8 * u + 2 * e + 1] = u < cnt ? __uint_as_float(hi) * kLog2e : -INFINITY;
-              bmax = fmaxf(bmax, fmaxf(v[8 * u + 2 * e], v[8 * u + 2 * e + 1]));
+              acc0 += ex2(fmaf(__uint_as_float(wd[e] << 16), kLog2e, nm));
+              acc1 += ex2(fmaf(__uint_as_float(wd[e] & 0xFFFF0000u), kLog2e, nm));
             }
           }
-          st.add_block(v, 32, bmax);
+          s += acc0 + acc1;
         }
       } else {
         for (int64_t i = threadIdx.x; i < V; i += kThreads) {
-          const uint32_t b = static_cast<uint32_t>(__ldcs(row + i)) << 16;
-          nonfinite |= (b & 0x7F800000u) == 0x7F800000u && b != 0xFF800000u;
-          const float v = __uint_as_float(b) * kLog2e;
-          st.add_block(&v, 1, v);
+          const float x = __uint_as_float(static_cast<uint32_t>(__ldcs(row + i)) << 16);
+          if (!(x > -INFINITY)) {
+            if (x != x) s = x;  // NaN: poison the sum, the final check reports it
+            continue;
+          }
+          if (x > xm) {
+            s = xm == -INFINITY ? 0.0f : s * ex2((xm - x) * kLog2e);
+            xm = x;
+          }
+          s += ex2((x - xm) * kLog2e);
         }
       }
     }
-    // CTA merge of the (max, sum) pairs
+    // CTA merge of the (max, sum) pairs, in log2(e)-scaled units
+    Lse st;
+    st.m = xm * kLog2e;
+    st.s = s;
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
       const float m2 = __shfl_xor_sync(0xFFFFFFFFu, st.m, o);
       const float s2 = __shfl_xor_sync(0xFFFFFFFFu, st.s, o);
       st.merge(m2, s2);
     }
-    if (__any_sync(0xFFFFFFFFu, nonfinite) && lane == 0) atomicOr(&bad_val, 1);
     if (lane == 0) {
       red_m[warp] = st.m;
       red_s[warp] = st.s;
@@ -144,21 +171,21 @@ __global__ void __launch_bounds__(kThreads) token_logprob_is_kernel(const uint16
       for (int i = 0; i < kThreads / 32; ++i) all.merge(red_m[i], red_s[i]);
       float lp = 0.0f, wt = 0.0f;
       if (live) {
+        const float lse2 = all.m + lg2(all.s);  // log2 of sum_v 2^(x_v log2 e)
+        // a NaN or +inf logit leaves the log-sum-exp NaN or +inf
+        if (lse2 != lse2 || lse2 == INFINITY) flag(status, QRR_DEV_NONFINITE);
         const float x = __uint_as_float(static_cast<uint32_t>(__ldg(logits + t * V + tok)) << 16);
-        // log(sum_v e^x_v) = (m + log2 s) ln 2 in natural units
-        lp = x - (all.m + lg2(all.s)) * kLn2;
+        lp = x - lse2 * kLn2;
         if (rollout_logp) {
           wt = ex2((lp - __ldg(rollout_logp + t)) * kLog2e);
           if (cap > 0.0f) wt = fminf(wt, cap);
         }
       }
       if (tok >= V) flag(status, QRR_DEV_BAD_INDEX);
-      if (bad_val) flag(status, QRR_DEV_NONFINITE);
-      bad_val = 0;
       logp[t] = lp;
       if (rollout_logp) w[t] = wt;
     }
-    __syncthreads();  // red_m / red_s / bad_val are reused by the next row
+    __syncthreads();  // red_m / red_s are reused by the next row
   }
 }
 
@@ -168,7 +195,7 @@ cudaError_t launch_token_logprob_is(const void* logits, int64_t T, int64_t V, co
   if (T == 0) return cudaSuccess;
   int dev = 0, sms = kSMs;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t cap_ctas = static_cast<int64_t>(sms) * 8;  // 8 resident CTAs per SM
+  const int64_t cap_ctas = static_cast<int64_t>(sms) * 6;  // 6 resident CTAs per SM
   const unsigned grid = static_cast<unsigned>(T < cap_ctas ? T : cap_ctas);
   const bool vec = V % 8 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
   if (vec)

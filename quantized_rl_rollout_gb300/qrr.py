@@ -75,6 +75,10 @@ SIGNATURES = {
                                               _c_p]),
     "qrr_round_probe": (ctypes.c_int, [_c_p, _c_i64, _c_i32, _c_p, _c_p]),
     "qrr_get_last_device_status": (ctypes.c_int, [_c_p, _c_p, _c_p]),
+    "qrr_requantize_weights_aqn": (ctypes.c_int, [ctypes.POINTER(WeightDesc), _c_i32, _c_i32, _c_i32, ctypes.c_float,
+                                                  ctypes.c_uint64, _c_i32, _c_p, _c_sz, _c_p, _c_p]),
+    "qrr_aqn_sigma": (ctypes.c_float, [_c_i32, _c_i32, ctypes.c_double, ctypes.c_double]),
+    "qrr_aqn_noise_probe": (ctypes.c_int, [_c_p, _c_i64, _c_i64, ctypes.c_uint64, _c_i32, _c_i32, _c_p]),
     "qrr_token_logprobs_is": (ctypes.c_int, [_c_p, _c_i64, _c_i64, _c_p, _c_p, ctypes.c_float, _c_p, _c_p, _c_p,
                                              _c_p]),
     "qrr_workspace_bytes": (_c_sz, [_c_i32, _c_i64, _c_i64, _c_i64, _c_i32]),
@@ -259,6 +263,16 @@ def gemm_fp8_blockwise(qa, sa, qw, sw, mode=SCALE_FP32, y=None, dev_status=None,
     return y
 
 
+def _weight_descs(weights, outputs, fmt):
+    count = len(weights)
+    descs = (WeightDesc * max(count, 1))()
+    for i, (w, out) in enumerate(zip(weights, outputs)):
+        _need(w, torch.bfloat16, f"weights[{i}]")
+        ts = out[2] if fmt == FORMAT_NVFP4 else None
+        descs[i] = WeightDesc(_ptr(w), w.shape[0], w.shape[1], _ptr(out[0]), _ptr(out[1]), _ptr(ts))
+    return descs, count
+
+
 def requantize_weights(weights, outputs, fmt=FORMAT_NVFP4, mode=SCALE_FP32, workspace=None, dev_status=None,
                        stream=None):
     """Re-quantize every bf16 weight of ``weights`` into ``outputs``.
@@ -266,18 +280,37 @@ def requantize_weights(weights, outputs, fmt=FORMAT_NVFP4, mode=SCALE_FP32, work
     ``outputs[i]`` is ``(codes, scales, tensor_scale)`` for NVFP4 or
     ``(q, scales)`` for FP8 128x128.
     """
-    count = len(weights)
-    descs = (WeightDesc * max(count, 1))()
-    for i, (w, out) in enumerate(zip(weights, outputs)):
-        _need(w, torch.bfloat16, f"weights[{i}]")
-        ts = out[2] if fmt == FORMAT_NVFP4 else None
-        descs[i] = WeightDesc(_ptr(w), w.shape[0], w.shape[1], _ptr(out[0]), _ptr(out[1]), _ptr(ts))
+    descs, count = _weight_descs(weights, outputs, fmt)
     dev = weights[0].device if count else torch.device("cuda")
     if workspace is None:
         workspace = _workspace(lib().qrr_requantize_workspace_bytes(count), dev)
     _check(lib().qrr_requantize_weights(descs, count, int(fmt), int(mode), _ptr(workspace), workspace.numel(),
                                         _ptr(dev_status), _stream(stream)), "qrr_requantize_weights")
     return outputs
+
+
+def requantize_weights_aqn(weights, outputs, sigma, seed, step, fmt=FORMAT_NVFP4, mode=SCALE_FP32, workspace=None,
+                           dev_status=None, stream=None):
+    """``requantize_weights`` of the noisy masters bf16(W + sigma z) (see ``qrr_requantize_weights_aqn``)."""
+    descs, count = _weight_descs(weights, outputs, fmt)
+    dev = weights[0].device if count else torch.device("cuda")
+    if workspace is None:
+        workspace = _workspace(lib().qrr_requantize_workspace_bytes(count), dev)
+    _check(lib().qrr_requantize_weights_aqn(descs, count, int(fmt), int(mode), float(sigma), int(seed), int(step),
+                                            _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream)),
+           "qrr_requantize_weights_aqn")
+    return outputs
+
+
+def aqn_sigma(step, steps, sigma_start, sigma_end) -> float:
+    return float(lib().qrr_aqn_sigma(int(step), int(steps), float(sigma_start), float(sigma_end)))
+
+
+def aqn_noise_probe(n, seed, tensor, step, start=0, out=None, stream=None):
+    out = torch.empty(n, dtype=torch.float32, device="cuda") if out is None else out
+    _check(lib().qrr_aqn_noise_probe(_ptr(out), int(n), int(start), int(seed), int(tensor), int(step),
+                                     _stream(stream)), "qrr_aqn_noise_probe")
+    return out
 
 
 def round_probe(values, fmt, out=None, stream=None):

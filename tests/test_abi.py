@@ -148,3 +148,21 @@ def test_generic_workspace_query_matches_per_call_queries(lib):
     assert lib.qrr_workspace_bytes(qrr.OP_REQUANTIZE_WEIGHTS, 7, 0, 0, 0) == lib.qrr_requantize_workspace_bytes(7)
     assert lib.qrr_workspace_bytes(qrr.OP_GEMM_FP8, 4096, 4096, 4096, 0) == 0
     assert lib.qrr_workspace_bytes(99, 1, 1, 1, 1) == 0
+
+
+def test_aqn_and_is_validation(lib):
+    from quantized_rl_rollout_gb300 import qrr
+
+    descs = (qrr.WeightDesc * 1)()
+    descs[0] = qrr.WeightDesc(FAKE, 4, 64, FAKE, FAKE, FAKE)
+    assert lib.qrr_requantize_weights_aqn(descs, 1, 0, 0, -1.0, 1, 0, FAKE, 4096, None, None) == 1  # sigma < 0
+    assert lib.qrr_requantize_weights_aqn(descs, 1, 0, 0, float("nan"), 1, 0, FAKE, 4096, None, None) == 1
+    assert lib.qrr_requantize_weights_aqn(descs, 1, 0, 0, 1e-3, 1, -2, FAKE, 4096, None, None) == 1  # step < 0
+    assert lib.qrr_requantize_weights_aqn(descs, 1, 0, 0, 1e-3, 1, 0, None, 0, None, None) == 4
+    assert lib.qrr_aqn_noise_probe(FAKE + 2, 4, 0, 1, 0, 0, None) == 3
+    assert lib.qrr_aqn_noise_probe(FAKE, -1, 0, 1, 0, 0, None) == 1
+    assert abs(lib.qrr_aqn_sigma(0, 100, 1e-2, 5e-4) - 1e-2) < 1e-9
+    assert abs(lib.qrr_aqn_sigma(99, 100, 1e-2, 5e-4) - 5e-4) < 1e-9
+    assert lib.qrr_token_logprobs_is(FAKE, 4, 0, FAKE, None, 0.0, FAKE, None, None, None) == 1  # V = 0
+    assert lib.qrr_token_logprobs_is(FAKE, 4, 8, FAKE, FAKE, 0.0, FAKE, None, None, None) == 1  # no w
+    assert lib.qrr_token_logprobs_is(FAKE + 8, 4, 8, FAKE, None, 0.0, FAKE, None, None, None) == 3

@@ -111,3 +111,14 @@ def test_flags(q):
         st.zero_()
         q.token_logprobs_is(lg2, tok, dev_status=st)
         assert q.get_last_device_status(st) & q.DEV_NONFINITE, bad
+
+
+def test_nan_beside_masked_entries(q):
+    """A NaN in a stretch of -inf logits (which the block max skips) is still reported."""
+    lg = torch.full((2, 1024), float("-inf"), dtype=torch.bfloat16, device=DEV)
+    lg[:, 900] = 1.0
+    lg[1, 40] = float("nan")
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lp = q.token_logprobs_is(lg, torch.tensor([900, 900], dtype=torch.int32, device=DEV), dev_status=st)
+    assert q.get_last_device_status(st) & q.DEV_NONFINITE
+    assert abs(lp[0].item()) <= LP_ABS
