@@ -22,7 +22,9 @@ written in numpy:
 * ``rollout_is`` -- token log-probabilities from a row of logits and the
   token-level importance-sampling weights between rollout and trainer;
 * ``aqn``      -- adaptive quantization noise: counter-based noise added to the
-  masters before re-quantization, with its schedule.
+  masters before re-quantization, with its schedule;
+* ``lora_backward`` -- the backward pass of the linear through the frozen
+  NVFP4 weight: dX, dA, dB.
 
 Sources.  The pages describe QeRL ("QeRL: Beyond Efficiency -- Quantization-
 enhanced Reinforcement Learning for LLMs", abstract; "NVIDIA and MIT Collaborate
@@ -39,4 +41,4 @@ float32 arithmetic (correctly rounded, subnormals kept) produces it; sums of
 products are formed in float64.
 """
 
-from . import formats, nvfp4, fp8, linear, requant, rollout_is, aqn  # noqa: F401
+from . import formats, nvfp4, fp8, linear, requant, rollout_is, aqn, lora_backward  # noqa: F401
