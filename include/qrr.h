@@ -256,6 +256,35 @@ qrr_status qrr_requantize_weights(const qrr_weight_desc* descs, int32_t count, i
                                   int32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Backward pass of the W4A16 + LoRA linear through the frozen NVFP4 weight
+ * ("NVIDIA and MIT Collaborate on QeRL", Key Features, "Stable
+ * Backpropagation": only the adapter is trained, its gradients stay precise;
+ * "Jet-RL: Enabling On-Policy FP8 RL ...", Quick Overview: the backward pass
+ * stays in BF16).  For the forward y = x . W_hat^T + (alpha/r) (x . A^T) . B^T
+ * and the upstream gradient dY:
+ *   dX = dY . W_hat + (alpha/r) (dY . B) . A      bf16 [M][K]
+ *   dA = (alpha/r) (dY . B)^T . x                 fp32 [r][K]
+ *   dB = (alpha/r) dY^T . (x . A^T)               fp32 [N][r]
+ *   dy    bf16 [M][N];  x bf16 [M][K] (the forward's input; only read with an adapter)
+ *   codes/scales/tensor_scale: the frozen NVFP4 weight [N][K]
+ *   lora_A bf16 [r][K], lora_B bf16 [N][r] (both NULL or r == 0: no adapter,
+ *          dA / dB untouched and may be NULL)
+ *   workspace  qrr_lora_backward_workspace_bytes(M, N, K, r) bytes (it holds
+ *          the weight's bf16 transpose, K x N x 2 bytes, among others)
+ * Shapes as the forward: K % 256 == 0, N % 128 == 0, r <= 64 and r % 8 == 0.
+ * The weight's e2m1 x e4m3 part is exact in bf16 and its tensor scale is
+ * applied in fp32; products are exact and sums fp32 (the rank-r projections
+ * carried as bf16 (high, low) pairs, about 2^-17 relative).  dA and dB are
+ * summed over token slices in a fixed order: results do not depend on
+ * timing. */
+size_t qrr_lora_backward_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r);
+qrr_status qrr_lora_backward_nvfp4(const void* dy, int64_t M, int64_t N, const void* x, int64_t K,
+                                   const uint8_t* codes, const uint8_t* scales, const float* tensor_scale,
+                                   const void* lora_A, const void* lora_B, int32_t r, float alpha, void* dx, float* dA,
+                                   float* dB, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                   void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Token log-probabilities and token-level importance-sampling weights
  * ("NVIDIA NeMo RL behaalt 48% ...", the paragraph on importance sampling in
  * "Waarom dit belangrijk is voor AI-economie": the shift between the
@@ -292,6 +321,7 @@ qrr_status qrr_get_last_device_status(int32_t* host_out, const int32_t* dev_stat
  *   QRR_OP_LINEAR_NVFP4_LORA   M tokens, N outputs, K inputs, LoRA rank r
  *   QRR_OP_REQUANTIZE_WEIGHTS  M = number of descriptors
  *   QRR_OP_QUANTIZE_FP8, QRR_OP_GEMM_FP8: no scratch (0)
+ *   QRR_OP_LORA_BACKWARD       M tokens, N outputs, K inputs, LoRA rank r
  * It returns the same value as the per-call query; 0 for an unknown op or
  * invalid sizes. */
 typedef enum qrr_op {
@@ -299,7 +329,8 @@ typedef enum qrr_op {
   QRR_OP_LINEAR_NVFP4_LORA = 1,
   QRR_OP_REQUANTIZE_WEIGHTS = 2,
   QRR_OP_QUANTIZE_FP8 = 3,
-  QRR_OP_GEMM_FP8 = 4
+  QRR_OP_GEMM_FP8 = 4,
+  QRR_OP_LORA_BACKWARD = 5
 } qrr_op;
 size_t qrr_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t r);
 

@@ -310,9 +310,148 @@ qrr_status noalloc_scratch(void** out) {
   return QRR_OK;
 }
 
+// ---- LoRA backward: workspace plan ----
+struct BwdPlan {
+  int t_cols, slice, ks_u, ks_t;
+  size_t wt_off, at2_off, bt_off, tu_off, tt_off, pu_off, pt_off, tick_off, tick_bytes, gpart_off, total;
+};
+
+BwdPlan plan_backward(int64_t M, int64_t N, int64_t K, int32_t r) {
+  BwdPlan p{};
+  p.t_cols = r > 0 ? 64 * static_cast<int>((2 * r + 63) / 64) : 0;
+  p.slice = 1024;  // contraction slice of the rank projections (16 steps of 64)
+  p.ks_u = static_cast<int>((N + p.slice - 1) / p.slice);
+  p.ks_t = static_cast<int>((K + p.slice - 1) / p.slice);
+  size_t off = 0;
+  p.wt_off = off;
+  off += round_up(static_cast<size_t>(K) * N * 2);
+  p.at2_off = off;
+  off += round_up(static_cast<size_t>(K) * p.t_cols * 2);
+  p.bt_off = off;
+  off += round_up(static_cast<size_t>(r) * N * 2);
+  p.tu_off = off;
+  off += round_up(static_cast<size_t>(M) * p.t_cols * 2);
+  p.tt_off = off;
+  off += round_up(static_cast<size_t>(M) * p.t_cols * 2);
+  p.pu_off = off;
+  off += round_up(static_cast<size_t>((p.ks_u + 3) & ~3) * M * r * 4);
+  p.pt_off = off;
+  off += round_up(static_cast<size_t>((p.ks_t + 3) & ~3) * M * r * 4);
+  p.tick_off = off;
+  p.tick_bytes = 2 * static_cast<size_t>((M + 127) / 128) * 4;
+  off += round_up(p.tick_bytes);
+  p.gpart_off = off;
+  if (r > 0 && M > 0) {
+    const size_t ga = static_cast<size_t>(lora_grad_slices(M, K)) * r * K;
+    const size_t gb = static_cast<size_t>(lora_grad_slices(M, N)) * r * N;
+    off += round_up((ga > gb ? ga : gb) * 4);
+  }
+  p.total = round_up(off) + kAlign;
+  return p;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t qrr_lora_backward_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r) {
+  if (M < 0 || N < 0 || K < 0 || r < 0 || r > 64) return 0;
+  return plan_backward(M, N, K, r).total;
+}
+
+qrr_status qrr_lora_backward_nvfp4(const void* dy, int64_t M, int64_t N, const void* x, int64_t K,
+                                   const uint8_t* codes, const uint8_t* scales, const float* tensor_scale,
+                                   const void* lora_A, const void* lora_B, int32_t r, float alpha, void* dx, float* dA,
+                                   float* dB, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                   void* stream) {
+  if (M < 0 || N < 0 || K < 0 || r < 0) return QRR_ERR_INVALID_ARG;
+  const bool lora = r > 0 && lora_A && lora_B;
+  if (!lora) r = 0;
+  if (!tensor_scale) return QRR_ERR_INVALID_ARG;
+  if (M * N > 0 && !dy) return QRR_ERR_INVALID_ARG;
+  if (M * K > 0 && (!dx || (lora && !x))) return QRR_ERR_INVALID_ARG;
+  if (N * K > 0 && (!codes || !scales)) return QRR_ERR_INVALID_ARG;
+  if (lora && ((K > 0 && !dA) || (N > 0 && !dB))) return QRR_ERR_INVALID_ARG;
+  if (K % 256 != 0 || N % 128 != 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return QRR_ERR_UNSUPPORTED_SHAPE;
+  if (r > 64 || (r > 0 && r % 8 != 0)) return QRR_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(dy) || !aligned16(x) || !aligned16(codes) || !aligned16(scales) || !aligned16(dx) ||
+      (reinterpret_cast<uintptr_t>(tensor_scale) & 3u) ||
+      (lora && (!aligned16(lora_A) || !aligned16(lora_B) || !aligned16(dA) || !aligned16(dB))))
+    return QRR_ERR_MISALIGNED;
+  const BwdPlan pl = plan_backward(M, N, K, r);
+  if (!workspace || workspace_bytes < pl.total) return QRR_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return QRR_ERR_MISALIGNED;
+  if (injected_cuda_fault()) return QRR_ERR_CUDA;
+  cudaStream_t s = as_stream(stream);
+  // degenerate sizes: sums over nothing are zero
+  if (M == 0 || N == 0 || K == 0) {
+    if (M * K > 0 && cudaMemsetAsync(dx, 0, static_cast<size_t>(M * K) * 2, s) != cudaSuccess) return QRR_ERR_CUDA;
+    if (lora && K > 0 && cudaMemsetAsync(dA, 0, static_cast<size_t>(r) * K * 4, s) != cudaSuccess) return QRR_ERR_CUDA;
+    if (lora && N > 0 && cudaMemsetAsync(dB, 0, static_cast<size_t>(N) * r * 4, s) != cudaSuccess) return QRR_ERR_CUDA;
+    return QRR_OK;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  __nv_bfloat16* wt = reinterpret_cast<__nv_bfloat16*>(ws + pl.wt_off);
+  uint16_t* at2 = reinterpret_cast<uint16_t*>(ws + pl.at2_off);
+  uint16_t* bt = reinterpret_cast<uint16_t*>(ws + pl.bt_off);
+  __nv_bfloat16* tu = reinterpret_cast<__nv_bfloat16*>(ws + pl.tu_off);
+  __nv_bfloat16* tt = reinterpret_cast<__nv_bfloat16*>(ws + pl.tt_off);
+  if (launch_lora_backward_prep(codes, scales, lora_A, lora_B, static_cast<int>(N), static_cast<int>(K), r, pl.t_cols,
+                                wt, at2, bt, s) != cudaSuccess)
+    return QRR_ERR_CUDA;
+  if (lora) {
+    // u' = (alpha/r) (dY . B) / g and t' = (alpha/r) (x . A^T) / g, split over
+    // 1024-wide contraction slices with a ticket per 128-token tile
+    if (cudaMemsetAsync(ws + pl.tick_off, 0, pl.tick_bytes, s) != cudaSuccess) return QRR_ERR_CUDA;
+    LoraDownBatch lb{};
+    lb.status = dev_status;
+    const int m_tiles = static_cast<int>((M + 127) / 128);
+    const void* src_x[2] = {dy, x};
+    const void* src_a[2] = {bt, lora_A};
+    const int64_t kk[2] = {N, K};
+    __nv_bfloat16* outs[2] = {tu, tt};
+    const size_t poff[2] = {pl.pu_off, pl.pt_off};
+    const int ksv[2] = {pl.ks_u, pl.ks_t};
+    for (int i = 0; i < 2; ++i) {
+      LoraDownLayer& ld = lb.l[lb.count++];
+      if (!make_tmap_2d(&ld.tx, src_x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, M, kk[i], kk[i] * 2, 128, 64,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !make_tmap_2d(&ld.ta, src_a[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r, kk[i], kk[i] * 2, (r + 15) / 16 * 16, 64,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+        return QRR_ERR_CUDA;
+      ld.t = outs[i];
+      ld.tensor_scale = tensor_scale;
+      ld.tpart = reinterpret_cast<float*>(ws + poff[i]);
+      ld.tickets = reinterpret_cast<uint32_t*>(ws + pl.tick_off) + i * m_tiles;
+      ld.x = static_cast<const uint16_t*>(src_x[i]);
+      ld.x16 = nullptr;
+      ld.pexp = nullptr;
+      ld.M = static_cast<int>(M);
+      ld.K = static_cast<int>(kk[i]);
+      ld.r = r;
+      ld.R = (r + 15) / 16 * 16;
+      ld.t_cols = pl.t_cols;
+      ld.ks = ksv[i];
+      ld.slice_steps = pl.slice / 64;
+      ld.lora_scale = alpha / static_cast<float>(r);
+    }
+    if (launch_lora_down_tc(lb, s) != cudaSuccess) return QRR_ERR_CUDA;
+  }
+  // dX = g (dY . W_q + u' . A)
+  Bf16GemmArgs ga{dy, wt, lora ? tu : nullptr, lora ? at2 : nullptr, tensor_scale, dx, M, K, N,
+                  lora ? pl.t_cols : 0};
+  if (launch_gemm_bf16_tc(ga, dev_status, s) != cudaSuccess) return QRR_ERR_CUDA;
+  if (lora) {
+    float* gpart = reinterpret_cast<float*>(ws + pl.gpart_off);
+    if (launch_lora_grad(x, reinterpret_cast<const uint16_t*>(tu), static_cast<int>(M), static_cast<int>(K), r,
+                         pl.t_cols, tensor_scale, false, gpart, dA, s) != cudaSuccess ||
+        launch_lora_grad(dy, reinterpret_cast<const uint16_t*>(tt), static_cast<int>(M), static_cast<int>(N), r,
+                         pl.t_cols, tensor_scale, true, gpart, dB, s) != cudaSuccess)
+      return QRR_ERR_CUDA;
+  }
+  return QRR_OK;
+}
+
 
 const char* qrr_status_string(int status) {
   switch (status) {
@@ -558,6 +697,7 @@ size_t qrr_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t 
       return M < 0 || M > INT32_MAX ? 0 : qrr_requantize_workspace_bytes(static_cast<int32_t>(M));
     case QRR_OP_QUANTIZE_FP8:
     case QRR_OP_GEMM_FP8: return 0;
+    case QRR_OP_LORA_BACKWARD: return qrr_lora_backward_workspace_bytes(M, N, K, r);
     default: return 0;
   }
 }

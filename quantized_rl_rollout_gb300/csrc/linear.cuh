@@ -88,6 +88,29 @@ cudaError_t launch_fp8_gemm_tc(const Fp8GemmArgs& a, int32_t* status, cudaStream
 // power-of-two scales on the native block-scaled MMA (gemm_fp8_mx.cu)
 cudaError_t launch_fp8_gemm_mx(const Fp8GemmArgs& a, int32_t* status, cudaStream_t stream);
 
+// ---- bf16 GEMM with an extra contraction block (gemm_bf16_tc.cu) ----
+// y[m, c] = g (sum_n A[m, n] B[c, n] + sum_j A2[m, j] B2[c, j]); all K-major
+// bf16, y bf16 [M, C]; K, K2 multiples of 64, C a multiple of 128.
+struct Bf16GemmArgs {
+  const void* A;   // [M, K]
+  const void* B;   // [C, K]
+  const void* A2;  // [M, K2] or null (K2 = 0)
+  const void* B2;  // [C, K2]
+  const float* g;  // device scalar (1 when null or 0)
+  void* y;
+  int64_t M, C, K, K2;
+};
+cudaError_t launch_gemm_bf16_tc(const Bf16GemmArgs& a, int32_t* status, cudaStream_t stream);
+
+// ---- LoRA backward helpers (lora_bwd.cu) ----
+cudaError_t launch_lora_backward_prep(const uint8_t* codes, const uint8_t* scales, const void* A, const void* B,
+                                      int N, int K, int r, int t_cols, __nv_bfloat16* wt, uint16_t* at2, uint16_t* bt,
+                                      cudaStream_t stream);
+int lora_grad_slices(int64_t M, int64_t C);
+cudaError_t launch_lora_grad(const void* X, const uint16_t* tp, int M, int C, int r, int t_cols,
+                             const float* tensor_scale, bool transposed, float* part, float* out,
+                             cudaStream_t stream);
+
 // ---- token log-probabilities and importance-sampling weights (rollout_is.cu) ----
 cudaError_t launch_token_logprob_is(const void* logits, int64_t T, int64_t V, const int32_t* tokens,
                                     const float* rollout_logp, float cap, float* logp, float* w, int32_t* status,

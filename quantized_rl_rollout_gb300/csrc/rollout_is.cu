@@ -108,15 +108,17 @@ __global__ void __launch_bounds__(kThreads, 6) token_logprob_is_kernel(const uin
           }
           const float bmax = bf16_max32(q);
           if (!(bmax > -INFINITY)) {
-            // all -inf, or NaN beside -inf (the packed max skips NaN): a NaN
-            // poisons the sum so that the final check reports it
+            // all -inf, or NaN beside -inf (the packed max skips NaN, and a
+            // sum whose max is -inf is dropped by the merge): report it here
+            bool nan_seen = false;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const uint32_t wd[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                if ((wd[e] & 0x7FFFu) > 0x7F80u || (wd[e] & 0x7FFF0000u) > 0x7F800000u) s = __int_as_float(0x7FC00000);
+                nan_seen |= (wd[e] & 0x7FFFu) > 0x7F80u || (wd[e] & 0x7FFF0000u) > 0x7F800000u;
             }
+            if (nan_seen) flag(status, QRR_DEV_NONFINITE);
             continue;
           }
           if (bmax > xm) {
@@ -140,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 6) token_logprob_is_kernel(const uin
         for (int64_t i = threadIdx.x; i < V; i += kThreads) {
           const float x = __uint_as_float(static_cast<uint32_t>(__ldcs(row + i)) << 16);
           if (!(x > -INFINITY)) {
-            if (x != x) s = x;  // NaN: poison the sum, the final check reports it
+            if (x != x) flag(status, QRR_DEV_NONFINITE);
             continue;
           }
           if (x > xm) {

@@ -29,6 +29,7 @@ OP_LINEAR_NVFP4_LORA = 1
 OP_REQUANTIZE_WEIGHTS = 2
 OP_QUANTIZE_FP8 = 3
 OP_GEMM_FP8 = 4
+OP_LORA_BACKWARD = 5
 
 _c_i64 = ctypes.c_int64
 _c_i32 = ctypes.c_int32
@@ -75,6 +76,9 @@ SIGNATURES = {
                                               _c_p]),
     "qrr_round_probe": (ctypes.c_int, [_c_p, _c_i64, _c_i32, _c_p, _c_p]),
     "qrr_get_last_device_status": (ctypes.c_int, [_c_p, _c_p, _c_p]),
+    "qrr_lora_backward_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_i64, _c_i32]),
+    "qrr_lora_backward_nvfp4": (ctypes.c_int, [_c_p, _c_i64, _c_i64, _c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i32,
+                                               ctypes.c_float, _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p, _c_p]),
     "qrr_requantize_weights_aqn": (ctypes.c_int, [ctypes.POINTER(WeightDesc), _c_i32, _c_i32, _c_i32, ctypes.c_float,
                                                   ctypes.c_uint64, _c_i32, _c_p, _c_sz, _c_p, _c_p]),
     "qrr_aqn_sigma": (ctypes.c_float, [_c_i32, _c_i32, ctypes.c_double, ctypes.c_double]),
@@ -358,3 +362,31 @@ def token_logprobs_is(logits, tokens, rollout_logp=None, cap=0.0, logp=None, w=N
                                        _ptr(w) if rollout_logp is not None else None, _ptr(dev_status),
                                        _stream(stream)), "qrr_token_logprobs_is")
     return logp if rollout_logp is None else (logp, w)
+
+
+def lora_backward_workspace_bytes(M, N, K, r) -> int:
+    return int(lib().qrr_lora_backward_workspace_bytes(M, N, K, r))
+
+
+def lora_backward_nvfp4(dy, x, codes, scales, tensor_scale, lora_A=None, lora_B=None, alpha=0.0, dx=None, dA=None,
+                        dB=None, workspace=None, dev_status=None, stream=None):
+    """(dX bf16 [M, K], dA fp32 [r, K], dB fp32 [N, r]) of the linear's backward
+    through the frozen NVFP4 weight (dA, dB None without an adapter)."""
+    _need(dy, torch.bfloat16, "dy")
+    m, n = dy.shape
+    k = codes.shape[1] * 2
+    r = 0 if lora_A is None or lora_B is None else int(lora_A.shape[0])
+    dev = dy.device
+    dx = torch.empty(m, k, dtype=torch.bfloat16, device=dev) if dx is None else dx
+    if r:
+        _need(x, torch.bfloat16, "x")
+        dA = torch.empty(r, k, dtype=torch.float32, device=dev) if dA is None else dA
+        dB = torch.empty(n, r, dtype=torch.float32, device=dev) if dB is None else dB
+    if workspace is None:
+        workspace = _workspace(lora_backward_workspace_bytes(m, n, k, r), dev)
+    _check(lib().qrr_lora_backward_nvfp4(_ptr(dy), m, n, _ptr(x), k, _ptr(codes), _ptr(scales), _ptr(tensor_scale),
+                                         _ptr(lora_A), _ptr(lora_B), r, float(alpha), _ptr(dx),
+                                         _ptr(dA) if r else None, _ptr(dB) if r else None, _ptr(workspace),
+                                         workspace.numel(), _ptr(dev_status), _stream(stream)),
+           "qrr_lora_backward_nvfp4")
+    return dx, (dA if r else None), (dB if r else None)
