@@ -12,6 +12,8 @@ tokens.  One step is one pass of the whole hot path over that layer set:
   decode   W4A16 + LoRA linear of all 7 layers at M = 1, 8 and 64 (one
            grouped call per token count)
   prefill  the same linears at M = 4096 (activations with 1% x10 channels)
+  lora_bwd the backward of those linears through the frozen NVFP4 weights at
+           M = 4096: dX (bf16) and the adapter gradients dA, dB (fp32)
   fp8      FP8 path at M = 4096: 128x128 weight re-quantize (fp8_requant),
            activation 1x128 quantize (fp8_act_quant), blockwise-scaled GEMM
            with fp32 scales (fp8_gemm, promotion) and with power-of-two scales
@@ -94,6 +96,7 @@ PHASE_KERNELS = {  # phase -> (kernel name prefix, template arguments as ncu pri
     "fp8_gemm": ("fp8_gemm_tc_kernel", ""),
     "fp8_gemm_pow2": ("fp8_gemm_mx_kernel", ""),
     "rollout_is": ("token_logprob_is_kernel", ""),
+    "lora_bwd": ("gemm_bf16_tc_kernel", ""),
 }
 
 
@@ -185,6 +188,12 @@ def fp8_quant_bytes(layers, m):
     w = sum(2 * l.n * l.k + l.n * l.k + 4 * ((l.n + 127) // 128) * (l.k // 128) for l in layers)
     a = sum(2 * m * l.k + m * l.k + 4 * m * (l.k // 128) for l in layers)
     return w, a
+
+
+def lora_bwd_flops(layers, m, r):
+    """dX = dY . W_hat (2 M N K) + the adapter's five rank-r products:
+    dY . B (2 M N r), (.) . A (2 M r K), dA (2 r K M), x . A^T (2 M K r), dB (2 N r M)."""
+    return sum(2 * m * l.n * l.k + 2 * m * r * (2 * l.n + 3 * l.k) for l in layers)
 
 
 def fp8_gemm_flops(layers, m):
@@ -430,6 +439,28 @@ class Workload:
         self.q.requantize_weights_aqn(self.masters, self.nv, sigma, 0x5EED, self.aqn_step, workspace=self.rq_ws)
         return 2
 
+    def _bwd(self):
+        if getattr(self, "bw", None) is None:
+            L = self.layers
+            dy = [inputs.activations(PREFILL_TOKENS, l.n, inputs.derive_seed(0, "8b", l.name, "dy"), device=self.dev)
+                  for l in L]
+            dx = [torch.empty(PREFILL_TOKENS, l.k, dtype=torch.bfloat16, device=self.dev) for l in L]
+            dA = [torch.empty(R, l.k, dtype=torch.float32, device=self.dev) for l in L]
+            dB = [torch.empty(l.n, R, dtype=torch.float32, device=self.dev) for l in L]
+            ws = torch.empty(max(self.q.lora_backward_workspace_bytes(PREFILL_TOKENS, l.n, l.k, R) for l in L),
+                             dtype=torch.uint8, device=self.dev)
+            self.bw = (dy, dx, dA, dB, ws)
+        return self.bw
+
+    def lora_bwd(self):
+        dy, dx, dA, dB, ws = self._bwd()
+        for i, _ in enumerate(self.layers):
+            c, s, t = self.nv[i]
+            A, B = self.lora[i]
+            self.q.lora_backward_nvfp4(dy[i], self.xp[i], c, s, t, A, B, ALPHA, dx=dx[i], dA=dA[i], dB=dB[i],
+                                       workspace=ws)
+        return 7 * 7  # per layer: transpose, factor transpose, rank projections, GEMM, 2 x (partials, reduce)
+
     def rollout_is(self):
         self.q.token_logprobs_is(self.lg, self.tok, self.rlp, IS_CAP, logp=self.lp, w=self.iw)
         return 1
@@ -480,8 +511,8 @@ class Workload:
 
 # one step over the 8B-class workload; the 32B-class stack (another
 # configuration, ~85 GB resident) is timed after it, in a region of its own
-PHASES = ["requant", "requant_aqn", "decode_m1", "decode_m8", "decode_m64", "prefill", "fp8_requant", "fp8_act_quant",
-          "fp8_gemm", "fp8_gemm_pow2", "rollout_is"]
+PHASES = ["requant", "requant_aqn", "decode_m1", "decode_m8", "decode_m64", "prefill", "lora_bwd", "fp8_requant",
+          "fp8_act_quant", "fp8_gemm", "fp8_gemm_pow2", "rollout_is"]
 EXTRA_PHASES = ["requant32b", "decode32b"]
 
 
@@ -506,6 +537,8 @@ def run_phase(w, name):
         return w.rollout_is()
     if name == "requant_aqn":
         return w.requant_aqn()
+    if name == "lora_bwd":
+        return w.lora_bwd()
     return w.fp8_gemm()
 
 
@@ -837,6 +870,10 @@ def main():
             f = linear_flops(L, PREFILL_TOKENS, R)
             breakdown[p] = {"ms": ms, "TFLOP/s": f / ms / 1e9, "frac_bf16": f / ms / 1e9 / peaks["bf16_tflops"],
                             "frac_bf16_sustained": f / ms / 1e9 / peaks["bf16_tflops_sustained"],
+                            "frac_bf16_spec": f / ms / 1e9 / SPEC_PEAKS["bf16_tflops"], "flops": f}
+        elif p == "lora_bwd":
+            f = lora_bwd_flops(L, PREFILL_TOKENS, R)
+            breakdown[p] = {"ms": ms, "TFLOP/s": f / ms / 1e9, "frac_bf16": f / ms / 1e9 / peaks["bf16_tflops"],
                             "frac_bf16_spec": f / ms / 1e9 / SPEC_PEAKS["bf16_tflops"], "flops": f}
         elif p == "fp8_requant":
             breakdown[p] = hbm(ms, fp8_quant_bytes(L, PREFILL_TOKENS)[0])

@@ -24,7 +24,9 @@ written in numpy:
 * ``aqn``      -- adaptive quantization noise: counter-based noise added to the
   masters before re-quantization, with its schedule;
 * ``lora_backward`` -- the backward pass of the linear through the frozen
-  NVFP4 weight: dX, dA, dB.
+  NVFP4 weight: dX, dA, dB;
+* ``attention`` -- decode attention over an E4M3 key/value cache with 1x128
+  row scales.
 
 Sources.  The pages describe QeRL ("QeRL: Beyond Efficiency -- Quantization-
 enhanced Reinforcement Learning for LLMs", abstract; "NVIDIA and MIT Collaborate
@@ -41,4 +43,4 @@ float32 arithmetic (correctly rounded, subnormals kept) produces it; sums of
 products are formed in float64.
 """
 
-from . import formats, nvfp4, fp8, linear, requant, rollout_is, aqn, lora_backward  # noqa: F401
+from . import formats, nvfp4, fp8, linear, requant, rollout_is, aqn, lora_backward, attention  # noqa: F401
