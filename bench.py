@@ -18,6 +18,9 @@ tokens.  One step is one pass of the whole hot path over that layer set:
            activation 1x128 quantize (fp8_act_quant), blockwise-scaled GEMM
            with fp32 scales (fp8_gemm, promotion) and with power-of-two scales
            (fp8_gemm_pow2, native block-scaled MMA)
+  attn     one decode step of attention over an E4M3 key/value cache: append
+           the step's rows, then attention for 64 sequences of 2048..4096
+           cached tokens, 32 query / 8 KV heads of 128 (attn_fp8)
   is       token log-probabilities and importance-sampling weights of 4096
            tokens over a 128256-entry vocabulary (rollout_is)
 
@@ -75,6 +78,7 @@ PREFILL_TOKENS = 4096
 R = 32
 ALPHA = 2.0 * R
 IS_TOKENS, IS_VOCAB, IS_CAP = 4096, 128256, 5.0  # importance-sampling phase: tokens x 8B-class vocabulary
+ATT_B, ATT_HQ, ATT_HKV, ATT_L = 64, 32, 8, 4096  # decode attention: sequences, query / KV heads, cache length
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 # GB300's published dense figures (per GPU), reported beside the measured peaks
 SPEC_PEAKS = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0, "fp8_tflops": 4500.0}
@@ -97,6 +101,7 @@ PHASE_KERNELS = {  # phase -> (kernel name prefix, template arguments as ncu pri
     "fp8_gemm_pow2": ("fp8_gemm_mx_kernel", ""),
     "rollout_is": ("token_logprob_is_kernel", ""),
     "lora_bwd": ("gemm_bf16_tc_kernel", ""),
+    "attn_fp8": ("attn_decode_fp8_kernel", ""),
 }
 
 
@@ -461,6 +466,35 @@ class Workload:
                                        workspace=ws)
         return 7 * 7  # per layer: transpose, factor transpose, rank projections, GEMM, 2 x (partials, reduce)
 
+    def _attn(self):
+        if getattr(self, "at", None) is None:
+            b, hq, hkv, lmax = ATT_B, ATT_HQ, ATT_HKV, ATT_L
+            g = torch.Generator(device="cpu")
+            g.manual_seed(inputs.derive_seed(0, "attn", "lens"))
+            lens = torch.randint(lmax // 2, lmax, (b,), generator=g, dtype=torch.int32)  # room for the new token
+            kq, ks = self.q.quantize_fp8_a1x128(inputs.activations(b * hkv * lmax, 128,
+                                                                   inputs.derive_seed(0, "attn", "k"), device=self.dev))
+            vq, vs = self.q.quantize_fp8_a1x128(inputs.activations(b * hkv * lmax, 128,
+                                                                   inputs.derive_seed(0, "attn", "v"), device=self.dev))
+            qq = inputs.activations(b * hq, 128, inputs.derive_seed(0, "attn", "q"), device=self.dev).view(b, hq, 128)
+            kn = inputs.activations(b * hkv, 128, inputs.derive_seed(0, "attn", "kn"), device=self.dev).view(b, hkv, 128)
+            vn = inputs.activations(b * hkv, 128, inputs.derive_seed(0, "attn", "vn"), device=self.dev).view(b, hkv, 128)
+            ws = torch.empty(self.q.lib().qrr_attention_decode_fp8_workspace_bytes(b, hq, lmax), dtype=torch.uint8,
+                             device=self.dev)
+            self.at = dict(kc=kq.view(b, hkv, lmax, 128), ks=ks.view(b, hkv, lmax), vc=vq.view(b, hkv, lmax, 128),
+                           vs=vs.view(b, hkv, lmax), q=qq, kn=kn, vn=vn, pos=lens.to(self.dev),
+                           lens=(lens + 1).to(self.dev), out=torch.empty_like(qq), ws=ws,
+                           bytes=int((lens + 1).sum()) * hkv * 2 * (128 + 4) + 2 * b * hq * 128 * 2
+                           + b * hkv * 2 * (128 * 2 + 128 + 4))
+        return self.at
+
+    def attn_fp8(self):
+        a = self._attn()
+        self.q.kv_append_fp8(a["kn"], a["vn"], a["pos"], a["kc"], a["ks"], a["vc"], a["vs"])
+        self.q.attention_decode_fp8(a["q"], a["kc"], a["ks"], a["vc"], a["vs"], a["lens"], out=a["out"],
+                                    workspace=a["ws"])
+        return 3
+
     def rollout_is(self):
         self.q.token_logprobs_is(self.lg, self.tok, self.rlp, IS_CAP, logp=self.lp, w=self.iw)
         return 1
@@ -512,7 +546,7 @@ class Workload:
 # one step over the 8B-class workload; the 32B-class stack (another
 # configuration, ~85 GB resident) is timed after it, in a region of its own
 PHASES = ["requant", "requant_aqn", "decode_m1", "decode_m8", "decode_m64", "prefill", "lora_bwd", "fp8_requant",
-          "fp8_act_quant", "fp8_gemm", "fp8_gemm_pow2", "rollout_is"]
+          "fp8_act_quant", "fp8_gemm", "fp8_gemm_pow2", "attn_fp8", "rollout_is"]
 EXTRA_PHASES = ["requant32b", "decode32b"]
 
 
@@ -539,6 +573,8 @@ def run_phase(w, name):
         return w.requant_aqn()
     if name == "lora_bwd":
         return w.lora_bwd()
+    if name == "attn_fp8":
+        return w.attn_fp8()
     return w.fp8_gemm()
 
 
@@ -871,6 +907,10 @@ def main():
             breakdown[p] = {"ms": ms, "TFLOP/s": f / ms / 1e9, "frac_bf16": f / ms / 1e9 / peaks["bf16_tflops"],
                             "frac_bf16_sustained": f / ms / 1e9 / peaks["bf16_tflops_sustained"],
                             "frac_bf16_spec": f / ms / 1e9 / SPEC_PEAKS["bf16_tflops"], "flops": f}
+        elif p == "attn_fp8":
+            breakdown[p] = hbm(ms, w._attn()["bytes"])
+            breakdown[p]["workload"] = (f"{ATT_B} sequences, {ATT_HQ} query / {ATT_HKV} KV heads of 128, "
+                                        f"E4M3 cache of {ATT_L // 2}..{ATT_L} tokens: append one step + attention")
         elif p == "lora_bwd":
             f = lora_bwd_flops(L, PREFILL_TOKENS, R)
             breakdown[p] = {"ms": ms, "TFLOP/s": f / ms / 1e9, "frac_bf16": f / ms / 1e9 / peaks["bf16_tflops"],

@@ -285,6 +285,38 @@ qrr_status qrr_lora_backward_nvfp4(const void* dy, int64_t M, int64_t N, const v
                                    void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* FP8 key/value cache and decode attention ("NVIDIA NeMo RL behaalt 48% ...",
+ * section "Praktische prestatiewinsten": FP8 extended to the KV cache and the
+ * attention operations; section "De technische doorbraak": 1x128 E4M3 blocks
+ * for activations).  Each cached row (one token, one KV head, head_dim 128)
+ * is E4M3 codes with one fp32 scale, quantized by the 1x128 rule of
+ * qrr_quantize_fp8_a1x128 (scale_mode as there).
+ * Layout: caches uint8 [B][Hkv][Lmax][128], scales fp32 [B][Hkv][Lmax];
+ * queries and outputs bf16 [B][Hq][128]; query head h reads KV head
+ * h / (Hq / Hkv).
+ *
+ * qrr_kv_append_fp8: quantizes one decode step's rows k_new, v_new (bf16
+ * [B][Hkv][128]) into slot pos[b] of sequence b (int32 [B]); a slot outside
+ * [0, Lmax) raises QRR_DEV_BAD_INDEX and writes nothing; a non-finite value
+ * raises QRR_DEV_NONFINITE.  k_new / v_new 8-byte aligned, caches 16-byte.
+ *
+ * qrr_attention_decode_fp8: o[b][h] = softmax(q[b][h] . K^T / sqrt(128)) . V
+ * over the first lens[b] cached tokens of sequence b (lens int32 [B], at most
+ * Lmax; 0 gives a zero row).  Hq / Hkv in {1, 2, 4, 8}; Lmax % 4 == 0.  The
+ * codes convert exactly; scores and sums are fp32, exponentials the base-2
+ * hardware approximation; the sequence is split in 256-token pieces whose
+ * partial results are merged in a fixed order.  Workspace:
+ * qrr_attention_decode_fp8_workspace_bytes(B, Hq, Lmax). */
+qrr_status qrr_kv_append_fp8(const void* k_new, const void* v_new, int32_t B, int32_t Hkv, const int32_t* pos,
+                             uint8_t* k_cache, float* k_scales, uint8_t* v_cache, float* v_scales, int32_t Lmax,
+                             int32_t scale_mode, int32_t* dev_status, void* stream);
+size_t qrr_attention_decode_fp8_workspace_bytes(int32_t B, int32_t Hq, int32_t Lmax);
+qrr_status qrr_attention_decode_fp8(const void* q, int32_t B, int32_t Hq, int32_t Hkv, const uint8_t* k_cache,
+                                    const float* k_scales, const uint8_t* v_cache, const float* v_scales,
+                                    const int32_t* lens, int32_t Lmax, void* out, void* workspace,
+                                    size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Token log-probabilities and token-level importance-sampling weights
  * ("NVIDIA NeMo RL behaalt 48% ...", the paragraph on importance sampling in
  * "Waarom dit belangrijk is voor AI-economie": the shift between the

@@ -665,6 +665,52 @@ static qrr_status requantize(const qrr_weight_desc* descs, int32_t count, int32_
   return QRR_OK;
 }
 
+qrr_status qrr_kv_append_fp8(const void* k_new, const void* v_new, int32_t B, int32_t Hkv, const int32_t* pos,
+                             uint8_t* k_cache, float* k_scales, uint8_t* v_cache, float* v_scales, int32_t Lmax,
+                             int32_t scale_mode, int32_t* dev_status, void* stream) {
+  if (B < 0 || Hkv < 0 || Lmax < 0 || !is_fp8_mode(scale_mode)) return QRR_ERR_INVALID_ARG;
+  if (B * Hkv > 0 && (!k_new || !v_new || !pos || !k_cache || !k_scales || !v_cache || !v_scales))
+    return QRR_ERR_INVALID_ARG;
+  auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  if ((reinterpret_cast<uintptr_t>(k_new) & 7u) || (reinterpret_cast<uintptr_t>(v_new) & 7u) || !a4(pos) ||
+      !aligned16(k_cache) || !aligned16(v_cache) || !a4(k_scales) || !a4(v_scales))
+    return QRR_ERR_MISALIGNED;
+  if (injected_cuda_fault()) return QRR_ERR_CUDA;
+  return from_cuda(launch_kv_append_fp8(k_new, v_new, B, Hkv, pos, Lmax, k_cache, k_scales, v_cache, v_scales,
+                                        scale_mode, dev_status, as_stream(stream)));
+}
+
+size_t qrr_attention_decode_fp8_workspace_bytes(int32_t B, int32_t Hq, int32_t Lmax) {
+  if (B < 0 || Hq < 0 || Lmax < 0) return 0;
+  return round_up(static_cast<size_t>(B) * Hq * attn_splits(Lmax) * (2 + 128) * 4) + kAlign;
+}
+
+qrr_status qrr_attention_decode_fp8(const void* q, int32_t B, int32_t Hq, int32_t Hkv, const uint8_t* k_cache,
+                                    const float* k_scales, const uint8_t* v_cache, const float* v_scales,
+                                    const int32_t* lens, int32_t Lmax, void* out, void* workspace,
+                                    size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (B < 0 || Hq < 0 || Hkv <= 0 || Lmax < 0) return QRR_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return QRR_ERR_UNSUPPORTED_SHAPE;
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return QRR_ERR_UNSUPPORTED_SHAPE;
+  if (Lmax % 4 != 0) return QRR_ERR_UNSUPPORTED_SHAPE;
+  if (B * Hq > 0 && (!q || !k_cache || !k_scales || !v_cache || !v_scales || !lens || !out)) return QRR_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(k_scales) || !aligned16(v_cache) || !aligned16(v_scales) ||
+      !aligned16(out) || (reinterpret_cast<uintptr_t>(lens) & 3u))
+    return QRR_ERR_MISALIGNED;
+  const size_t need = qrr_attention_decode_fp8_workspace_bytes(B, Hq, Lmax);
+  if (!workspace || workspace_bytes < need) return QRR_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return QRR_ERR_MISALIGNED;
+  if (injected_cuda_fault()) return QRR_ERR_CUDA;
+  const size_t rows = static_cast<size_t>(B) * Hq * attn_splits(Lmax);
+  float* pm = static_cast<float*>(workspace);
+  float* pl = pm + rows;
+  float* po = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round_up(rows * 8));
+  (void)pl;
+  return from_cuda(launch_attention_decode_fp8(q, k_cache, k_scales, v_cache, v_scales, lens, B, Hq, Hkv, Lmax, out,
+                                               pm, pm + rows, po, dev_status, as_stream(stream)));
+}
+
 qrr_status qrr_token_logprobs_is(const void* logits, int64_t T, int64_t V, const int32_t* tokens,
                                  const float* rollout_logp, float cap, float* logp, float* w, int32_t* dev_status,
                                  void* stream) {

@@ -1,0 +1,361 @@
+// Decode attention over an FP8 (E4M3) key/value cache, and the append of a
+// decode step's keys and values to that cache.
+//
+// ("NVIDIA NeMo RL behaalt 48% ...", section "Praktische prestatiewinsten":
+// FP8 extended to the KV cache and the attention operations; section "De
+// technische doorbraak": activations in 1x128 E4M3 blocks.)  Each cached key
+// or value row (one token, one KV head, 128 values) is E4M3 codes with one
+// fp32 scale, the 1x128 activation rule; query head h reads KV head
+// h / (Hq / Hkv); o = softmax(q . K^T / sqrt(128)) . V.
+//
+// Layout: caches [B][Hkv][Lmax][128] bytes, scales [B][Hkv][Lmax] fp32 (a
+// sequence's rows of one KV head are contiguous), q and o [B][Hq][128] bf16.
+//
+// Decode attention reads every cached byte once and does G = Hq / Hkv
+// multiply-adds per byte, so it is HBM-bound; it runs on the CUDA cores in
+// fp32 (the E4M3 codes convert exactly).  Split over the sequence: a CTA
+// takes 256 tokens of one (sequence, KV head), pulls their key and value rows
+// and scales into shared memory with four bulk copies, and writes a partial
+// (max, sum, unnormalized output) per query head of the group; a second
+// kernel merges the partials in split order.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "linear.cuh"
+#include "quant.cuh"
+#include "tc.cuh"
+
+namespace qrr {
+
+namespace {
+
+constexpr int D = 128;
+constexpr int TS = 256;  // tokens per CTA
+constexpr int kThreads = 128;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// four E4M3 bytes -> four fp32 (exact)
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float (&f)[4]) {
+  uint32_t lo, hi;
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  f[0] = a.x;
+  f[1] = a.y;
+  f[2] = b.x;
+  f[3] = b.y;
+}
+
+template <int G>
+struct AttnShared {
+  uint8_t k[TS * D];  // 32 KB
+  uint8_t v[TS * D];  // 32 KB
+  float ks[TS], vs[TS];
+  float p[TS][G];      // scores, then softmax numerators times the value row scale
+  float red[4][G];     // per-warp partial max / sum
+  uint64_t bar;
+  int abort;
+};
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Append one decode step's key and value rows: row (b, g) of k_new / v_new
+// (bf16 [B][Hkv][128]) is quantized by the 1x128 rule and written at slot
+// pos[b] of the caches.  One warp per row, lane = 4 values.
+__global__ void kv_append_fp8_kernel(const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new, int B,
+                                     int Hkv, const int32_t* __restrict__ pos, int Lmax, uint8_t* __restrict__ kc,
+                                     float* __restrict__ ksc, uint8_t* __restrict__ vc, float* __restrict__ vsc,
+                                     int mode, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);  // over 2 * B * Hkv
+  if (row >= 2 * B * Hkv) return;
+  const int kind = row / (B * Hkv), bg = row % (B * Hkv), b = bg / Hkv;
+  const int p = __ldg(pos + b);
+  if (p < 0 || p >= Lmax) {
+    if (lane == 0) flag(status, QRR_DEV_BAD_INDEX);
+    return;
+  }
+  const uint16_t* src = (kind ? v_new : k_new) + static_cast<int64_t>(bg) * D;
+  const uint2 w = __ldg(reinterpret_cast<const uint2*>(src) + lane);
+  uint32_t m = max(max(w.x & 0x7FFFu, w.x >> 16 & 0x7FFFu), max(w.y & 0x7FFFu, w.y >> 16 & 0x7FFFu));
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  if (m >= 0x7F80u && lane == 0) flag(status, QRR_DEV_NONFINITE);
+  const float v448 = __fdiv_rn(bf16bits_to_f32(m), 448.0f);
+  uint32_t out = 0u;
+  float s = 0.0f;
+  if (v448 > 0.0f) {
+    float a0, a1, a2, a3;
+    if (mode == QRR_SCALE_FP32) {
+      s = v448;
+      const SharedDivisor2 div(s);
+      div(bf16_lo(w.x), bf16_hi(w.x), a0, a1);
+      div(bf16_lo(w.y), bf16_hi(w.y), a2, a3);
+    } else {
+      const int e = pow2_ceil_exp(v448);
+      s = pow2_from_exp(e);
+      const Pow2Scaler sc(e);
+      a0 = sc(bf16_lo(w.x));
+      a1 = sc(bf16_hi(w.x));
+      a2 = sc(bf16_lo(w.y));
+      a3 = sc(bf16_hi(w.y));
+    }
+    out = cvt_e4m3x2(a0, a1) | (cvt_e4m3x2(a2, a3) << 16);
+  }
+  const int64_t slot = static_cast<int64_t>(bg) * Lmax + p;
+  reinterpret_cast<uint32_t*>((kind ? vc : kc) + slot * D)[lane] = out;
+  if (lane == 0) (kind ? vsc : ksc)[slot] = s;
+}
+
+// ---------------------------------------------------------------------------
+// Partial attention of one (sequence b, KV head g, split s) for the G query
+// heads of the group: part_m / part_l [.., G] (base-2 max, sum) and part_o
+// [.., G, 128] (unnormalized).
+template <int G>
+__global__ void __launch_bounds__(kThreads) attn_decode_fp8_kernel(
+    const uint16_t* __restrict__ q, const uint8_t* __restrict__ kc, const float* __restrict__ ksc,
+    const uint8_t* __restrict__ vc, const float* __restrict__ vsc, const int32_t* __restrict__ lens, int Hkv, int Lmax,
+    int splits, float* __restrict__ part_m, float* __restrict__ part_l, float* __restrict__ part_o,
+    int32_t* status) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  AttnShared<G>& sh = *reinterpret_cast<AttnShared<G>*>(smem_raw);
+  // q / sqrt(d) * log2(e) as [16-value piece][value][head], each piece's row
+  // padded by 4 words: the 8 pieces that the threads of a shared-memory phase
+  // read at once (see the rotated key reads below) sit on distinct banks
+  constexpr int QROW = 16 * G + 4;
+  __shared__ __align__(16) float qs[8][QROW];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int s = blockIdx.x % splits, bg = blockIdx.x / splits;
+  const int b = bg / Hkv, g = bg % Hkv;
+  const int len = min(__ldg(lens + b), Lmax);
+  const int t0 = s * TS;
+  const int n = min(TS, len - t0);  // tokens of this split (<= 0: nothing)
+  const int64_t pidx = static_cast<int64_t>(blockIdx.x) * G;
+  if (n <= 0) {
+    if (tid < G) {
+      part_m[pidx + tid] = -INFINITY;
+      part_l[pidx + tid] = 0.0f;
+    }
+    return;
+  }
+  const int nr = (n + 3) & ~3;  // bulk copies move multiples of 16 bytes of scales
+  const int64_t row0 = static_cast<int64_t>(bg) * Lmax + t0;
+  if (tid == 0) {
+    mbar_init(&sh.bar, 1);
+    sh.abort = 0;
+    fence_barrier_init();
+  }
+  // the group's queries, pre-scaled for base-2 exponentials
+  const float qscale = 0.08838834764831845f * kLog2e;  // 1 / sqrt(128) * log2(e)
+  for (int i = tid; i < G * D; i += kThreads) {
+    const int h = i / D, d = i % D;
+    const uint16_t qb = __ldg(q + (static_cast<int64_t>(b) * Hkv * G + g * G + h) * D + d);
+    qs[d >> 4][(d & 15) * G + h] = bf16bits_to_f32(qb) * qscale;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&sh.bar, 2 * n * D + 2 * nr * 4);
+    bulk_load(sh.k, kc + row0 * D, n * D, &sh.bar);
+    bulk_load(sh.v, vc + row0 * D, n * D, &sh.bar);
+    bulk_load(sh.ks, ksc + row0, nr * 4, &sh.bar);
+    bulk_load(sh.vs, vsc + row0, nr * 4, &sh.bar);
+  }
+  const bool ok = mbar_wait(&sh.bar, 0, &sh.abort, status);
+  // ---- scores: thread = token (two per thread), rows read in a rotated
+  // order of 16-byte pieces so the 8 threads of a shared-memory phase hit
+  // distinct banks
+  float mx[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) mx[h] = -INFINITY;
+  if (ok) {
+    for (int t = tid; t < n; t += kThreads) {
+      float acc[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) acc[h] = 0.0f;
+      const uint4* row = reinterpret_cast<const uint4*>(sh.k + t * D);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int piece = (i + t) & 7;
+        const uint4 w = row[piece];
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float f[4];
+          e4m3x4_to_f32(ws[e], f);
+          const float* qp = &qs[piece][(4 * e) * G];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int h = 0; h < G; ++h) acc[h] = fmaf(f[c], qp[c * G + h], acc[h]);
+        }
+      }
+      const float kscale = sh.ks[t];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float sc = acc[h] * kscale;
+        sh.p[t][h] = sc;
+        mx[h] = fmaxf(mx[h], sc);
+      }
+    }
+  }
+  // ---- softmax over the split's tokens (base 2)
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float v = mx[h];
+    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    if (lane == 0) sh.red[warp][h] = v;
+  }
+  __syncthreads();
+  float m[G], lsum[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m[h] = fmaxf(fmaxf(sh.red[0][h], sh.red[1][h]), fmaxf(sh.red[2][h], sh.red[3][h]));
+    lsum[h] = 0.0f;
+  }
+  __syncthreads();  // sh.red is reused for the sums
+  for (int t = tid; t < n; t += kThreads) {
+    const float vscale = sh.vs[t];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float pe = ex2f(sh.p[t][h] - m[h]);
+      lsum[h] += pe;
+      sh.p[t][h] = pe * vscale;
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float v = lsum[h];
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    if (lane == 0) sh.red[warp][h] = v;
+  }
+  __syncthreads();
+  // ---- p . V: warp w takes tokens w, w + 4, ...; lane = 4 values of d
+  float o[G][4];
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) o[h][c] = 0.0f;
+  if (ok) {
+    for (int t = warp; t < n; t += 4) {
+      float f[4];
+      e4m3x4_to_f32(reinterpret_cast<const uint32_t*>(sh.v + t * D)[lane], f);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float pw = sh.p[t][h];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[h][c] = fmaf(pw, f[c], o[h][c]);
+      }
+    }
+  }
+  // the four warps' partial outputs meet in shared memory (the key buffer is free now)
+  float* red_o = reinterpret_cast<float*>(sh.k);  // [4 warps][G][128]
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+    *reinterpret_cast<float4*>(red_o + (warp * G + h) * D + 4 * lane) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+  __syncthreads();
+  for (int i = tid; i < G * D; i += kThreads) {
+    const float acc = red_o[i] + red_o[G * D + i] + red_o[2 * G * D + i] + red_o[3 * G * D + i];
+    part_o[pidx * D + i] = acc;
+  }
+  if (tid < G) {
+    part_m[pidx + tid] = ok ? m[tid] : -INFINITY;
+    part_l[pidx + tid] = ok ? (sh.red[0][tid] + sh.red[1][tid] + sh.red[2][tid] + sh.red[3][tid]) : 0.0f;
+  }
+}
+
+// Merge the splits of every (sequence, query head) in split order: one warp
+// per output row, lane = 4 values.
+__global__ void attn_combine_kernel(const float* __restrict__ part_m, const float* __restrict__ part_l,
+                                    const float* __restrict__ part_o, int B, int Hkv, int G, int splits,
+                                    __nv_bfloat16* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);  // (b, h) over B * Hq
+  if (row >= B * Hkv * G) return;
+  const int bg = row / G, h = row % G;
+  float M = -INFINITY;
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, part_m[(static_cast<int64_t>(bg) * splits + s) * G + h]);
+  float L = 0.0f, acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (M > -INFINITY) {
+    for (int s = 0; s < splits; ++s) {
+      const int64_t pi = (static_cast<int64_t>(bg) * splits + s) * G + h;
+      const float ms = part_m[pi];
+      if (ms == -INFINITY) continue;
+      const float w = ex2f(ms - M);
+      L += w * part_l[pi];
+      const float4 v = *reinterpret_cast<const float4*>(part_o + pi * D + 4 * lane);
+      acc[0] += w * v.x;
+      acc[1] += w * v.y;
+      acc[2] += w * v.z;
+      acc[3] += w * v.w;
+    }
+  }
+  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+  const __nv_bfloat162 a = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+  const __nv_bfloat162 c = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+  uint2 w;
+  w.x = *reinterpret_cast<const uint32_t*>(&a);
+  w.y = *reinterpret_cast<const uint32_t*>(&c);
+  reinterpret_cast<uint2*>(out + static_cast<int64_t>(row) * D)[lane] = w;
+}
+
+int attn_splits(int Lmax) { return (Lmax + TS - 1) / TS; }
+
+cudaError_t launch_kv_append_fp8(const void* k_new, const void* v_new, int B, int Hkv, const int32_t* pos, int Lmax,
+                                 uint8_t* kc, float* ksc, uint8_t* vc, float* vsc, int mode, int32_t* status,
+                                 cudaStream_t stream) {
+  const int rows = 2 * B * Hkv;
+  if (rows == 0) return cudaSuccess;
+  kv_append_fp8_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(static_cast<const uint16_t*>(k_new),
+                                                           static_cast<const uint16_t*>(v_new), B, Hkv, pos, Lmax, kc,
+                                                           ksc, vc, vsc, mode, status);
+  return cudaGetLastError();
+}
+
+template <int G>
+static cudaError_t launch_attn_g(const void* q, const uint8_t* kc, const float* ksc, const uint8_t* vc,
+                                 const float* vsc, const int32_t* lens, int B, int Hkv, int Lmax, float* pm, float* pl,
+                                 float* po, int32_t* status, cudaStream_t stream) {
+  static bool attr = false;
+  const int smem = static_cast<int>(sizeof(AttnShared<G>));
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_fp8_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int splits = attn_splits(Lmax);
+  const unsigned grid = static_cast<unsigned>(B * Hkv * splits);
+  attn_decode_fp8_kernel<G><<<grid, kThreads, smem, stream>>>(static_cast<const uint16_t*>(q), kc, ksc, vc, vsc, lens,
+                                                             Hkv, Lmax, splits, pm, pl, po, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attention_decode_fp8(const void* q, const uint8_t* kc, const float* ksc, const uint8_t* vc,
+                                        const float* vsc, const int32_t* lens, int B, int Hq, int Hkv, int Lmax,
+                                        void* out, float* pm, float* pl, float* po, int32_t* status,
+                                        cudaStream_t stream) {
+  if (B == 0 || Hq == 0) return cudaSuccess;
+  const int G = Hq / Hkv;
+  cudaError_t e;
+  switch (G) {
+    case 1: e = launch_attn_g<1>(q, kc, ksc, vc, vsc, lens, B, Hkv, Lmax, pm, pl, po, status, stream); break;
+    case 2: e = launch_attn_g<2>(q, kc, ksc, vc, vsc, lens, B, Hkv, Lmax, pm, pl, po, status, stream); break;
+    case 4: e = launch_attn_g<4>(q, kc, ksc, vc, vsc, lens, B, Hkv, Lmax, pm, pl, po, status, stream); break;
+    default: e = launch_attn_g<8>(q, kc, ksc, vc, vsc, lens, B, Hkv, Lmax, pm, pl, po, status, stream); break;
+  }
+  if (e != cudaSuccess) return e;
+  const int rows = B * Hq;
+  attn_combine_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(pm, pl, po, B, Hkv, G, attn_splits(Lmax),
+                                                          static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace qrr

@@ -111,6 +111,16 @@ cudaError_t launch_lora_grad(const void* X, const uint16_t* tp, int M, int C, in
                              const float* tensor_scale, bool transposed, float* part, float* out,
                              cudaStream_t stream);
 
+// ---- FP8 key/value cache and decode attention (attention_fp8.cu) ----
+int attn_splits(int Lmax);
+cudaError_t launch_kv_append_fp8(const void* k_new, const void* v_new, int B, int Hkv, const int32_t* pos, int Lmax,
+                                 uint8_t* kc, float* ksc, uint8_t* vc, float* vsc, int mode, int32_t* status,
+                                 cudaStream_t stream);
+cudaError_t launch_attention_decode_fp8(const void* q, const uint8_t* kc, const float* ksc, const uint8_t* vc,
+                                        const float* vsc, const int32_t* lens, int B, int Hq, int Hkv, int Lmax,
+                                        void* out, float* pm, float* pl, float* po, int32_t* status,
+                                        cudaStream_t stream);
+
 // ---- token log-probabilities and importance-sampling weights (rollout_is.cu) ----
 cudaError_t launch_token_logprob_is(const void* logits, int64_t T, int64_t V, const int32_t* tokens,
                                     const float* rollout_logp, float cap, float* logp, float* w, int32_t* status,

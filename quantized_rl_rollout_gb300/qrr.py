@@ -76,6 +76,11 @@ SIGNATURES = {
                                               _c_p]),
     "qrr_round_probe": (ctypes.c_int, [_c_p, _c_i64, _c_i32, _c_p, _c_p]),
     "qrr_get_last_device_status": (ctypes.c_int, [_c_p, _c_p, _c_p]),
+    "qrr_kv_append_fp8": (ctypes.c_int, [_c_p, _c_p, _c_i32, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_i32, _c_p,
+                                         _c_p]),
+    "qrr_attention_decode_fp8_workspace_bytes": (_c_sz, [_c_i32, _c_i32, _c_i32]),
+    "qrr_attention_decode_fp8": (ctypes.c_int, [_c_p, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_p,
+                                                _c_p, _c_sz, _c_p, _c_p]),
     "qrr_lora_backward_workspace_bytes": (_c_sz, [_c_i64, _c_i64, _c_i64, _c_i32]),
     "qrr_lora_backward_nvfp4": (ctypes.c_int, [_c_p, _c_i64, _c_i64, _c_p, _c_i64, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i32,
                                                ctypes.c_float, _c_p, _c_p, _c_p, _c_p, _c_sz, _c_p, _c_p]),
@@ -390,3 +395,33 @@ def lora_backward_nvfp4(dy, x, codes, scales, tensor_scale, lora_A=None, lora_B=
                                          workspace.numel(), _ptr(dev_status), _stream(stream)),
            "qrr_lora_backward_nvfp4")
     return dx, (dA if r else None), (dB if r else None)
+
+
+def kv_append_fp8(k_new, v_new, pos, k_cache, k_scales, v_cache, v_scales, mode=SCALE_FP32, dev_status=None,
+                  stream=None):
+    """Quantize one decode step's key/value rows [B, Hkv, 128] into slot pos[b] of the FP8 caches."""
+    _need(k_new, torch.bfloat16, "k_new")
+    _need(v_new, torch.bfloat16, "v_new")
+    _need(pos, torch.int32, "pos")
+    b, hkv, _ = k_new.shape
+    lmax = k_cache.shape[2]
+    _check(lib().qrr_kv_append_fp8(_ptr(k_new), _ptr(v_new), b, hkv, _ptr(pos), _ptr(k_cache), _ptr(k_scales),
+                                   _ptr(v_cache), _ptr(v_scales), lmax, int(mode), _ptr(dev_status), _stream(stream)),
+           "qrr_kv_append_fp8")
+
+
+def attention_decode_fp8(q, k_cache, k_scales, v_cache, v_scales, lens, out=None, workspace=None, dev_status=None,
+                         stream=None):
+    """o [B, Hq, 128] bf16 of decode attention over the FP8 caches [B, Hkv, Lmax, 128]."""
+    _need(q, torch.bfloat16, "q")
+    _need(lens, torch.int32, "lens")
+    b, hq, _ = q.shape
+    hkv, lmax = k_cache.shape[1], k_cache.shape[2]
+    out = torch.empty_like(q) if out is None else out
+    if workspace is None:
+        workspace = _workspace(lib().qrr_attention_decode_fp8_workspace_bytes(b, hq, lmax), q.device)
+    _check(lib().qrr_attention_decode_fp8(_ptr(q), b, hq, hkv, _ptr(k_cache), _ptr(k_scales), _ptr(v_cache),
+                                          _ptr(v_scales), _ptr(lens), lmax, _ptr(out), _ptr(workspace),
+                                          workspace.numel(), _ptr(dev_status), _stream(stream)),
+           "qrr_attention_decode_fp8")
+    return out
