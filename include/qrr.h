@@ -389,11 +389,11 @@ qrr_status qrr_wait_probe(int64_t limit_cycles, int32_t arrive, int32_t* dev_sta
  *   W'[e] = bf16_rn(fp32(W[e]) + fp32(sigma * z[e]))
  * and W' is quantized exactly as qrr_requantize_weights would (same formats,
  * scale modes, workspace, grouping).  z[e] is a standardized sum of four
- * uniforms (mean 0, variance 1, within +-2 sqrt 3) drawn from Philox4x32-10
- * (Salmon et al., SC'11) at counter (e / 2 low word, e / 2 high word,
- * descriptor index j, step), key (seed low word, seed high word): the four
- * 16-bit halves k_i of words r0, r1 (even e) or r2, r3 (odd e) give
- * z = fp32((k1 + k2 + k3 + k4 - 131070) / 65536) * fp32(sqrt 3).  e is the
+ * uniforms (mean 0, variance about 1, within +-2 sqrt 3) drawn from
+ * Philox4x32-10 (Salmon et al., SC'11) at counter (e / 4 low word, e / 4 high
+ * word, descriptor index j, step), key (seed low word, seed high word): the
+ * four bytes k_i of output word r[e % 4] give
+ * z = fp32((k1 + k2 + k3 + k4 - 510) / 256) * fp32(sqrt 3).  e is the
  * element's row-major index in its tensor.  Every step is integer or one
  * correctly rounded fp32 operation, so the result is reproducible bit for bit.
  * The noise is regenerated from its counter in every pass: nothing noisy is

@@ -20,16 +20,16 @@ pages give neither the noise's form nor its schedule.  Readings taken:
   handed to the kernel as one fp32 number;
 * z is drawn per element from the counter-based generator Philox4x32-10
   (Salmon et al., "Parallel random numbers: as easy as 1, 2, 3", SC'11):
-  counter (e // 2 low word, e // 2 high word, tensor index j, step s), key
-  (seed low word, seed high word); element e takes output words (r0, r1)
-  when e is even, (r2, r3) when odd;
+  counter (e // 4 low word, e // 4 high word, tensor index j, step s), key
+  (seed low word, seed high word); element e takes output word r[e % 4];
 * z is the standardized sum of four uniforms (the Irwin-Hall
-  approximation of a normal variable, variance 1, support +-2 sqrt 3): the
-  four 16-bit halves k_i of the two words give
-  ``z = fp32((k1 + k2 + k3 + k4 - 131070) * 2^-16) * fp32(sqrt 3)``, each
-  uniform being (k_i + 1/2) / 65536.  It is chosen because every step is an
-  integer operation or a single correctly-rounded fp32 operation, so the
-  noise is reproducible bit for bit on any IEEE machine.
+  approximation of a normal variable, variance 65535/65536, support within
+  +-2 sqrt 3): the four bytes k_i of the word give
+  ``z = fp32((k1 + k2 + k3 + k4 - 510) * 2^-8) * fp32(sqrt 3)``, each uniform
+  being (k_i + 1/2) / 256.  It is chosen because every step is an integer
+  operation or a single correctly-rounded fp32 operation, so the noise is
+  reproducible bit for bit on any IEEE machine, and one generator call
+  serves four elements.
 """
 
 import numpy as np
@@ -63,14 +63,13 @@ def philox4x32_10(c0, c1, c2, c3, k0, k1):
 def noise(n: int, seed: int, tensor: int, step: int, start: int = 0) -> np.ndarray:
     """z for elements start .. start + n - 1 of a tensor (float32)."""
     e = np.arange(start, start + n, dtype=np.uint64)
-    pair = e >> np.uint64(1)
-    r = philox4x32_10(pair & MASK, pair >> np.uint64(32), np.full_like(pair, tensor), np.full_like(pair, step),
+    quad = e >> np.uint64(2)
+    r = philox4x32_10(quad & MASK, quad >> np.uint64(32), np.full_like(quad, tensor), np.full_like(quad, step),
                       np.uint64(seed) & MASK, np.uint64(seed) >> np.uint64(32))
-    odd = (e & np.uint64(1)).astype(bool)
-    a = np.where(odd, r[2], r[0]).astype(np.int64)
-    b = np.where(odd, r[3], r[1]).astype(np.int64)
-    ksum = (a & 0xFFFF) + (a >> 16) + (b & 0xFFFF) + (b >> 16)
-    zc = ((ksum - 131070).astype(np.float32) * np.float32(2.0 ** -16)).astype(np.float32)  # exact
+    sel = (e & np.uint64(3)).astype(np.int64)
+    w = np.choose(sel, r).astype(np.int64)
+    ksum = (w & 0xFF) + ((w >> 8) & 0xFF) + ((w >> 16) & 0xFF) + (w >> 24)
+    zc = ((ksum - 510).astype(np.float32) * np.float32(2.0 ** -8)).astype(np.float32)  # exact
     return (zc * SQRT3).astype(np.float32)
 
 

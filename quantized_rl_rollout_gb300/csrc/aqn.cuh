@@ -5,15 +5,15 @@
 // Learning for LLMs", Abstract) adds noise to the quantized policy whose
 // strength changes during training.  Here element e of tensor j at training
 // step s gets
-//   z = sqrt(3) (k1 + k2 + k3 + k4 - 131070) / 65536
-// from the four 16-bit halves k_i of two output words of Philox4x32-10
+//   z = sqrt(3) (k1 + k2 + k3 + k4 - 510) / 256
+// from the four bytes k_i of output word r[e % 4] of Philox4x32-10
 // (J. K. Salmon et al., "Parallel random numbers: as easy as 1, 2, 3",
-// SC'11) at counter (e / 2 low, e / 2 high, j, s), key (seed low, seed high)
-// -- words r0, r1 for even e, r2, r3 for odd e -- and the master becomes
+// SC'11) at counter (e / 4 low, e / 4 high, j, s), key (seed low, seed
+// high), and the master becomes
 //   W' = bf16_rn(fp32(W) + fp32(sigma z)).
 // Every step is an integer operation or one correctly rounded fp32 operation
 // (no contraction into an FMA), so the noise and W' are reproducible bit for
-// bit on any IEEE machine.
+// bit on any IEEE machine; one generator call serves four elements.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -31,8 +31,9 @@ __device__ __forceinline__ void philox4x32_10(uint32_t c0, uint32_t c1, uint32_t
                                               uint32_t k1, uint32_t (&r)[4]) {
 #pragma unroll
   for (int i = 0; i < 10; ++i) {
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c0, p1 = static_cast<uint64_t>(0xCD9E8D57u) * c2;
+    const uint32_t hi0 = static_cast<uint32_t>(p0 >> 32), lo0 = static_cast<uint32_t>(p0);
+    const uint32_t hi1 = static_cast<uint32_t>(p1 >> 32), lo1 = static_cast<uint32_t>(p1);
     const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
     c0 = n0;
     c1 = lo1;
@@ -47,20 +48,17 @@ __device__ __forceinline__ void philox4x32_10(uint32_t c0, uint32_t c1, uint32_t
   r[3] = c3;
 }
 
-// The standardized sum of the four 16-bit halves of two words.
-__device__ __forceinline__ float aqn_z(uint32_t a, uint32_t b) {
-  const int centred = static_cast<int>((a & 0xFFFFu) + (a >> 16) + (b & 0xFFFFu) + (b >> 16)) - 131070;
-  const float zc = __fmul_rn(__int2float_rn(centred), 0x1p-16f);  // exact
+// The standardized sum of the four bytes of a word.
+__device__ __forceinline__ float aqn_z(uint32_t w) {
+  const int centred = static_cast<int>((w & 0xFFu) + ((w >> 8) & 0xFFu) + ((w >> 16) & 0xFFu) + (w >> 24)) - 510;
+  const float zc = __fmul_rn(__int2float_rn(centred), 0x1p-8f);  // exact
   return __fmul_rn(zc, 1.7320508075688772f);
 }
 
-// z of elements 2 p and 2 p + 1 of tensor `tensor`.
-__device__ __forceinline__ void aqn_z2(uint64_t p, uint32_t tensor, const AqnParams& a, float& z0, float& z1) {
-  uint32_t r[4];
-  philox4x32_10(static_cast<uint32_t>(p), static_cast<uint32_t>(p >> 32), tensor, a.step,
+// The four generator words of elements 4 c .. 4 c + 3 of tensor `tensor`.
+__device__ __forceinline__ void aqn_words(uint64_t c, uint32_t tensor, const AqnParams& a, uint32_t (&r)[4]) {
+  philox4x32_10(static_cast<uint32_t>(c), static_cast<uint32_t>(c >> 32), tensor, a.step,
                 static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32), r);
-  z0 = aqn_z(r[0], r[1]);
-  z1 = aqn_z(r[2], r[3]);
 }
 
 // bf16 bits of bf16_rn(fp32(w) + fp32(sigma z)).
@@ -69,18 +67,20 @@ __device__ __forceinline__ uint32_t aqn_noisy(uint32_t wbits, float sigma, float
   return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(s)));
 }
 
-// The packed pair of bf16 values in `w` (elements 2 p, 2 p + 1), made noisy.
-__device__ __forceinline__ uint32_t aqn_noisy2(uint32_t w, uint64_t p, uint32_t tensor, const AqnParams& a) {
-  float z0, z1;
-  aqn_z2(p, tensor, a, z0, z1);
-  return aqn_noisy(w & 0xFFFFu, a.sigma, z0) | (aqn_noisy(w >> 16, a.sigma, z1) << 16);
-}
-
-// Eight consecutive bf16 values starting at element e0 (even).
+// Eight consecutive bf16 values starting at element e0 (a multiple of 8):
+// two generator calls.
 __device__ __forceinline__ uint4 aqn_noisy8(uint4 v, uint64_t e0, uint32_t tensor, const AqnParams& a) {
-  const uint64_t p = e0 >> 1;
-  return make_uint4(aqn_noisy2(v.x, p, tensor, a), aqn_noisy2(v.y, p + 1, tensor, a), aqn_noisy2(v.z, p + 2, tensor, a),
-                    aqn_noisy2(v.w, p + 3, tensor, a));
+  uint32_t r0[4], r1[4];
+  aqn_words(e0 >> 2, tensor, a, r0);
+  aqn_words((e0 >> 2) + 1, tensor, a, r1);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t za = i < 2 ? r0[2 * i] : r1[2 * i - 4], zb = i < 2 ? r0[2 * i + 1] : r1[2 * i - 3];
+    o[i] = aqn_noisy(w[i] & 0xFFFFu, a.sigma, aqn_z(za)) | (aqn_noisy(w[i] >> 16, a.sigma, aqn_z(zb)) << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 }  // namespace qrr

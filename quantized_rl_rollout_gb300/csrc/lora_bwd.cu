@@ -100,18 +100,25 @@ __global__ void lora_factor_transpose_kernel(const uint16_t* __restrict__ A, con
 // Adapter gradient partials: for one slice of tokens [m0, m0 + mlen),
 //   part[s][j][c] = sum_m X[m][c] (hi + lo)(tp[m][2j], tp[m][2j + 1])
 // X bf16 [M][C]; tp the (high, low) bf16 pairs [M][t_cols].  CTA: 128
-// columns x all r ranks; thread = (column, every other rank).
+// columns x all r ranks, staged 32 tokens at a time in shared memory; each
+// thread keeps a register tile of 4 columns x 4 ranks (x 2 for r > 32), so
+// every pair of 16-byte shared loads feeds 16 (or 32) FMAs.
 __global__ void __launch_bounds__(256) lora_grad_partial_kernel(const uint16_t* __restrict__ X,
                                                                 const uint16_t* __restrict__ tp, int M, int C, int r,
                                                                 int t_cols, int m_per_slice, float* __restrict__ part) {
-  __shared__ float xs[32][128];
-  __shared__ float us[32][64];
+  __shared__ __align__(16) float xs[32][128];
+  __shared__ __align__(16) float us[32][64];
   const int c0 = blockIdx.x * 128, s = blockIdx.y;
   const int m_begin = s * m_per_slice, m_end = min(M, m_begin + m_per_slice);
-  const int cl = threadIdx.x & 127, jh = threadIdx.x >> 7;
-  float acc[32];
+  const int cg = threadIdx.x & 31, jg = threadIdx.x >> 5;  // columns 4 cg .. 4 cg + 3; ranks 4 jg .. 4 jg + 3 (+ 32)
+  const int halves = r > 32 ? 2 : 1;
+  float acc[2][4][4];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[h][a][b] = 0.0f;
   for (int mb = m_begin; mb < m_end; mb += 32) {
     const int mn = min(32, m_end - mb);
     // x chunk: 32 rows x 128 bf16 (16 vectors of 8 per row)
@@ -127,10 +134,10 @@ __global__ void __launch_bounds__(256) lora_grad_partial_kernel(const uint16_t* 
           v[2 * e + 1] = bf16_hi(w[e]);
         }
       }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) xs[rr][8 * seg + e] = v[e];
+      *reinterpret_cast<float4*>(&xs[rr][8 * seg]) = make_float4(v[0], v[1], v[2], v[3]);
+      *reinterpret_cast<float4*>(&xs[rr][8 * seg + 4]) = make_float4(v[4], v[5], v[6], v[7]);
     }
-    // rank projections: 32 rows x r values (hi + lo)
+    // rank projections: 32 rows x r values (hi + lo), zero past r
     for (int idx = threadIdx.x; idx < 32 * 64; idx += 256) {
       const int rr = idx >> 6, j = idx & 63;
       float u = 0.0f;
@@ -142,17 +149,31 @@ __global__ void __launch_bounds__(256) lora_grad_partial_kernel(const uint16_t* 
     }
     __syncthreads();
     for (int mm = 0; mm < mn; ++mm) {
-      const float x = xs[mm][cl];
+      const float4 x4 = *reinterpret_cast<const float4*>(&xs[mm][4 * cg]);
+      const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (jh + 2 * i < r) acc[i] = fmaf(x, us[mm][jh + 2 * i], acc[i]);
+      for (int h = 0; h < 2; ++h) {
+        if (h < halves) {
+          const float4 u4 = *reinterpret_cast<const float4*>(&us[mm][32 * h + 4 * jg]);
+          const float uv[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) acc[h][a][b] = fmaf(xv[a], uv[b], acc[h][a][b]);
+        }
+      }
     }
     __syncthreads();
   }
-  if (c0 + cl < C)
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (jh + 2 * i < r) part[(static_cast<int64_t>(s) * r + jh + 2 * i) * C + c0 + cl] = acc[i];
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int j = 32 * h + 4 * jg + b;
+      if (h < halves && j < r && c0 + 4 * cg < C)
+        *reinterpret_cast<float4*>(part + (static_cast<int64_t>(s) * r + j) * C + c0 + 4 * cg) =
+            make_float4(acc[h][0][b], acc[h][1][b], acc[h][2][b], acc[h][3][b]);
+    }
 }
 
 // out = g * sum over slices (in slice order) of part[s][j][c]; layout

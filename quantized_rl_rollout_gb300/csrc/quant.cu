@@ -488,9 +488,9 @@ __global__ void aqn_noise_probe_kernel(float* __restrict__ out, int64_t n, int64
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t e = start + i;
-    float z0, z1;
-    aqn_z2(static_cast<uint64_t>(e) >> 1, tensor, a, z0, z1);
-    out[i] = (e & 1) ? z1 : z0;
+    uint32_t r[4];
+    aqn_words(static_cast<uint64_t>(e) >> 2, tensor, a, r);
+    out[i] = aqn_z(r[e & 3]);
   }
 }
 
