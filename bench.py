@@ -371,12 +371,6 @@ class Workload:
         self.f8a = [(torch.empty(PREFILL_TOKENS, l.k, dtype=torch.uint8, device=device),
                      torch.empty(PREFILL_TOKENS, l.k // 128, dtype=torch.float32, device=device)) for l in L]
         self.yf = [torch.empty(PREFILL_TOKENS, l.n, dtype=torch.bfloat16, device=device) for l in L]
-        # token log-probabilities / importance weights over an 8B-class vocabulary
-        self.lg = inputs.logits(IS_TOKENS, IS_VOCAB, inputs.derive_seed(seed, "is", "logits"), device=device)
-        self.tok = inputs.sampled_tokens(self.lg, inputs.derive_seed(seed, "is", "tokens"))
-        self.rlp = inputs.jitter(torch.full((IS_TOKENS,), -2.0, device=device), inputs.derive_seed(seed, "is", "r"), 1.0)
-        self.lp = torch.empty(IS_TOKENS, dtype=torch.float32, device=device)
-        self.iw = torch.empty(IS_TOKENS, dtype=torch.float32, device=device)
         # power-of-two-scale operands for the native block-scaled GEMM
         self.f8w2 = [qrr.quantize_fp8_w128x128(w, qrr.SCALE_POW2) for w in self.W]
         self.f8a2 = [qrr.quantize_fp8_a1x128(x, qrr.SCALE_POW2) for x in self.xp]
@@ -496,6 +490,14 @@ class Workload:
         return 3
 
     def rollout_is(self):
+        if getattr(self, "lg", None) is None:
+            # token log-probabilities / importance weights over an 8B-class vocabulary
+            self.lg = inputs.logits(IS_TOKENS, IS_VOCAB, inputs.derive_seed(0, "is", "logits"), device=self.dev)
+            self.tok = inputs.sampled_tokens(self.lg, inputs.derive_seed(0, "is", "tokens"))
+            self.rlp = inputs.jitter(torch.full((IS_TOKENS,), -2.0, device=self.dev), inputs.derive_seed(0, "is", "r"),
+                                     1.0)
+            self.lp = torch.empty(IS_TOKENS, dtype=torch.float32, device=self.dev)
+            self.iw = torch.empty(IS_TOKENS, dtype=torch.float32, device=self.dev)
         self.q.token_logprobs_is(self.lg, self.tok, self.rlp, IS_CAP, logp=self.lp, w=self.iw)
         return 1
 

@@ -48,11 +48,15 @@ __device__ __forceinline__ void philox4x32_10(uint32_t c0, uint32_t c1, uint32_t
   r[3] = c3;
 }
 
-// The standardized sum of the four bytes of a word.
+// The standardized sum of the four bytes of a word: one dot-product
+// instruction sums the bytes, an add to 2^23 turns the sum into an fp32
+// integer exactly, and (sum - 510) is scaled by fp32(sqrt 3) 2^-8 in one
+// correctly rounded multiply -- bit for bit fp32(sqrt 3) times the exact
+// (sum - 510) 2^-8, as scaling by a power of two commutes with rounding.
 __device__ __forceinline__ float aqn_z(uint32_t w) {
-  const int centred = static_cast<int>((w & 0xFFu) + ((w >> 8) & 0xFFu) + ((w >> 16) & 0xFFu) + (w >> 24)) - 510;
-  const float zc = __fmul_rn(__int2float_rn(centred), 0x1p-8f);  // exact
-  return __fmul_rn(zc, 1.7320508075688772f);
+  const uint32_t sum = __dp4a(w, 0x01010101u, 0u);                          // 0 .. 1020
+  const float f = __fsub_rn(__uint_as_float(0x4B000000u | sum), 8388608.0f);  // = sum, exactly
+  return __fmul_rn(__fsub_rn(f, 510.0f), 1.7320508075688772f * 0x1p-8f);
 }
 
 // The four generator words of elements 4 c .. 4 c + 3 of tensor `tensor`.

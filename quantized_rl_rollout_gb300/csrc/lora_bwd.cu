@@ -195,7 +195,7 @@ __global__ void lora_grad_reduce_kernel(const float* __restrict__ part, int slic
 
 int lora_grad_slices(int64_t M, int64_t C) {
   const int64_t col_ctas = (C + 127) / 128;
-  int64_t s = (2 * kSMs + col_ctas - 1) / col_ctas;  // about two waves of CTAs
+  int64_t s = (8 * kSMs + col_ctas - 1) / col_ctas;  // about eight CTAs per SM: their loads cover each other's latency
   s = s < (M + 31) / 32 ? s : (M + 31) / 32;
   return static_cast<int>(s < 1 ? 1 : s);
 }
