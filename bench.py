@@ -545,10 +545,13 @@ class Workload:
         return 2 * len(groups)
 
 
-# one step over the 8B-class workload; the 32B-class stack (another
-# configuration, ~85 GB resident) is timed after it, in a region of its own
-PHASES = ["requant", "requant_aqn", "decode_m1", "decode_m8", "decode_m64", "prefill", "lora_bwd", "fp8_requant",
-          "fp8_act_quant", "fp8_gemm", "fp8_gemm_pow2", "attn_fp8", "rollout_is"]
+# one step over the 8B-class workload (the hot path's method steps); the
+# 32B-class stack (another configuration, ~85 GB resident) and the next rows
+# built beside the path (AQN re-quantization, LoRA backward, FP8-KV attention,
+# importance weights) are timed after it, each in a region of its own
+PHASES = ["requant", "decode_m1", "decode_m8", "decode_m64", "prefill", "fp8_requant", "fp8_act_quant", "fp8_gemm",
+          "fp8_gemm_pow2"]
+NEXT_PHASES = ["requant_aqn", "lora_bwd", "attn_fp8", "rollout_is"]
 EXTRA_PHASES = ["requant32b", "decode32b"]
 
 
@@ -835,10 +838,13 @@ def main():
     qrr.lib()
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    phases = [p for p in args.phases.split(",") if p and p not in EXTRA_PHASES]
-    extra = [p for p in args.phases.split(",") if p in EXTRA_PHASES]
-    if not args.no_32b:
-        extra = extra or list(EXTRA_PHASES)
+    asked = [p for p in args.phases.split(",") if p]
+    phases = [p for p in asked if p in PHASES]
+    nxt = [p for p in asked if p in NEXT_PHASES]
+    extra = [p for p in asked if p in EXTRA_PHASES]
+    if args.phases == ",".join(PHASES):  # the default: every region
+        nxt = list(NEXT_PHASES)
+        extra = [] if args.no_32b else list(EXTRA_PHASES)
     peaks = load_peaks()
     fp8_meas = measure_fp8_peak(device)
     w = Workload(qrr, device)
@@ -863,8 +869,21 @@ def main():
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
 
+    # the next rows beside the path: a region of their own after the step
+    # (same protocol: warm-up, L2 flush before every phase)
+    per_next, clk_next = {}, None
+    if nxt:
+        for _ in range(warmup):
+            for p in nxt:
+                run_phase(w, p)
+        torch.cuda.synchronize()
+        clocks_n = Clocks(local)
+        clocks_n.start()
+        per_next, l_next = timed_steps(w, args.steps, nxt)
+        torch.cuda.synchronize()
+        clk_next = clocks_n.stop()
+
     # the 32B-class stack: another configuration, timed in a region of its own
-    # after the step (same protocol: warm-up, L2 flush before every phase)
     per_extra, clk32, wall32 = {}, None, None
     if extra:
         for p in extra:  # builds the stack on first use
@@ -883,6 +902,7 @@ def main():
 
     med = {p: statistics.median(v) for p, v in per_phase.items()}
     med_extra = {p: statistics.median(v) for p, v in per_extra.items()}
+    med_extra.update({p: statistics.median(v) for p, v in per_next.items()})
     L = configs.LAYERS_8B
     fp8_peak = fp8_meas if fp8_meas else 2.0 * peaks["bf16_tflops"]
     fp8_peak_source = "measured in this run (torch._scaled_mm E4M3 8192^3, best of 10)" if fp8_meas else \
@@ -938,6 +958,8 @@ def main():
             breakdown[p] = hbm(ms, configs.DECODE_32B["depth"] * requant_nvfp4_bytes(configs.LAYERS_32B))
             breakdown[p]["region"] = "separate (after the step)"
 
+    for p in per_next:
+        breakdown[p]["region"] = "separate (after the step)"
     step_ms = sum(med.values())
     step_ms = max_over_ranks(dist, step_ms)
     value = whole_job(dist, world, dec_bytes, dec_ms) if dec_ms else None
@@ -984,9 +1006,10 @@ def main():
                 "vs_baseline": None, "dtype": "nvfp4xbf16", "data": "synthetic",
                 "config": {"workload": WORKLOAD, "phases": phases, "l2": "flushed (512 MB write) before every phase",
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                           "separately_timed": extra},
+                           "separately_timed": nxt + extra},
                 "roofline": roof, "breakdown": breakdown, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": launches, "clocks": clk, "clocks_32b_region": clk32, "wall_s_timed": wall,
+                "gpu_launches": launches, "clocks": clk, "clocks_next_region": clk_next, "clocks_32b_region": clk32,
+                "wall_s_timed": wall,
                 "wall_s_timed_32b": wall32,
                 "peaks": dict(peaks, fp8_tflops=fp8_peak, fp8_source=fp8_peak_source, spec=SPEC_PEAKS)}
         print(json.dumps(line))

@@ -19,8 +19,9 @@
 //      tensor cores (the forward's LoRA-down kernel), as (high, low) pairs;
 //   3. dX = g (dY . W_q + u' . A) on the tensor cores (gemm_bf16_tc.cu);
 //   4. dA[j, k] = g sum_m u'[m, j] x[m, k] and dB[n, j] = g sum_m dY[m, n] t'[m, j]
-//      on the CUDA cores in fp32: token slices in parallel, partials summed
-//      in slice order, so the result does not depend on timing.
+//      on the tensor cores, with x, dY and the projections read as MN-major
+//      operands (no transposes): token slices in parallel, fp32 partials
+//      summed in slice order, so the result does not depend on timing.
 #include <cuda_bf16.h>
 
 #include "linear.cuh"
@@ -97,83 +98,131 @@ __global__ void lora_factor_transpose_kernel(const uint16_t* __restrict__ A, con
   }
 }
 
-// Adapter gradient partials: for one slice of tokens [m0, m0 + mlen),
+// Adapter gradient partials on the tensor cores: for one slice of tokens
 //   part[s][j][c] = sum_m X[m][c] (hi + lo)(tp[m][2j], tp[m][2j + 1])
-// X bf16 [M][C]; tp the (high, low) bf16 pairs [M][t_cols].  CTA: 128
-// columns x all r ranks, staged 32 tokens at a time in shared memory; each
-// thread keeps a register tile of 4 columns x 4 ranks (x 2 for r > 32), so
-// every pair of 16-byte shared loads feeds 16 (or 32) FMAs.
-__global__ void __launch_bounds__(256) lora_grad_partial_kernel(const uint16_t* __restrict__ X,
-                                                                const uint16_t* __restrict__ tp, int M, int C, int r,
-                                                                int t_cols, int m_per_slice, float* __restrict__ part) {
-  __shared__ __align__(16) float xs[32][128];
-  __shared__ __align__(16) float us[32][64];
+// as D[c][c'] = sum_m X[m][c] tp[m][c'] (M = 128 columns c of X, N = t_cols
+// columns of tp, K = the slice's tokens), then column pairs summed.  X and tp
+// are token-major in memory, i.e. MN-major operands: TMA stages 64-token
+// boxes of 64 columns (128-byte swizzle) and the MMA reads them through
+// MN-major descriptors, so nothing is transposed.
+//   warp 0  TMA: per 64-token stage, X [64 x 128] (two boxes) and tp [64 x t_cols]
+//   warp 1  MMA: 4 x tcgen05.mma kind::f16 (M128 N t_cols K16), A and B MN-major
+//   warps 2..5  the 128 x t_cols accumulator out of TMEM, pairs summed, stored
+namespace {
+constexpr int kGStages = 4;
+constexpr int kGA = 2 * 64 * 128;      // X stage: 2 boxes of 64 tokens x 64 columns (bf16)
+constexpr int kGB = 2 * 64 * 128;      // tp stage: up to 2 boxes
+constexpr int kGStage = kGA + kGB;     // 32 KB
+constexpr size_t kGSmem = 1024 + kGStages * kGStage + 256;
+}  // namespace
+
+struct GradTcParams {
+  CUtensorMap tx;  // X [M][C] bf16, box 64 x 64
+  CUtensorMap tt;  // tp [M][t_cols] bf16, box 64 x 64
+  float* part;
+  int M, C, r, t_cols, m_per_slice;
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(192, 1) lora_grad_tc_kernel(const __grid_constant__ GradTcParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  struct Ctl {
+    uint64_t full[kGStages], empty[kGStages], d_full;
+    uint32_t tmem;
+    int abort;
+  };
+  Ctl& sh = *reinterpret_cast<Ctl*>(tiles + kGStages * kGStage);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c0 = blockIdx.x * 128, s = blockIdx.y;
-  const int m_begin = s * m_per_slice, m_end = min(M, m_begin + m_per_slice);
-  const int cg = threadIdx.x & 31, jg = threadIdx.x >> 5;  // columns 4 cg .. 4 cg + 3; ranks 4 jg .. 4 jg + 3 (+ 32)
-  const int halves = r > 32 ? 2 : 1;
-  float acc[2][4][4];
-#pragma unroll
-  for (int h = 0; h < 2; ++h)
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) acc[h][a][b] = 0.0f;
-  for (int mb = m_begin; mb < m_end; mb += 32) {
-    const int mn = min(32, m_end - mb);
-    // x chunk: 32 rows x 128 bf16 (16 vectors of 8 per row)
-    for (int idx = threadIdx.x; idx < 32 * 16; idx += 256) {
-      const int rr = idx >> 4, seg = idx & 15;
-      float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      if (rr < mn && c0 + 8 * seg < C) {
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(X + static_cast<int64_t>(mb + rr) * C + c0) + seg);
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          v[2 * e] = bf16_lo(w[e]);
-          v[2 * e + 1] = bf16_hi(w[e]);
-        }
-      }
-      *reinterpret_cast<float4*>(&xs[rr][8 * seg]) = make_float4(v[0], v[1], v[2], v[3]);
-      *reinterpret_cast<float4*>(&xs[rr][8 * seg + 4]) = make_float4(v[4], v[5], v[6], v[7]);
+  const int m_begin = s * p.m_per_slice, m_end = min(p.M, m_begin + p.m_per_slice);
+  const int steps = m_end > m_begin ? (m_end - m_begin + 63) / 64 : 0;
+  const int nb = p.t_cols / 64;  // tp boxes per stage
+  volatile int* abort = &sh.abort;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kGStages; ++i) {
+      mbar_init(&sh.full[i], 1);
+      mbar_init(&sh.empty[i], 1);
     }
-    // rank projections: 32 rows x r values (hi + lo), zero past r
-    for (int idx = threadIdx.x; idx < 32 * 64; idx += 256) {
-      const int rr = idx >> 6, j = idx & 63;
-      float u = 0.0f;
-      if (rr < mn && j < r) {
-        const uint32_t pw = __ldg(reinterpret_cast<const uint32_t*>(tp + static_cast<int64_t>(mb + rr) * t_cols) + j);
-        u = bf16_lo(pw) + bf16_hi(pw);
-      }
-      us[rr][j] = u;
-    }
-    __syncthreads();
-    for (int mm = 0; mm < mn; ++mm) {
-      const float4 x4 = *reinterpret_cast<const float4*>(&xs[mm][4 * cg]);
-      const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (h < halves) {
-          const float4 u4 = *reinterpret_cast<const float4*>(&us[mm][32 * h + 4 * jg]);
-          const float uv[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-          for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) acc[h][a][b] = fmaf(xv[a], uv[b], acc[h][a][b]);
-        }
-      }
-    }
-    __syncthreads();
+    mbar_init(&sh.d_full, 1);
+    sh.abort = 0;
+    fence_barrier_init();
   }
-#pragma unroll
-  for (int h = 0; h < 2; ++h)
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const int j = 32 * h + 4 * jg + b;
-      if (h < halves && j < r && c0 + 4 * cg < C)
-        *reinterpret_cast<float4*>(part + (static_cast<int64_t>(s) * r + j) * C + c0 + 4 * cg) =
-            make_float4(acc[h][0][b], acc[h][1][b], acc[h][2][b], acc[h][3][b]);
+  if (warp == 1) tmem_alloc(&sh.tmem, 128);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem;
+  if (warp == 0) {
+    if (elect_one()) {
+      int issued = 0;
+      for (int k = 0; k < steps; ++k) {
+        const int st = k % kGStages, use = k / kGStages;
+        if (use > 0 && !mbar_wait(&sh.empty[st], (use - 1) & 1, abort, p.status)) break;
+        uint8_t* a = tiles + st * kGStage;
+        const int m = m_begin + 64 * k;
+        mbar_arrive_expect_tx(&sh.full[st], kGA + nb * 8192);
+        tma_load_2d(&p.tx, &sh.full[st], a, c0, m);
+        tma_load_2d(&p.tx, &sh.full[st], a + 8192, c0 + 64, m);
+        for (int b = 0; b < nb; ++b) tma_load_2d(&p.tt, &sh.full[st], a + kGA + 8192 * b, 64 * b, m);
+        issued = k + 1;
+      }
+      volatile int no_abort = 0;
+      for (int k = issued - 1; k >= 0 && k >= issued - kGStages; --k)
+        mbar_wait(&sh.full[k % kGStages], (k / kGStages) & 1, &no_abort, p.status);
     }
+  } else if (warp == 1) {
+    if (elect_one()) {
+      const uint32_t idesc = make_idesc_major(kFmtBF16, kFmtBF16, 128, static_cast<uint32_t>(p.t_cols), true, true);
+      bool ok = true;
+      for (int k = 0; k < steps; ++k) {
+        const int st = k % kGStages;
+        if (!mbar_wait(&sh.full[st], (k / kGStages) & 1, abort, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a = smem_u32(tiles + st * kGStage), b = a + kGA;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ss(tmem, sw128_mn_desc(a + 2048 * kk, 8192), sw128_mn_desc(b + 2048 * kk, 8192), idesc,
+                      (k > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&sh.empty[st]);
+      }
+      mma_commit(&sh.d_full);
+      volatile int no_abort = 0;
+      if (!ok) mbar_wait(&sh.d_full, 0, &no_abort, p.status);
+    }
+  } else {
+    const int q = warp & 3;
+    const int c = c0 + 32 * q + lane;
+    const bool ok = steps > 0 && mbar_wait(&sh.d_full, 0, abort, p.status) && !*abort;
+    tc_fence_after();
+    for (int cb = 0; cb < p.t_cols; cb += 32) {
+      uint32_t v[32];
+      if (ok) {
+        tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + cb, v);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0u;  // an empty slice adds nothing
+      }
+      if (c < p.C)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int j = cb / 2 + i;
+          if (j < p.r)
+            p.part[(static_cast<int64_t>(s) * p.r + j) * p.C + c] =
+                __uint_as_float(v[2 * i]) + __uint_as_float(v[2 * i + 1]);
+        }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
 }
 
 // out = g * sum over slices (in slice order) of part[s][j][c]; layout
@@ -195,8 +244,8 @@ __global__ void lora_grad_reduce_kernel(const float* __restrict__ part, int slic
 
 int lora_grad_slices(int64_t M, int64_t C) {
   const int64_t col_ctas = (C + 127) / 128;
-  int64_t s = (8 * kSMs + col_ctas - 1) / col_ctas;  // about eight CTAs per SM: their loads cover each other's latency
-  s = s < (M + 31) / 32 ? s : (M + 31) / 32;
+  int64_t s = (kSMs + col_ctas - 1) / col_ctas;  // about one wave of CTAs
+  s = s < (M + 255) / 256 ? s : (M + 255) / 256;  // at least 256 tokens per slice
   return static_cast<int>(s < 1 ? 1 : s);
 }
 
@@ -219,11 +268,29 @@ cudaError_t launch_lora_backward_prep(const uint8_t* codes, const uint8_t* scale
 cudaError_t launch_lora_grad(const void* X, const uint16_t* tp, int M, int C, int r, int t_cols,
                              const float* tensor_scale, bool transposed, float* part, float* out,
                              cudaStream_t stream) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(lora_grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kGSmem));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
   const int slices = lora_grad_slices(M, C);
-  const int m_per = (M + slices - 1) / slices;
+  GradTcParams p{};
+  if (!make_tmap_2d(&p.tx, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, M, C, static_cast<uint64_t>(C) * 2, 64, 64,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&p.tt, tp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, M, t_cols, static_cast<uint64_t>(t_cols) * 2, 64, 64,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  p.part = part;
+  p.M = M;
+  p.C = C;
+  p.r = r;
+  p.t_cols = t_cols;
+  p.m_per_slice = ((M + slices - 1) / slices + 63) / 64 * 64;  // whole 64-token stages per slice
+  p.status = nullptr;
   const dim3 grid(static_cast<unsigned>((C + 127) / 128), static_cast<unsigned>(slices));
-  lora_grad_partial_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(X), tp, M, C, r, t_cols, m_per,
-                                                     part);
+  lora_grad_tc_kernel<<<grid, 192, kGSmem, stream>>>(p);
   lora_grad_reduce_kernel<<<grid_for_elems(static_cast<int64_t>(r) * C), 256, 0, stream>>>(
       part, slices, r, C, tensor_scale, transposed, out);
   return cudaGetLastError();

@@ -203,11 +203,35 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor of an MN-major operand tile in the
+// 128-byte-swizzled layout TMA writes when it loads boxes of 64 MN-contiguous
+// 16-bit elements: each 128-byte row is one K index, 8 rows (1024 bytes) form
+// a swizzle atom along K (stride byte offset), and the next 64 MN elements
+// start `mn_stride` bytes later (leading byte offset).  Measured on GB300
+// with a probe of small-integer matrices: exact results with these roles,
+// wrong ones with the two offsets swapped.  A K16 MMA step advances the start
+// address by 16 rows (2048 bytes).
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t smem_addr, uint32_t mn_stride) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
 // Instruction descriptor: D fp32, A/B formats, both K-major, shape M x N.
 // Bits: D format [4,6) (1 = f32), A format [7,10), B format [10,13),
 // A/B major [15], [16] (0 = K-major), N >> 3 [17,23), M >> 4 [24,29).
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt, uint32_t b_fmt, uint32_t m, uint32_t n) {
   return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// The same with A and/or B MN-major (bits 15 and 16).
+__host__ __device__ constexpr uint32_t make_idesc_major(uint32_t a_fmt, uint32_t b_fmt, uint32_t m, uint32_t n,
+                                                        bool a_mn, bool b_mn) {
+  return make_idesc(a_fmt, b_fmt, m, n) | (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u);
 }
 
 constexpr uint32_t kFmtBF16 = 1;  // kind::f16 operand format
