@@ -960,12 +960,13 @@ def main():
 
     for p in per_next:
         breakdown[p]["region"] = "separate (after the step)"
-    step_ms = sum(med.values())
+    step_ms = sum(med.values()) if med else sum(med_extra.values())
     step_ms = max_over_ranks(dist, step_ms)
     value = whole_job(dist, world, dec_bytes, dec_ms) if dec_ms else None
 
     # dominant phase of the step -> roofline object
-    dom = max(phases, key=lambda p: med[p])
+    all_med = dict(med_extra, **med)
+    dom = max(phases, key=lambda p: med[p]) if phases else max(all_med, key=lambda p: all_med[p])
     d = breakdown[dom]
     if "GB/s" in d:
         roof = {"bound": "hbm", "achieved": d["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",

@@ -14,10 +14,11 @@
 // Decode attention reads every cached byte once and does G = Hq / Hkv
 // multiply-adds per byte, so it is HBM-bound; it runs on the CUDA cores in
 // fp32 (the E4M3 codes convert exactly).  Split over the sequence: a CTA
-// takes 256 tokens of one (sequence, KV head), pulls their key and value rows
-// and scales into shared memory with four bulk copies, and writes a partial
-// (max, sum, unnormalized output) per query head of the group; a second
-// kernel merges the partials in split order.
+// takes 512 tokens of one (sequence, KV head), streams their key and value
+// rows and scales through shared memory in 64-token chunks by bulk copies
+// (three in flight), and writes a partial (max, sum, unnormalized output) per
+// query head of the group; a second kernel merges the partials in split
+// order.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -30,7 +31,6 @@ namespace qrr {
 namespace {
 
 constexpr int D = 128;
-constexpr int TS = 256;  // tokens per CTA
 constexpr int kThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -55,17 +55,21 @@ __device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float (&f)[4]) {
   f[3] = b.y;
 }
 
+constexpr int CH = 64;      // tokens per pipeline chunk
+constexpr int NST = 3;      // chunks in flight
+constexpr int TSPLIT = 512; // tokens per CTA
+
 template <int G>
 struct AttnShared {
-  uint8_t k[TS * D];  // 32 KB
-  uint8_t v[TS * D];  // 32 KB
-  float ks[TS], vs[TS];
-  float p[TS][G];      // scores, then softmax numerators times the value row scale
-  float red[4][G];     // per-warp partial max / sum
-  uint64_t bar;
+  uint8_t k[NST][CH * D];  // 8 KB per chunk
+  uint8_t v[NST][CH * D];
+  float ks[NST][CH], vs[NST][CH];
+  float p[CH][G];   // this chunk's softmax numerators times the value row scale
+  float red[4][G];  // per-warp partial max / sum
+  float o[4][G][D]; // per-warp outputs, merged at the end
+  uint64_t full[NST], empty[NST];
   int abort;
 };
-
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -119,7 +123,10 @@ __global__ void kv_append_fp8_kernel(const uint16_t* __restrict__ k_new, const u
 // ---------------------------------------------------------------------------
 // Partial attention of one (sequence b, KV head g, split s) for the G query
 // heads of the group: part_m / part_l [.., G] (base-2 max, sum) and part_o
-// [.., G, 128] (unnormalized).
+// [.., G, 128] (unnormalized).  The split's tokens stream through a ring of
+// 64-token chunks (key rows, value rows and their scales by bulk copies);
+// each chunk updates a running max, sum and output (online softmax), so the
+// loads of later chunks overlap the arithmetic of earlier ones.
 template <int G>
 __global__ void __launch_bounds__(kThreads) attn_decode_fp8_kernel(
     const uint16_t* __restrict__ q, const uint8_t* __restrict__ kc, const float* __restrict__ ksc,
@@ -137,8 +144,8 @@ __global__ void __launch_bounds__(kThreads) attn_decode_fp8_kernel(
   const int s = blockIdx.x % splits, bg = blockIdx.x / splits;
   const int b = bg / Hkv, g = bg % Hkv;
   const int len = min(__ldg(lens + b), Lmax);
-  const int t0 = s * TS;
-  const int n = min(TS, len - t0);  // tokens of this split (<= 0: nothing)
+  const int t0 = s * TSPLIT;
+  const int n = min(TSPLIT, len - t0);  // tokens of this split (<= 0: nothing)
   const int64_t pidx = static_cast<int64_t>(blockIdx.x) * G;
   if (n <= 0) {
     if (tid < G) {
@@ -147,14 +154,16 @@ __global__ void __launch_bounds__(kThreads) attn_decode_fp8_kernel(
     }
     return;
   }
-  const int nr = (n + 3) & ~3;  // bulk copies move multiples of 16 bytes of scales
+  const int chunks = (n + CH - 1) / CH;
   const int64_t row0 = static_cast<int64_t>(bg) * Lmax + t0;
   if (tid == 0) {
-    mbar_init(&sh.bar, 1);
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&sh.full[i], 1);
+      mbar_init(&sh.empty[i], kThreads / 32);
+    }
     sh.abort = 0;
     fence_barrier_init();
   }
-  // the group's queries, pre-scaled for base-2 exponentials
   const float qscale = 0.08838834764831845f * kLog2e;  // 1 / sqrt(128) * log2(e)
   for (int i = tid; i < G * D; i += kThreads) {
     const int h = i / D, d = i % D;
@@ -162,29 +171,45 @@ __global__ void __launch_bounds__(kThreads) attn_decode_fp8_kernel(
     qs[d >> 4][(d & 15) * G + h] = bf16bits_to_f32(qb) * qscale;
   }
   __syncthreads();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&sh.bar, 2 * n * D + 2 * nr * 4);
-    bulk_load(sh.k, kc + row0 * D, n * D, &sh.bar);
-    bulk_load(sh.v, vc + row0 * D, n * D, &sh.bar);
-    bulk_load(sh.ks, ksc + row0, nr * 4, &sh.bar);
-    bulk_load(sh.vs, vsc + row0, nr * 4, &sh.bar);
+  // chunk c: n_c tokens; scales move in multiples of 4 (16 bytes), which stay
+  // inside the cache because Lmax % 4 == 0
+  auto issue = [&](int c) {
+    const int st = c % NST;
+    const int nc = min(CH, n - c * CH), nr = (nc + 3) & ~3;
+    const int64_t r = row0 + c * CH;
+    mbar_arrive_expect_tx(&sh.full[st], 2 * nc * D + 2 * nr * 4);
+    bulk_load(sh.k[st], kc + r * D, nc * D, &sh.full[st]);
+    bulk_load(sh.v[st], vc + r * D, nc * D, &sh.full[st]);
+    bulk_load(sh.ks[st], ksc + r, nr * 4, &sh.full[st]);
+    bulk_load(sh.vs[st], vsc + r, nr * 4, &sh.full[st]);
+  };
+  if (tid == 0)
+    for (int c = 0; c < NST && c < chunks; ++c) issue(c);
+  // running state (every thread keeps the head maxima; l and o per thread)
+  float m_run[G], l_run[G], o[G][4];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m_run[h] = -INFINITY;
+    l_run[h] = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) o[h][c] = 0.0f;
   }
-  const bool ok = mbar_wait(&sh.bar, 0, &sh.abort, status);
-  // ---- scores: thread = token (two per thread), rows read in a rotated
-  // order of 16-byte pieces so the 8 threads of a shared-memory phase hit
-  // distinct banks
-  float mx[G];
+  bool ok = true;
+  for (int c = 0; c < chunks; ++c) {
+    const int st = c % NST;
+    const int nc = min(CH, n - c * CH);
+    ok = mbar_wait(&sh.full[st], (c / NST) & 1, &sh.abort, status) && ok;
+    // ---- scores: two threads per token, each half of the head dimension
+    // (key pieces read in a rotated order, distinct banks per phase)
+    const int t = tid >> 1, half = tid & 1;
+    float acc[G];
 #pragma unroll
-  for (int h = 0; h < G; ++h) mx[h] = -INFINITY;
-  if (ok) {
-    for (int t = tid; t < n; t += kThreads) {
-      float acc[G];
+    for (int h = 0; h < G; ++h) acc[h] = 0.0f;
+    if (ok && t < nc) {
+      const uint4* row = reinterpret_cast<const uint4*>(sh.k[st] + t * D);
 #pragma unroll
-      for (int h = 0; h < G; ++h) acc[h] = 0.0f;
-      const uint4* row = reinterpret_cast<const uint4*>(sh.k + t * D);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int piece = (i + t) & 7;
+      for (int i = 0; i < 4; ++i) {
+        const int piece = 4 * half + ((i + t) & 3);
         const uint4 w = row[piece];
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -193,82 +218,89 @@ __global__ void __launch_bounds__(kThreads) attn_decode_fp8_kernel(
           e4m3x4_to_f32(ws[e], f);
           const float* qp = &qs[piece][(4 * e) * G];
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-            for (int h = 0; h < G; ++h) acc[h] = fmaf(f[c], qp[c * G + h], acc[h]);
+            for (int h = 0; h < G; ++h) acc[h] = fmaf(f[cc], qp[cc * G + h], acc[h]);
         }
       }
-      const float kscale = sh.ks[t];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float sc = acc[h] * kscale;
-        sh.p[t][h] = sc;
-        mx[h] = fmaxf(mx[h], sc);
-      }
     }
-  }
-  // ---- softmax over the split's tokens (base 2)
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float v = mx[h];
-    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    if (lane == 0) sh.red[warp][h] = v;
-  }
-  __syncthreads();
-  float m[G], lsum[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    m[h] = fmaxf(fmaxf(sh.red[0][h], sh.red[1][h]), fmaxf(sh.red[2][h], sh.red[3][h]));
-    lsum[h] = 0.0f;
-  }
-  __syncthreads();  // sh.red is reused for the sums
-  for (int t = tid; t < n; t += kThreads) {
-    const float vscale = sh.vs[t];
+    float cmax[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const float pe = ex2f(sh.p[t][h] - m[h]);
-      lsum[h] += pe;
-      sh.p[t][h] = pe * vscale;
+      acc[h] += __shfl_xor_sync(0xFFFFFFFFu, acc[h], 1);  // the two halves of the token
+      const float sc = (ok && t < nc) ? acc[h] * sh.ks[st][t] : -INFINITY;
+      acc[h] = sc;
+      float v = sc;
+      for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+      cmax[h] = v;
+    }
+    if (lane == 0)
+#pragma unroll
+      for (int h = 0; h < G; ++h) sh.red[warp][h] = cmax[h];
+    __syncthreads();
+    float alpha[G], mnew[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float cm = fmaxf(fmaxf(sh.red[0][h], sh.red[1][h]), fmaxf(sh.red[2][h], sh.red[3][h]));
+      mnew[h] = fmaxf(m_run[h], cm);
+      alpha[h] = m_run[h] == -INFINITY ? 0.0f : ex2f(m_run[h] - mnew[h]);
+      m_run[h] = mnew[h];
+      l_run[h] *= alpha[h];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) o[h][cc] *= alpha[h];
+    }
+    if (half == 0 && t < nc) {
+      const float vscale = sh.vs[st][t];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float pe = ok ? ex2f(acc[h] - mnew[h]) : 0.0f;
+        l_run[h] += pe;
+        sh.p[t][h] = pe * vscale;
+      }
+    }
+    __syncthreads();
+    // ---- p . V: warp w takes tokens w, w + 4, ...; lane = 4 values of d
+    if (ok)
+      for (int tt = warp; tt < nc; tt += 4) {
+        float f[4];
+        e4m3x4_to_f32(reinterpret_cast<const uint32_t*>(sh.v[st] + tt * D)[lane], f);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float pw = sh.p[tt][h];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) o[h][cc] = fmaf(pw, f[cc], o[h][cc]);
+        }
+      }
+    __syncthreads();  // sh.p and sh.red are rewritten by the next chunk
+    if (lane == 0) mbar_arrive(&sh.empty[st]);
+    if (tid == 0 && c + NST < chunks) {
+      // the ring slot is free once every warp has read it
+      if (!mbar_wait(&sh.empty[st], (c / NST) & 1, &sh.abort, status)) ok = false;
+      else issue(c + NST);
     }
   }
+  // ---- merge the warps' outputs and the threads' sums
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    float v = lsum[h];
-    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    *reinterpret_cast<float4*>(&sh.o[warp][h][4 * lane]) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+    float v = l_run[h];
+    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
     if (lane == 0) sh.red[warp][h] = v;
   }
   __syncthreads();
-  // ---- p . V: warp w takes tokens w, w + 4, ...; lane = 4 values of d
-  float o[G][4];
-#pragma unroll
-  for (int h = 0; h < G; ++h)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) o[h][c] = 0.0f;
-  if (ok) {
-    for (int t = warp; t < n; t += 4) {
-      float f[4];
-      e4m3x4_to_f32(reinterpret_cast<const uint32_t*>(sh.v + t * D)[lane], f);
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float pw = sh.p[t][h];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) o[h][c] = fmaf(pw, f[c], o[h][c]);
-      }
-    }
-  }
-  // the four warps' partial outputs meet in shared memory (the key buffer is free now)
-  float* red_o = reinterpret_cast<float*>(sh.k);  // [4 warps][G][128]
-#pragma unroll
-  for (int h = 0; h < G; ++h)
-    *reinterpret_cast<float4*>(red_o + (warp * G + h) * D + 4 * lane) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
-  __syncthreads();
   for (int i = tid; i < G * D; i += kThreads) {
-    const float acc = red_o[i] + red_o[G * D + i] + red_o[2 * G * D + i] + red_o[3 * G * D + i];
-    part_o[pidx * D + i] = acc;
+    const int h = i / D, d = i % D;
+    part_o[pidx * D + i] = sh.o[0][h][d] + sh.o[1][h][d] + sh.o[2][h][d] + sh.o[3][h][d];
   }
   if (tid < G) {
-    part_m[pidx + tid] = ok ? m[tid] : -INFINITY;
+    part_m[pidx + tid] = ok ? m_run[tid] : -INFINITY;
     part_l[pidx + tid] = ok ? (sh.red[0][tid] + sh.red[1][tid] + sh.red[2][tid] + sh.red[3][tid]) : 0.0f;
+  }
+  // every issued copy has landed before the CTA exits
+  if (tid == 0) {
+    volatile int no_abort = 0;
+    for (int c = max(0, chunks - NST); c < chunks; ++c)
+      mbar_wait(&sh.full[c % NST], (c / NST) & 1, &no_abort, status);
   }
 }
 
@@ -307,7 +339,7 @@ __global__ void attn_combine_kernel(const float* __restrict__ part_m, const floa
   reinterpret_cast<uint2*>(out + static_cast<int64_t>(row) * D)[lane] = w;
 }
 
-int attn_splits(int Lmax) { return (Lmax + TS - 1) / TS; }
+int attn_splits(int Lmax) { return (Lmax + TSPLIT - 1) / TSPLIT; }
 
 cudaError_t launch_kv_append_fp8(const void* k_new, const void* v_new, int B, int Hkv, const int32_t* pos, int Lmax,
                                  uint8_t* kc, float* ksc, uint8_t* vc, float* vsc, int mode, int32_t* status,
