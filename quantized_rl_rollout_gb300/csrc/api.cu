@@ -59,8 +59,8 @@ struct LinPlan {
   bool pair;  // 256-token tiles on CTA pairs (2-CTA clusters), each pair two 128-row tiles
   int bn, bk, m_tiles, count;
   struct Layer {
-    int n_tiles, splits, kcps, lora_chunks, lora_ks, lora_slice;
-    size_t t_off, x16_off, p_off, part_off, tpart_off, cnt_off, ticket_off;
+    int n_tiles, splits, kcps, lora_chunks;
+    size_t t_off, x16_off, p_off, part_off, cnt_off;
   } l[kMaxW4Layers];
   size_t cnt_begin, cnt_bytes, total;
 };
@@ -136,22 +136,12 @@ LinPlan plan_linear(int64_t M, const LinIn* in, int count) {
     if (p.f16) off += round_up(static_cast<size_t>(M) * 4);
     L.part_off = off;
     if (L.splits > 1) off += round_up(static_cast<size_t>(L.splits) * M * in[j].N * 4);
-    // decode LoRA down projection: fp32 partials over K slices.  Short slices
-    // give many CTAs in one wave, each reading a short slice of x and A; the
-    // last CTA of a token tile then sums M r partials per slice, so the slices
-    // grow with the token count to keep that sum off the critical path.
-    L.lora_slice = M <= 8 ? 512 : M <= 32 ? 1024 : 2048;
-    L.lora_ks = static_cast<int>((in[j].K + L.lora_slice - 1) / L.lora_slice);
-    L.tpart_off = off;
-    if (in[j].r > 0 && p.f16) off += round_up(static_cast<size_t>((L.lora_ks + 3) & ~3) * M * in[j].r * 4);
   }
-  // split-K tile counters and LoRA tickets: one block, zeroed per call
+  // split-K tile counters: one block, cleared per call by the decode prologue
   p.cnt_begin = off;
   for (int j = 0; j < count; ++j) {
     p.l[j].cnt_off = off;
     off += static_cast<size_t>(p.m_tiles) * p.l[j].n_tiles * 4;
-    p.l[j].ticket_off = off;
-    off += (in[j].r > 0 ? static_cast<size_t>((M + 127) / 128) : 0) * 4;  // one per 128-token tile
   }
   p.cnt_bytes = off - p.cnt_begin;
   p.total = round_up(off) + kAlign;
@@ -185,8 +175,10 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   // layers with K == 0 produce zeros; layers with N == 0 produce nothing
   W4Params p{};
-  LoraDownBatch lb{};
+  LoraDownBatch lb{};    // prefill: the adapter's down projection
+  DecodeProBatch db{};   // decode: x16, p and t' in one cluster launch
   lb.status = dev_status;
+  db.status = dev_status;
   p.status = dev_status;
   bool any_split = false;
   for (int j = 0; j < count; ++j) {
@@ -200,35 +192,45 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
     __nv_bfloat16* tbuf = reinterpret_cast<__nv_bfloat16*>(ws + pj.t_off);
     __half* x16 = reinterpret_cast<__half*>(ws + pj.x16_off);
     int* pexp = reinterpret_cast<int*>(ws + pj.p_off);
-    if (a.r > 0 || pl.f16) {
-      // prologue: the LoRA down projection on the tensor cores (decode: cut
-      // into 512-wide K slices so it runs in one wave) and the f16 image of x
+    const int R = (a.r + 15) / 16 * 16;
+    if (pl.f16) {
+      DecodeProLayer& dl = db.l[db.count++];
+      dl.x = static_cast<const uint16_t*>(a.x);
+      dl.A = static_cast<const uint16_t*>(a.A);
+      dl.x16 = x16;
+      dl.pexp = pexp;
+      dl.t = tbuf;
+      dl.tensor_scale = a.tensor_scale;
+      dl.M = static_cast<int>(M);
+      dl.K = static_cast<int>(a.K);
+      dl.r = a.r;
+      dl.R = a.r > 0 ? R : 0;
+      dl.t_cols = 64 * pj.lora_chunks;
+      dl.lora_scale = a.r > 0 ? a.alpha / static_cast<float>(a.r) : 0.0f;
+    } else if (a.r > 0) {
+      // prologue: the LoRA down projection on the tensor cores, one CTA per
+      // 128-token tile over the whole K
       LoraDownLayer& ld = lb.l[lb.count++];
       if (!make_tmap_2d(&ld.tx, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, M, a.K, a.K * 2, 128, 64,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !make_tmap_2d(&ld.ta, a.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.r, a.K, a.K * 2, R, 64,
                         CU_TENSOR_MAP_SWIZZLE_128B))
         return QRR_ERR_CUDA;
-      if (a.r > 0) {
-        if (!make_tmap_2d(&ld.ta, a.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.r, a.K, a.K * 2, (a.r + 15) / 16 * 16, 64,
-                          CU_TENSOR_MAP_SWIZZLE_128B))
-          return QRR_ERR_CUDA;
-      } else {
-        ld.ta = ld.tx;  // never read without an adapter
-      }
       ld.t = tbuf;
       ld.tensor_scale = a.tensor_scale;
-      ld.tpart = reinterpret_cast<float*>(ws + pj.tpart_off);
-      ld.tickets = reinterpret_cast<uint32_t*>(ws + pj.ticket_off);
+      ld.tpart = nullptr;
+      ld.tickets = nullptr;
       ld.x = static_cast<const uint16_t*>(a.x);
-      ld.x16 = pl.f16 ? x16 : nullptr;
-      ld.pexp = pexp;
+      ld.x16 = nullptr;
+      ld.pexp = nullptr;
       ld.M = static_cast<int>(M);
       ld.K = static_cast<int>(a.K);
       ld.r = a.r;
-      ld.R = (a.r + 15) / 16 * 16;
+      ld.R = R;
       ld.t_cols = 64 * pj.lora_chunks;
-      ld.ks = pl.f16 ? pj.lora_ks : 1;
-      ld.slice_steps = pl.f16 ? pj.lora_slice / 64 : static_cast<int>(a.K / 64);
-      ld.lora_scale = a.r > 0 ? a.alpha / static_cast<float>(a.r) : 0.0f;
+      ld.ks = 1;
+      ld.slice_steps = static_cast<int>(a.K / 64);
+      ld.lora_scale = a.alpha / static_cast<float>(a.r);
     }
     W4Layer& L = p.layer[p.count++];
     const void* xsrc = pl.f16 ? static_cast<const void*>(x16) : a.x;
@@ -263,10 +265,19 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
     L.m_tiles = pl.m_tiles;
     L.splits = pj.splits;
     L.kcps = pj.kcps;
-    any_split = any_split || pj.splits > 1 || a.r > 0;
+    any_split = any_split || pj.splits > 1;
   }
   if (p.count == 0) return QRR_OK;
-  if (any_split && cudaMemsetAsync(ws + pl.cnt_begin, 0, pl.cnt_bytes, s) != cudaSuccess) return QRR_ERR_CUDA;
+  if (pl.f16) {
+    // split-K is planned for decode only, and its counters are cleared by the
+    // prologue, which the GEMM waits for before it touches them
+    if (any_split) {
+      db.clear = reinterpret_cast<uint32_t*>(ws + pl.cnt_begin);
+      db.clear_words = static_cast<int>(pl.cnt_bytes / 4);
+    }
+    if (launch_decode_prologue(db, s) != cudaSuccess) return QRR_ERR_CUDA;
+    return from_cuda(launch_w4a16_tc(p, pl.bn, pl.f16, pl.pair, true, s));
+  }
   if (lb.count > 0 && launch_lora_down_tc(lb, s) != cudaSuccess) return QRR_ERR_CUDA;
   return from_cuda(launch_w4a16_tc(p, pl.bn, pl.f16, pl.pair, lb.count > 0, s));
 }

@@ -33,11 +33,20 @@ struct W4Layer {
   int first_unit;
 };
 
+// Per-CTA unit lists of a launch (single CTAs): CTA b takes units
+// sched[sched_off[b] .. sched_off[b + 1]) in that order.  Without a list
+// (use_sched == 0, and always for CTA pairs) units go round-robin.
+constexpr int kMaxSchedUnits = 2048;
+constexpr int kMaxSchedCtas = 160;
+
 struct W4Params {
   W4Layer layer[kMaxW4Layers];
   int count;
   int total_units;
   int32_t* status;
+  int use_sched;
+  uint16_t sched_off[kMaxSchedCtas + 1];
+  uint16_t sched[kMaxSchedUnits];
 };
 
 // Prologue of one layer (lora_tc.cu): the LoRA down projection on the tensor
@@ -68,6 +77,33 @@ struct LoraDownBatch {
 };
 
 cudaError_t launch_lora_down_tc(LoraDownBatch& b, cudaStream_t stream);
+
+// Decode prologue (decode_prologue.cu), at most 64 tokens: per layer one
+// cluster of CTAs over K slices writes x16 / pexp and t' (the cluster sums
+// its slices through distributed shared memory), and the launch clears the
+// GEMM's split-K tile counters.
+struct DecodeProLayer {
+  const uint16_t* x;  // bf16 [M, K]
+  const uint16_t* A;  // LoRA A bf16 [r, K] (r > 0)
+  __half* x16;        // f16 [M, K]
+  int* pexp;          // [M]
+  __nv_bfloat16* t;   // [M, t_cols] (r > 0)
+  const float* tensor_scale;
+  int M, K, r, R, t_cols;  // R: r rounded up to a multiple of 16 (0 without an adapter)
+  float lora_scale;
+  int first_cta;  // set by the launcher
+};
+
+struct DecodeProBatch {
+  DecodeProLayer l[kMaxW4Layers];
+  int count;
+  uint32_t* clear;  // words zeroed by the launch (the GEMM's tile counters), or null
+  int clear_words;
+  int32_t* status;
+  int xr, stages, ks;  // set by the launcher
+};
+
+cudaError_t launch_decode_prologue(DecodeProBatch& b, cudaStream_t stream);
 
 int w4_bn_for(int64_t M);
 int w4_bk_for(int64_t M);

@@ -50,7 +50,14 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+#include <queue>
 #include <type_traits>
+#include <utility>
+#include <vector>
 
 #include "linear.cuh"
 #include "tc.cuh"
@@ -64,7 +71,7 @@ namespace qrr {
 #ifdef QRR_TRACE_BUILD
 __device__ unsigned long long qrr_trace_buf[8][4][256];
 // global-timer stamps per CTA: start, x stream released, first MMA, end
-__device__ unsigned long long qrr_gtrace_buf[256][4];
+__device__ unsigned long long qrr_gtrace_buf[256][8];
 #define QRR_GSTAMP(ev)                                               \
   do {                                                               \
     unsigned long long t_;                                           \
@@ -117,7 +124,9 @@ struct Cfg {
   // unambiguous, at most STAGES stages back); a deeper TMEM ring gets one
   // release barrier per slot, at the price of a second commit per chunk.
   static constexpr int AST_FIT = (512 - A_COL) / ACOLS;
-  static constexpr bool SLOT_BARS = AST_FIT > CPS * STAGES;
+  // 256-wide decode stages release each A slot per chunk: waiting for the
+  // stage's second chunk would hold the slot back by a chunk's dequant time
+  static constexpr bool SLOT_BARS = AST_FIT > CPS * STAGES || BK >= 256;
   static constexpr int AST = (AST_FIT > 8 ? 8 : AST_FIT) / G * G;
   static constexpr int THREADS = 32 * (2 + 4 + 4 * G);
   // registers per thread for one resident CTA: each of the SM's four
@@ -255,6 +264,13 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
   const uint32_t rank = PAIR ? cluster_rank() : 0u;
   const int ustart = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int ustep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  // this CTA's units: a list balanced by cost on the host when given,
+  // round-robin otherwise; unit_at(i) is the i-th of them
+  const bool sched = !PAIR && p.use_sched;
+  const int sched0 = sched ? p.sched_off[blockIdx.x] : 0;
+  const int n_my = sched ? p.sched_off[blockIdx.x + 1] - sched0
+                         : (ustart < p.total_units ? (p.total_units - 1 - ustart) / ustep + 1 : 0);
+  auto unit_at = [&](int i) { return sched ? static_cast<int>(p.sched[sched0 + i]) : ustart + i * ustep; };
   // Every wait acquires at CTA scope, which keeps the SM's L1 contents valid
   // across it: what the peer CTA of a pair hands over through a barrier is
   // tensor-memory state, TMA bytes or tensor-core completion, none of it
@@ -334,13 +350,14 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
     // bf16 x does not, and t' (the LoRA stages) always does.
     if (elect_one()) {
       struct Cursor {
-        int u = -1, c = 0, j = 0, nt = 0, mt = 0, sp = 0, c0 = 0, nk = 0, nl = 0;
+        int i = -1, c = 0, j = 0, nt = 0, mt = 0, sp = 0, c0 = 0, nk = 0, nl = 0;
       };
       auto next = [&](Cursor& k) {  // advance to the next stage of the CTA; false past the last
-        if (k.u >= 0 && ++k.c < k.nk + k.nl) return true;
+        if (k.i >= n_my) return false;
+        if (k.i >= 0 && ++k.c < k.nk + k.nl) return true;
         k.c = 0;
-        for (k.u = k.u < 0 ? ustart : k.u + ustep; k.u < p.total_units; k.u += ustep) {
-          locate(k.u, k.j, k.nt, k.mt, k.sp, k.c0, k.nk, k.nl);
+        for (++k.i; k.i < n_my; ++k.i) {
+          locate(unit_at(k.i), k.j, k.nt, k.mt, k.sp, k.c0, k.nk, k.nl);
           if (k.nk + k.nl > 0) return true;
         }
         return false;
@@ -437,9 +454,9 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
       Ring st, at;
       uint32_t units = 0, chunks = 0;
       bool ok = true;
-      for (int u = ustart; u < p.total_units && ok; u += ustep, ++units) {
+      for (int ui = 0; ui < n_my && ok; ++ui, ++units) {
         int j, nt, mt, sp, c0, nk, nl;
-        locate(u, j, nt, mt, sp, c0, nk, nl);
+        locate(unit_at(ui), j, nt, mt, sp, c0, nk, nl);
         const int db = units % C::DBUF;
         const uint32_t duse = units / C::DBUF;
         QRR_STAMP(1, 2, units);
@@ -495,6 +512,9 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
         commit(&sh.d_full[db]);
         QRR_STAMP(2, 3, units);
       }
+#ifdef QRR_TRACE_BUILD
+      if (blockIdx.x < 256) qrr_gtrace_buf[blockIdx.x][4] = chunks;
+#endif
       if constexpr (PAIR)
         mma_commit_pair(&sh.done, 0x1);
       else
@@ -511,9 +531,9 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
     if constexpr (F16) griddep_wait();  // the per-token exponents come from the prologue kernel
     uint32_t units = 0;
-    for (int u = ustart; u < p.total_units; u += ustep, ++units) {
+    for (int ui = 0; ui < n_my; ++ui, ++units) {
       int j, nt, mt, sp, c0, nk, nl;
-      locate(u, j, nt, mt, sp, c0, nk, nl);
+      locate(unit_at(ui), j, nt, mt, sp, c0, nk, nl);
       const int M = p.layer[j].M, N = p.layer[j].N, splits = p.layer[j].splits, n_tiles = p.layer[j].n_tiles;
       const int* const pexp = p.layer[j].pexp;
       __nv_bfloat16* const y = p.layer[j].y;
@@ -674,31 +694,36 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
     const int rot = BK == 256 ? (row & 7) : ((row >> 2) & 1);
     // this CTA's A chunks: its units in order, (nk + nl) stages of CPS chunks
     uint32_t total = 0;
-    for (int u = ustart; u < p.total_units; u += ustep) {
+    for (int ui = 0; ui < n_my; ++ui) {
       int j, nt, mt, sp, c0, nk, nl;
-      locate(u, j, nt, mt, sp, c0, nk, nl);
+      locate(unit_at(ui), j, nt, mt, sp, c0, nk, nl);
       total += static_cast<uint32_t>((nk + nl) * C::CPS);
     }
-    int u = ustart - ustep;
+    int ui = -1;
     uint32_t ubeg = 0, uend = 0;  // chunk range of unit u
     int j = 0, nt = 0, mt = 0, sp = 0, c0 = 0, nk = 0, nl = 0;
+    // the unit's layer fields, read once per unit (see the epilogue)
+    int LM = 0, Lr = 0, n = 0;
+    const int* Lpexp = nullptr;
+    const uint16_t* LB = nullptr;
+    const uint8_t* srow = nullptr;
     while (true) {
       uint32_t chunk = 0;
       if (lane == 0) chunk = atomicAdd(&sh.next_chunk[q], 1u);
       chunk = __shfl_sync(0xFFFFFFFFu, chunk, 0);
       if (chunk >= total) break;
       while (chunk >= uend) {  // claims only grow: move forward to the chunk's unit
-        u += ustep;
-        locate(u, j, nt, mt, sp, c0, nk, nl);
+        ++ui;
+        locate(unit_at(ui), j, nt, mt, sp, c0, nk, nl);
         ubeg = uend;
         uend += static_cast<uint32_t>((nk + nl) * C::CPS);
+        LM = p.layer[j].M;
+        Lr = p.layer[j].r;
+        Lpexp = p.layer[j].pexp;
+        LB = p.layer[j].B;
+        n = nt * 128 + row;
+        srow = p.layer[j].scales + static_cast<int64_t>(n) * (p.layer[j].K / 16);
       }
-      // layer fields in registers (see the epilogue)
-      const int LM = p.layer[j].M, Lr = p.layer[j].r;
-      const int* const Lpexp = p.layer[j].pexp;
-      const uint16_t* const LB = p.layer[j].B;
-      const int n = nt * 128 + row;
-      const uint8_t* srow = p.layer[j].scales + static_cast<int64_t>(n) * (p.layer[j].K / 16);
       const int c = static_cast<int>((chunk - ubeg) / C::CPS);   // stage within the unit
       const int hc = static_cast<int>((chunk - ubeg) % C::CPS);  // chunk within the stage
       const uint32_t sseq = chunk / C::CPS;                      // stage sequence number of the CTA
@@ -888,6 +913,77 @@ cudaError_t launch_bn(const W4Params& p, int grid, bool after_prologue, cudaStre
 
 }  // namespace
 
+// Longest-processing-time-first assignment of the units to `grid` CTAs: a
+// unit costs its K stages (weights and LoRA) plus its epilogue (about half a
+// stage, or three when it writes a split-K partial and may run the
+// reduction); each unit in turn, costliest first, goes to the least loaded
+// CTA, which then processes its units in index order.  The last schedule is
+// kept and reused while the launch's shape repeats.
+void build_schedule(W4Params& p, int grid, int bk) {
+  struct Key {
+    int grid, bk, count, n[kMaxW4Layers][5];
+    bool operator==(const Key& o) const { return memcmp(this, &o, sizeof(Key)) == 0; }
+  };
+  static std::mutex mu;
+  static Key last_key;
+  static bool have = false;
+  static uint16_t last_off[kMaxSchedCtas + 1];
+  static uint16_t last_sched[kMaxSchedUnits];
+  Key key;
+  memset(&key, 0, sizeof(key));
+  key.grid = grid;
+  key.bk = bk;
+  key.count = p.count;
+  for (int j = 0; j < p.count; ++j) {
+    const W4Layer& L = p.layer[j];
+    key.n[j][0] = L.n_tiles;
+    key.n[j][1] = L.m_tiles;
+    key.n[j][2] = L.splits;
+    key.n[j][3] = L.kcps;
+    key.n[j][4] = L.K * 1024 + L.lora_chunks;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!have || !(key == last_key)) {
+    const int units = p.total_units;
+    std::vector<std::pair<double, int>> cost(units);
+    for (int j = 0; j < p.count; ++j) {
+      const W4Layer& L = p.layer[j];
+      const int kc = L.K / bk, ksub = bk / 64;
+      const int per = L.n_tiles * L.m_tiles;
+      for (int local = 0; local < per * L.splits; ++local) {
+        const int sp = local / per;
+        const int nk = std::min((sp + 1) * L.kcps, kc) - sp * L.kcps;
+        const int nl = (L.r > 0 && sp == L.splits - 1) ? (L.lora_chunks + ksub - 1) / ksub : 0;
+        cost[L.first_unit + local] = {nk + nl + (L.splits > 1 ? 3.0 : 0.5), L.first_unit + local};
+      }
+    }
+    std::stable_sort(cost.begin(), cost.end(), [](const std::pair<double, int>& a, const std::pair<double, int>& b) {
+      return a.first > b.first;
+    });
+    std::priority_queue<std::pair<double, int>, std::vector<std::pair<double, int>>, std::greater<>> load;
+    for (int b = 0; b < grid; ++b) load.push({0.0, b});
+    std::vector<std::vector<int>> mine(grid);
+    for (const auto& c : cost) {
+      auto top = load.top();
+      load.pop();
+      mine[top.second].push_back(c.second);
+      load.push({top.first + c.first, top.second});
+    }
+    int off = 0;
+    for (int b = 0; b < grid; ++b) {
+      std::sort(mine[b].begin(), mine[b].end());
+      last_off[b] = static_cast<uint16_t>(off);
+      for (int u : mine[b]) last_sched[off++] = static_cast<uint16_t>(u);
+    }
+    last_off[grid] = static_cast<uint16_t>(off);
+    last_key = key;
+    have = true;
+  }
+  memcpy(p.sched_off, last_off, sizeof(uint16_t) * (grid + 1));
+  memcpy(p.sched, last_sched, sizeof(uint16_t) * p.total_units);
+  p.use_sched = 1;
+}
+
 int w4_bn_for(int64_t M) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
@@ -913,6 +1009,8 @@ cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, bool pair, bool after
   int dev = 0, sms = kSMs;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = units < sms ? units : sms;
+  p.use_sched = 0;
+  if (!pair && units <= kMaxSchedUnits && grid <= kMaxSchedCtas) build_schedule(p, grid, f16 ? 256 : 64);
   if (f16) {
     switch (bn) {
       case 16: return launch_bn<16, 256, true, kDecodeGroups>(p, grid, after_prologue, stream);

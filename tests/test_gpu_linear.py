@@ -339,3 +339,34 @@ def test_requantize_many_tensors_grouping(q):
     for w, (c, s, t) in zip(Ws, outs):
         rc, rs, rt = oracle.nvfp4.quantize(to_np(w))
         assert t.item() == float(rt) and np.array_equal(c.cpu().numpy(), rc) and np.array_equal(s.cpu().numpy(), rs)
+
+
+@pytest.mark.parametrize("m", [4, 40])
+def test_decode_token_max_in_one_slice(q, m):
+    """Each token's largest |x| sits in a different part of K (first, middle
+    and last 64-wide steps): the per-token power of two of the f16 operand
+    comes from the maximum over the whole row, which the decode prologue
+    forms from its K slices, so every token still matches the oracle."""
+    n, k, r = 256, 2048, 16
+    W, codes, scales, ts, A, B, alpha = _layer(q, n, k, r, "slicemax")
+    x = inputs.activations(m, k, inputs.derive_seed(0, "slicemax", m), device=DEV).float()
+    x[0, k - 5] = 3.0e4
+    x[1, 3] = -5.0e3
+    x[2] *= 1e-6
+    x[2, 1000] = 1.0
+    x[3, 700] = 1.0e-30
+    x = x.to(torch.bfloat16)
+    y = q.linear_nvfp4_lora(x, codes, scales, ts, A, B, alpha)
+    torch.cuda.synchronize()
+    _assert_close(y, _ref(x, codes, scales, ts, A, B, alpha), f"m={m}")
+
+
+def test_decode_nonfinite_x_flagged(q):
+    """An infinite activation at decode sizes raises the non-finite status bit."""
+    W, codes, scales, ts, A, B, alpha = _layer(q, 256, 1024, 16, "nonfin")
+    x = inputs.activations(3, 1024, 11, device=DEV)
+    x[1, 517] = float("inf")
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    q.linear_nvfp4_lora(x, codes, scales, ts, A, B, alpha, dev_status=st)
+    torch.cuda.synchronize()
+    assert q.get_last_device_status(st) & q.DEV_NONFINITE
