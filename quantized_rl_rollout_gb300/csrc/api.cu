@@ -246,6 +246,9 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
       if (!make_tmap_2d(&L.tt, tbuf, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, M, 64 * pj.lora_chunks,
                         64 * pj.lora_chunks * 2, box_m, 64, CU_TENSOR_MAP_SWIZZLE_128B))
         return QRR_ERR_CUDA;
+      if (pl.f16 && !make_tmap_2d(&L.tb, a.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.N, a.r, a.r * 2, 128,
+                                  static_cast<uint32_t>(a.r), CU_TENSOR_MAP_SWIZZLE_NONE))
+        return QRR_ERR_CUDA;
     } else {
       L.tt = L.tx;  // never read without an adapter
     }

@@ -92,9 +92,21 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
   return v;
 }
 
-// t'[m, 2j], t'[m, 2j+1] of one rank: v = scale t / g as (high, low) bf16
-__device__ __forceinline__ void write_tprime(__nv_bfloat16* trow, int jj, float scale, float t, float g) {
-  const float v = __fdiv_rn(scale * t, g);
+// The power of two p with amax 2^-p in [2^14, 2^15) for max |x| bits `mx`
+// (0 for an all-zero row).
+__device__ __forceinline__ int pexp_of(uint32_t mx) {
+  if (mx == 0u) return 0;
+  int e;
+  frexpf(bf16bits_to_f32(mx), &e);  // amax = f 2^e, 0.5 <= f < 1
+  return e - 15;
+}
+
+// t'[m, 2j], t'[m, 2j+1] of one rank: v = (scale t / g) 2^-p_m as (high,
+// low) bf16.  The factor 2^-p_m is the one the GEMM's accumulator carries
+// for token m (its f16 image of x is scaled by it); multiplying by a power
+// of two is exact, so this equals scaling the (high, low) pair afterwards.
+__device__ __forceinline__ void write_tprime(__nv_bfloat16* trow, int jj, float scale, float t, float g, int pexp) {
+  const float v = Pow2Scaler(pexp)(__fdiv_rn(scale * t, g));
   const __nv_bfloat16 hi = __float2bfloat16_rn(v);
   const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
   trow[2 * jj] = hi;
@@ -261,12 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_prologue_kernel(const __gr
     uint32_t mx = 0u;
 #pragma unroll
     for (int rr = 0; rr < kKsMax; ++rr) mx = max(mx, part[rr]);
-    int pe = 0;
-    if (mx != 0u) {
-      int e;
-      frexpf(bf16bits_to_f32(mx), &e);  // amax = f 2^e, 0.5 <= f < 1
-      pe = e - 15;                      // amax 2^-p in [2^14, 2^15)
-    }
+    const int pe = pexp_of(mx);
     sh.pexp[m] = pe;
     if (rank == 0) {
       if (mx >= 0x7F80u) flag(b.status, QRR_DEV_NONFINITE);
@@ -321,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_prologue_kernel(const __gr
       float sum = 0.0f;
 #pragma unroll
       for (int rr = 0; rr < kKsMax; ++rr) sum += part[rr];  // slice order; the slices past ks add 0
-      write_tprime(t + static_cast<int64_t>(m) * t_cols, jj, lscale, sum, g);
+      write_tprime(t + static_cast<int64_t>(m) * t_cols, jj, lscale, sum, g, sh.pexp[m]);
     }
     const int pad = t_cols - 2 * r;
     for (int idx = rank * kThreads + tid; idx < M * pad; idx += ks * kThreads)
@@ -373,6 +380,7 @@ __device__ __forceinline__ void unpack8_bf16(uint4 v, float (&f)[8]) {
 __global__ void __launch_bounds__(kSmallThreads) decode_prologue_small_kernel(const __grid_constant__ DecodeProBatch b) {
   __shared__ uint32_t red_u[kSmallThreads / 32];
   __shared__ float red_f[kSmallThreads / 32][kSmallM * kRanksPerCta];
+  __shared__ uint32_t red_m[kSmallThreads / 32][kSmallM];
   griddep_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int j = 0;
@@ -396,12 +404,7 @@ __global__ void __launch_bounds__(kSmallThreads) decode_prologue_small_kernel(co
     mx = 0u;
 #pragma unroll
     for (int w = 0; w < kSmallThreads / 32; ++w) mx = max(mx, red_u[w]);
-    int pe = 0;
-    if (mx != 0u) {
-      int e;
-      frexpf(bf16bits_to_f32(mx), &e);  // amax = f 2^e, 0.5 <= f < 1
-      pe = e - 15;                      // amax 2^-p in [2^14, 2^15)
-    }
+    const int pe = pexp_of(mx);
     if (tid == 0) {
       if (mx >= 0x7F80u) flag(b.status, QRR_DEV_NONFINITE);
       L.pexp[m] = pe;
@@ -422,13 +425,16 @@ __global__ void __launch_bounds__(kSmallThreads) decode_prologue_small_kernel(co
     }
     return;
   }
-  // ---- t of 4 ranks, all tokens ----
+  // ---- t of kRanksPerCta ranks, all tokens ----
   const int r = L.r, j0 = (local - M) * kRanksPerCta;
   float acc[kSmallM][kRanksPerCta];
+  uint32_t xmax[kSmallM];  // each token's max |x| (its p scales t')
 #pragma unroll
-  for (int mm = 0; mm < kSmallM; ++mm)
+  for (int mm = 0; mm < kSmallM; ++mm) {
+    xmax[mm] = 0u;
 #pragma unroll
     for (int jj = 0; jj < kRanksPerCta; ++jj) acc[mm][jj] = 0.0f;
+  }
   const uint4* arow[kRanksPerCta];
 #pragma unroll
   for (int jj = 0; jj < kRanksPerCta; ++jj)
@@ -456,6 +462,7 @@ __global__ void __launch_bounds__(kSmallThreads) decode_prologue_small_kernel(co
       for (int jj = 0; jj < kRanksPerCta; ++jj) unpack8_bf16(av[b][jj], a[jj]);
 #pragma unroll
       for (int mm = 0; mm < kSmallM; ++mm) {
+        xmax[mm] = max(xmax[mm], absmax_bits8(xv[b][mm]));
         float xf[8];
         unpack8_bf16(xv[b][mm], xf);
 #pragma unroll
@@ -474,15 +481,24 @@ __global__ void __launch_bounds__(kSmallThreads) decode_prologue_small_kernel(co
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
       if (lane == 0) red_f[warp][mm * kRanksPerCta + jj] = v;
     }
+#pragma unroll
+  for (int mm = 0; mm < kSmallM; ++mm) {
+    const uint32_t v = __reduce_max_sync(0xFFFFFFFFu, xmax[mm]);
+    if (lane == 0) red_m[warp][mm] = v;
+  }
   __syncthreads();
   if (tid < M * kRanksPerCta) {
     const int mm = tid / kRanksPerCta, jj = tid % kRanksPerCta;
     float t = 0.0f;
 #pragma unroll
     for (int w = 0; w < kSmallThreads / 32; ++w) t += red_f[w][tid];
+    uint32_t mx = 0u;
+#pragma unroll
+    for (int w = 0; w < kSmallThreads / 32; ++w) mx = max(mx, red_m[w][mm]);
     if (j0 + jj < r) {
       const float st = *L.tensor_scale;
-      write_tprime(L.t + static_cast<int64_t>(mm) * L.t_cols, j0 + jj, L.lora_scale, t, st > 0.0f ? st : 1.0f);
+      write_tprime(L.t + static_cast<int64_t>(mm) * L.t_cols, j0 + jj, L.lora_scale, t, st > 0.0f ? st : 1.0f,
+                   pexp_of(mx));
     }
   }
   // the padding columns of t' past 2 r: the first t CTA of the layer

@@ -21,6 +21,7 @@ struct W4Layer {
   CUtensorMap tcodes;  // packed codes u8 [N, K/2], box [128, 32]
   CUtensorMap tt;      // LoRA t' bf16 [M, 64 * lora_chunks], box as tx, 128 B swizzle
   CUtensorMap tscales;  // block scales u8 [N, K/16], box [128, 16] (256-wide K stages)
+  CUtensorMap tb;       // decode: LoRA B bf16 [N, r], box [128, r], into the LoRA stage's code slot
   const uint8_t* scales;
   const float* tensor_scale;
   const uint16_t* B;  // LoRA B [N, r], r <= 64

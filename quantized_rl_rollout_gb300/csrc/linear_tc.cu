@@ -371,6 +371,12 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
           tma_load_2d(&p.layer[k.j].tcodes, fb, xs + C::X_BYTES, kb / 2, k.nt * 128);
           if constexpr (C::SC_TMA)
             tma_load_2d(&p.layer[k.j].tscales, fb, xs + C::X_BYTES + C::C_BYTES, kb / 16, k.nt * 128);
+        } else if (F16) {
+          // LoRA stage: no codes; the adapter's B rows of the tile take
+          // their place (r <= 64: at most 16 KB)
+          uint8_t* xs = tiles + idx * C::STAGE;
+          mbar_arrive_expect_tx(fb, 128u * static_cast<uint32_t>(p.layer[k.j].r) * 2u);
+          tma_load_2d(&p.layer[k.j].tb, fb, xs + C::X_BYTES, 0, k.nt * 128);
         } else {
           mbar_arrive(fb);  // LoRA stage: no codes
         }
@@ -704,7 +710,6 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
     int j = 0, nt = 0, mt = 0, sp = 0, c0 = 0, nk = 0, nl = 0;
     // the unit's layer fields, read once per unit (see the epilogue)
     int LM = 0, Lr = 0, n = 0;
-    const int* Lpexp = nullptr;
     const uint16_t* LB = nullptr;
     const uint8_t* srow = nullptr;
     while (true) {
@@ -719,7 +724,6 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
         uend += static_cast<uint32_t>((nk + nl) * C::CPS);
         LM = p.layer[j].M;
         Lr = p.layer[j].r;
-        Lpexp = p.layer[j].pexp;
         LB = p.layer[j].B;
         n = nt * 128 + row;
         srow = p.layer[j].scales + static_cast<int64_t>(n) * (p.layer[j].K / 16);
@@ -751,15 +755,6 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
           }
           if (q == 2 && lane == 0) QRR_STAMP(4, 3, chunk);
           if (!free || !mbar_wait(&sh.full[sidx], (sseq / C::STAGES) & 1, abort, p.status)) break;
-          // a LoRA chunk reads the t' tile (and the per-token exponents) that
-          // the prologue kernel wrote
-          if (c >= nk) {
-            griddep_wait();
-            // the f16 path rescales the t' tile in shared memory: it must
-            // have landed
-            if constexpr (F16)
-              if (!mbar_wait(&sh.full_x[sidx], (sseq / C::STAGES) & 1, abort, p.status)) break;
-          }
           if (q == 2 && lane == 0) QRR_STAMP(4, 1, chunk);
           if (q != 2 && lane == 0) QRR_STAMP(5 + (q == 3 ? 2 : q), 1, chunk);
           tc_fence_after();
@@ -793,32 +788,14 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
               tmem_st32(a_addr + 32 * h, out);
             }
           } else {
-            if constexpr (F16) {
-              // t' holds (alpha/r) t / g; the f16 path's accumulator carries
-              // the per-token factor 2^-p_m, so scale this chunk's t' rows by
-              // it (exact) before the tensor core reads them
-              const int tig = q * 32 + lane;
-              constexpr int PIECES = (C::ACH / 64) * BN * 8;
-              const int m0 = mt * BN;
-              for (int idx = tig; idx < PIECES; idx += 128) {
-                const int sub = idx / (BN * 8), rem = idx % (BN * 8), mr = rem >> 3;
-                if (m0 + mr >= LM) continue;
-                uint4* pc = reinterpret_cast<uint4*>(const_cast<uint8_t*>(stage) +
-                                                     (hc * (C::ACH / 64) + sub) * C::X_SUB + mr * 128 +
-                                                     (rem & 7) * 16);
-                const Pow2Scaler sc(Lpexp[m0 + mr]);
-                uint4 v = *pc;
-                uint32_t* wv = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) wv[e] = pack_bf16x2(sc(bf16_lo(wv[e])), sc(bf16_hi(wv[e])));
-                *pc = v;
-              }
-              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            }
             // LoRA chunk: A word i holds (B[n, rb+i], B[n, rb+i]) against the
-            // (high, low) halves of t'; zero past rank r
+            // (high, low) halves of t' (on the f16 path the prologue wrote t'
+            // already scaled by the token's 2^-p_m, the factor the
+            // accumulator carries); zero past rank r.  The decode tile's B
+            // rows sit in the stage's code slot, row-major [128][r].
             const int rb = (c - nk) * (BK / 2) + hc * (C::ACH / 2);
-            const uint16_t* brow = LB + static_cast<int64_t>(n) * Lr + rb;
+            const uint16_t* brow = F16 ? reinterpret_cast<const uint16_t*>(stage + C::X_BYTES) + row * Lr + rb
+                                       : LB + static_cast<int64_t>(n) * Lr + rb;
 #pragma unroll
             for (int h = 0; h < C::ACH / 64; ++h) {
               uint32_t out[32];
@@ -826,7 +803,12 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
               for (int v4 = 0; v4 < 4; ++v4) {
                 const int v8 = 4 * h + v4;
                 uint4 bv = make_uint4(0, 0, 0, 0);
-                if (rb + 8 * v8 < Lr) bv = __ldg(reinterpret_cast<const uint4*>(brow) + v8);
+                if (rb + 8 * v8 < Lr) {
+                  if constexpr (F16)
+                    bv = reinterpret_cast<const uint4*>(brow)[v8];
+                  else
+                    bv = __ldg(reinterpret_cast<const uint4*>(brow) + v8);
+                }
                 const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
