@@ -58,6 +58,7 @@ struct LinPlan {
   bool f16;
   bool pair;  // 256-token tiles on CTA pairs (2-CTA clusters), each pair two 128-row tiles
   int bn, bk, m_tiles, count;
+  bool sk;  // decode with a stream-K table (else one unit per tile)
   struct Layer {
     int n_tiles, splits, kcps, lora_chunks;
     size_t t_off, x16_off, p_off, part_off, cnt_off;
@@ -65,10 +66,14 @@ struct LinPlan {
   size_t cnt_begin, cnt_bytes, total;
 };
 
-// Decode (<= 64 tokens) takes the f16 operand path and splits K; the split
-// length (in pipeline stages) is the one that best fills whole waves of the
-// SMs across all layers of the call, with each layer's fp32 partials capped
-// at about a quarter of its weight bytes.  Prefill runs one unit per tile.
+// Decode (<= 64 tokens) takes the f16 operand path.  Up to 32 tokens the
+// stages of all its tiles are cut into one contiguous range per SM
+// (stream-K): a tile split across CTAs writes fp32 partials, one slot per
+// piece, and the piece that finishes last sums them in piece order.  At more
+// tokens a partial costs as much as a few stages, so K is split per layer by
+// a length that fills whole waves of the SMs (each layer's partials capped at
+// about a quarter of its weight bytes) and the units go to the CTAs longest
+// first.  Prefill runs one unit per tile.
 LinPlan plan_linear(int64_t M, const LinIn* in, int count) {
   LinPlan p{};
   const bool decode = M <= 64;
@@ -94,7 +99,24 @@ LinPlan plan_linear(int64_t M, const LinIn* in, int count) {
   // token tile, so each SM streams half of x.
   p.pair = !decode && p.bn == 256;
   for (int j = 0; j < count; ++j) p.pair = p.pair && p.l[j].n_tiles % 2 == 0;
-  if (decode) {
+  if (decode && M <= 32) {
+    // the layers the launch will carry (those with N and K), as it will
+    int skc[kMaxW4Layers], nl[kMaxW4Layers], nt[kMaxW4Layers], mt[kMaxW4Layers], pieces[kMaxW4Layers];
+    int idx[kMaxW4Layers];
+    int n = 0;
+    for (int j = 0; j < count; ++j) {
+      if (in[j].N == 0 || in[j].K == 0) continue;
+      skc[n] = static_cast<int>(in[j].K / p.bk);
+      nl[n] = in[j].r > 0 ? 1 : 0;
+      nt[n] = p.l[j].n_tiles;
+      mt[n] = p.m_tiles;
+      idx[n++] = j;
+    }
+    p.sk = stream_k_units(skc, nl, nt, mt, n, decode_grid(), nullptr, pieces) >= 0;
+    if (p.sk)
+      for (int i = 0; i < n; ++i) p.l[idx[i]].splits = pieces[i];  // partial slots
+  }
+  if (decode && !p.sk) {
     // Cost model in pipeline stages: a unit costs its K stages plus its
     // epilogue (about half a stage, or three when it writes a split-K partial
     // and may run the reduction); units go round-robin to the SMs, so the
@@ -271,9 +293,21 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
     any_split = any_split || pj.splits > 1;
   }
   if (p.count == 0) return QRR_OK;
+  if (pl.f16 && pl.sk) {
+    int kc[kMaxW4Layers], nl[kMaxW4Layers], nt[kMaxW4Layers], mt[kMaxW4Layers], pieces[kMaxW4Layers];
+    for (int j = 0; j < p.count; ++j) {
+      kc[j] = p.layer[j].K / pl.bk;
+      nl[j] = p.layer[j].r > 0 ? 1 : 0;
+      nt[j] = p.layer[j].n_tiles;
+      mt[j] = p.layer[j].m_tiles;
+    }
+    if (stream_k_units(kc, nl, nt, mt, p.count, decode_grid(), &p, pieces) < 0) return QRR_ERR_UNSUPPORTED_SHAPE;
+  } else if (pl.f16) {
+    lpt_units(p, pl.bk, decode_grid());  // no table (round-robin) when it does not fit
+  }
   if (pl.f16) {
-    // split-K is planned for decode only, and its counters are cleared by the
-    // prologue, which the GEMM waits for before it touches them
+    // split tiles occur on the decode path only, and their counters are
+    // cleared by the prologue, which the GEMM waits for before it touches them
     if (any_split) {
       db.clear = reinterpret_cast<uint32_t*>(ws + pl.cnt_begin);
       db.clear_words = static_cast<int>(pl.cnt_bytes / 4);

@@ -34,21 +34,40 @@ struct W4Layer {
   int first_unit;
 };
 
-// Per-CTA unit lists of a launch (single CTAs): CTA b takes units
-// sched[sched_off[b] .. sched_off[b + 1]) in that order.  Without a list
-// (use_sched == 0, and always for CTA pairs) units go round-robin.
-constexpr int kMaxSchedUnits = 2048;
-constexpr int kMaxSchedCtas = 160;
+// Unit table of a decode launch: CTA b takes units
+// unit[unit_off[b] .. unit_off[b + 1]) in that order, each a contiguous piece
+// of one tile's stage sequence (a stream-K range, or one split of a per-layer
+// split-K).  Word 0: layer (4 bits), m tile (4), n tile (16), the tile's
+// piece count (8); word 1: first K stage (12), K stages (11), the piece's
+// index within its tile (8), LoRA stage (1).  Without a table (use_table 0)
+// the units go round-robin.
+constexpr int kMaxTableUnits = 1024;
+constexpr int kMaxTableCtas = 160;
 
 struct W4Params {
   W4Layer layer[kMaxW4Layers];
   int count;
   int total_units;
   int32_t* status;
-  int use_sched;
-  uint16_t sched_off[kMaxSchedCtas + 1];
-  uint16_t sched[kMaxSchedUnits];
+  int use_table, table_grid;
+  uint16_t unit_off[kMaxTableCtas + 1];
+  uint32_t unit[kMaxTableUnits][2];
 };
+
+// The stream-K cut of a decode launch over `grid` CTAs: the stages of every
+// tile (its K stages, then its LoRA stage), tile after tile and layer after
+// layer, in `grid` ranges of equal length.  kc / nl / tiles per layer;
+// writes the units and offsets when `p` is given, and each layer's largest
+// piece count.  Returns the number of units, or -1 when a field does not fit
+// its bits or the table is too small.
+int stream_k_units(const int* kc, const int* nl, const int* n_tiles, const int* m_tiles, int count, int grid,
+                   W4Params* p, int* max_pieces);
+// The units of a launch with per-layer splits (L.splits, L.kcps), given to
+// `grid` CTAs longest first, as a unit table; leaves p.use_table 0 when the
+// table cannot hold them.
+void lpt_units(W4Params& p, int bk, int grid);
+// CTAs of a decode launch (the SM count of the current device).
+int decode_grid();
 
 // Prologue of one layer (lora_tc.cu): the LoRA down projection on the tensor
 // cores into t' (ks > 1: split over K slices of slice_steps x 64 with fp32

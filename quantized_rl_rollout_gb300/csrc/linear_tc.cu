@@ -50,13 +50,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include <string.h>
-
 #include <algorithm>
-#include <mutex>
-#include <queue>
 #include <type_traits>
-#include <utility>
 #include <vector>
 
 #include "linear.cuh"
@@ -264,13 +259,13 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
   const uint32_t rank = PAIR ? cluster_rank() : 0u;
   const int ustart = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int ustep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-  // this CTA's units: a list balanced by cost on the host when given,
-  // round-robin otherwise; unit_at(i) is the i-th of them
-  const bool sched = !PAIR && p.use_sched;
-  const int sched0 = sched ? p.sched_off[blockIdx.x] : 0;
-  const int n_my = sched ? p.sched_off[blockIdx.x + 1] - sched0
-                         : (ustart < p.total_units ? (p.total_units - 1 - ustart) / ustep + 1 : 0);
-  auto unit_at = [&](int i) { return sched ? static_cast<int>(p.sched[sched0 + i]) : ustart + i * ustep; };
+  // this CTA's units: its slice of the unit table (decode), round-robin
+  // otherwise; unit_at(i) is the i-th of them
+  const bool sk = !PAIR && p.use_table;
+  const int sk0 = sk ? p.unit_off[blockIdx.x] : 0;
+  const int n_my = sk ? p.unit_off[blockIdx.x + 1] - sk0
+                      : (ustart < p.total_units ? (p.total_units - 1 - ustart) / ustep + 1 : 0);
+  auto unit_at = [&](int i) { return sk ? sk0 + i : ustart + i * ustep; };
   // Every wait acquires at CTA scope, which keeps the SM's L1 contents valid
   // across it: what the peer CTA of a pair hands over through a barrier is
   // tensor-memory state, TMA bytes or tensor-core completion, none of it
@@ -323,8 +318,20 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
   tc_fence_after();
   const uint32_t tmem = sh.tmem;
 
-  // unit -> (layer, n tile, m tile, split, stage range, LoRA stages)
+  // unit -> (layer, n tile, m tile, piece, stage range, LoRA stages); the
+  // tile's piece count is unit_pieces(u)
   auto locate = [&](int u, int& j, int& nt, int& mt, int& sp, int& c0, int& nk, int& nl) {
+    if (sk) {
+      const uint32_t w0 = p.unit[u][0], w1 = p.unit[u][1];
+      j = static_cast<int>(w0 & 0xFu);
+      mt = static_cast<int>((w0 >> 4) & 0xFu);
+      nt = static_cast<int>((w0 >> 8) & 0xFFFFu);
+      c0 = static_cast<int>(w1 & 0xFFFu);
+      nk = static_cast<int>((w1 >> 12) & 0x7FFu);
+      sp = static_cast<int>((w1 >> 23) & 0xFFu);
+      nl = static_cast<int>(w1 >> 31);
+      return;
+    }
     j = 0;
     while (j + 1 < p.count && p.layer[j + 1].first_unit <= u) ++j;
     const W4Layer& L = p.layer[j];
@@ -340,6 +347,8 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
     nl = (L.r > 0 && sp == L.splits - 1) ? (L.lora_chunks + KSUB - 1) / KSUB : 0;
     if constexpr (PAIR) nt = 2 * nt + static_cast<int>(rank);
   };
+
+  auto unit_pieces = [&](int u, int j) { return sk ? static_cast<int>(p.unit[u][0] >> 24) : p.layer[j].splits; };
 
   if (warp == kTma) {
     // ------------------------------ TMA ------------------------------
@@ -540,7 +549,8 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
     for (int ui = 0; ui < n_my; ++ui, ++units) {
       int j, nt, mt, sp, c0, nk, nl;
       locate(unit_at(ui), j, nt, mt, sp, c0, nk, nl);
-      const int M = p.layer[j].M, N = p.layer[j].N, splits = p.layer[j].splits, n_tiles = p.layer[j].n_tiles;
+      const int M = p.layer[j].M, N = p.layer[j].N, n_tiles = p.layer[j].n_tiles;
+      const int splits = unit_pieces(unit_at(ui), j);  // pieces of this tile
       const int* const pexp = p.layer[j].pexp;
       __nv_bfloat16* const y = p.layer[j].y;
       float* const partial = p.layer[j].partial;
@@ -895,75 +905,153 @@ cudaError_t launch_bn(const W4Params& p, int grid, bool after_prologue, cudaStre
 
 }  // namespace
 
-// Longest-processing-time-first assignment of the units to `grid` CTAs: a
-// unit costs its K stages (weights and LoRA) plus its epilogue (about half a
-// stage, or three when it writes a split-K partial and may run the
-// reduction); each unit in turn, costliest first, goes to the least loaded
-// CTA, which then processes its units in index order.  The last schedule is
-// kept and reused while the launch's shape repeats.
-void build_schedule(W4Params& p, int grid, int bk) {
-  struct Key {
-    int grid, bk, count, n[kMaxW4Layers][5];
-    bool operator==(const Key& o) const { return memcmp(this, &o, sizeof(Key)) == 0; }
-  };
-  static std::mutex mu;
-  static Key last_key;
-  static bool have = false;
-  static uint16_t last_off[kMaxSchedCtas + 1];
-  static uint16_t last_sched[kMaxSchedUnits];
-  Key key;
-  memset(&key, 0, sizeof(key));
-  key.grid = grid;
-  key.bk = bk;
-  key.count = p.count;
-  for (int j = 0; j < p.count; ++j) {
-    const W4Layer& L = p.layer[j];
-    key.n[j][0] = L.n_tiles;
-    key.n[j][1] = L.m_tiles;
-    key.n[j][2] = L.splits;
-    key.n[j][3] = L.kcps;
-    key.n[j][4] = L.K * 1024 + L.lora_chunks;
+int decode_grid() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return kSMs;
   }
-  std::lock_guard<std::mutex> lock(mu);
-  if (!have || !(key == last_key)) {
-    const int units = p.total_units;
-    std::vector<std::pair<double, int>> cost(units);
-    for (int j = 0; j < p.count; ++j) {
-      const W4Layer& L = p.layer[j];
-      const int kc = L.K / bk, ksub = bk / 64;
-      const int per = L.n_tiles * L.m_tiles;
-      for (int local = 0; local < per * L.splits; ++local) {
-        const int sp = local / per;
-        const int nk = std::min((sp + 1) * L.kcps, kc) - sp * L.kcps;
-        const int nl = (L.r > 0 && sp == L.splits - 1) ? (L.lora_chunks + ksub - 1) / ksub : 0;
-        cost[L.first_unit + local] = {nk + nl + (L.splits > 1 ? 3.0 : 0.5), L.first_unit + local};
+  if (cached[dev] == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+      cudaGetLastError();
+      sms = kSMs;
+    }
+    cached[dev] = sms < kMaxTableCtas ? sms : kMaxTableCtas;
+  }
+  return cached[dev];
+}
+
+int stream_k_units(const int* kc, const int* nl, const int* n_tiles, const int* m_tiles, int count, int grid,
+                   W4Params* p, int* max_pieces) {
+  long long total = 0;
+  for (int j = 0; j < count; ++j) {
+    max_pieces[j] = 1;
+    total += static_cast<long long>(n_tiles[j]) * m_tiles[j] * (kc[j] + nl[j]);
+  }
+  if (total == 0 || count > 16) return total == 0 ? 0 : -1;
+  if (grid > total) grid = static_cast<int>(total);
+  if (grid < 1 || grid > kMaxTableCtas) return -1;
+  struct Seg {
+    int j, t, s0, s1;
+  };
+  std::vector<Seg> seg;
+  std::vector<int> first(grid + 1);
+  int j = 0, t = 0;
+  long long ts = 0;  // first stage of tile (j, t)
+  for (int b = 0; b < grid; ++b) {
+    const long long lo = total * b / grid, hi = total * (b + 1) / grid;
+    first[b] = static_cast<int>(seg.size());
+    long long pos = lo;
+    while (pos < hi) {
+      while (n_tiles[j] * m_tiles[j] == 0 || kc[j] + nl[j] == 0) {  // layers without stages
+        ++j;
+        t = 0;
+      }
+      const long long len = kc[j] + nl[j];
+      const long long end = hi < ts + len ? hi : ts + len;
+      seg.push_back({j, t, static_cast<int>(pos - ts), static_cast<int>(end - ts)});
+      pos = end;
+      if (end == ts + len) {  // next tile
+        ts += len;
+        if (++t == n_tiles[j] * m_tiles[j]) {
+          ++j;
+          t = 0;
+        }
       }
     }
-    std::stable_sort(cost.begin(), cost.end(), [](const std::pair<double, int>& a, const std::pair<double, int>& b) {
-      return a.first > b.first;
-    });
-    std::priority_queue<std::pair<double, int>, std::vector<std::pair<double, int>>, std::greater<>> load;
-    for (int b = 0; b < grid; ++b) load.push({0.0, b});
-    std::vector<std::vector<int>> mine(grid);
-    for (const auto& c : cost) {
-      auto top = load.top();
-      load.pop();
-      mine[top.second].push_back(c.second);
-      load.push({top.first + c.first, top.second});
-    }
-    int off = 0;
-    for (int b = 0; b < grid; ++b) {
-      std::sort(mine[b].begin(), mine[b].end());
-      last_off[b] = static_cast<uint16_t>(off);
-      for (int u : mine[b]) last_sched[off++] = static_cast<uint16_t>(u);
-    }
-    last_off[grid] = static_cast<uint16_t>(off);
-    last_key = key;
-    have = true;
   }
-  memcpy(p.sched_off, last_off, sizeof(uint16_t) * (grid + 1));
-  memcpy(p.sched, last_sched, sizeof(uint16_t) * p.total_units);
-  p.use_sched = 1;
+  first[grid] = static_cast<int>(seg.size());
+  const int n = static_cast<int>(seg.size());
+  if (n > kMaxTableUnits) return -1;
+  // a tile's pieces are consecutive: index within the tile and tile counts
+  std::vector<int> sp(n), pieces(n);
+  for (int i = 0; i < n; ++i) sp[i] = (i > 0 && seg[i - 1].j == seg[i].j && seg[i - 1].t == seg[i].t) ? sp[i - 1] + 1 : 0;
+  for (int i = n - 1; i >= 0; --i)
+    pieces[i] = (i + 1 < n && seg[i + 1].j == seg[i].j && seg[i + 1].t == seg[i].t) ? pieces[i + 1] : sp[i] + 1;
+  for (int i = 0; i < n; ++i) {
+    const Seg& g = seg[i];
+    const int mt = g.t / n_tiles[g.j], nt = g.t % n_tiles[g.j];
+    const int K = kc[g.j];
+    const int c0 = g.s0 < K ? g.s0 : K;
+    const int nk = (g.s1 < K ? g.s1 : K) - c0;
+    const int l = (nl[g.j] > 0 && g.s1 > K) ? 1 : 0;
+    if (mt > 15 || nt > 0xFFFF || pieces[i] > 0xFF || c0 > 0xFFF || nk > 0x7FF || sp[i] > 0xFF) return -1;
+    max_pieces[g.j] = pieces[i] > max_pieces[g.j] ? pieces[i] : max_pieces[g.j];
+    if (p != nullptr) {
+      p->unit[i][0] = static_cast<uint32_t>(g.j) | static_cast<uint32_t>(mt) << 4 | static_cast<uint32_t>(nt) << 8 |
+                      static_cast<uint32_t>(pieces[i]) << 24;
+      p->unit[i][1] = static_cast<uint32_t>(c0) | static_cast<uint32_t>(nk) << 12 |
+                      static_cast<uint32_t>(sp[i]) << 23 | static_cast<uint32_t>(l) << 31;
+    }
+  }
+  if (p != nullptr) {
+    for (int b = 0; b <= grid; ++b) p->unit_off[b] = static_cast<uint16_t>(first[b]);
+    p->use_table = 1;
+    p->table_grid = grid;
+    p->total_units = n;
+  }
+  return n;
+}
+
+// Longest processing time first: a unit costs its K stages plus its LoRA
+// stage plus its epilogue (about half a stage, or three when it writes a
+// split-K partial and may run the reduction); each unit in turn, costliest
+// first, goes to the least loaded CTA, which takes its units in index order.
+void lpt_units(W4Params& p, int bk, int grid) {
+  p.use_table = 0;
+  struct U {
+    double cost;
+    int j, mt, nt, sp, c0, nk, nl, pieces;
+  };
+  std::vector<U> us;
+  for (int j = 0; j < p.count; ++j) {
+    const W4Layer& L = p.layer[j];
+    const int kc = L.K / bk, ksub = bk / 64;
+    for (int sp = 0; sp < L.splits; ++sp)
+      for (int mt = 0; mt < L.m_tiles; ++mt)
+        for (int nt = 0; nt < L.n_tiles; ++nt) {
+          const int c0 = sp * L.kcps;
+          const int nk = std::min(c0 + L.kcps, kc) - c0;
+          const int nl = (L.r > 0 && sp == L.splits - 1) ? (L.lora_chunks + ksub - 1) / ksub : 0;
+          us.push_back({nk + nl + (L.splits > 1 ? 3.0 : 0.5), j, mt, nt, sp, c0, nk, nl, L.splits});
+        }
+  }
+  const int n = static_cast<int>(us.size());
+  if (n == 0 || n > kMaxTableUnits || p.count > 16) return;
+  if (grid > n) grid = n;
+  if (grid < 1 || grid > kMaxTableCtas) return;
+  std::vector<int> order(n);
+  for (int i = 0; i < n; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return us[a].cost > us[b].cost; });
+  std::vector<double> load(grid, 0.0);
+  std::vector<std::vector<int>> mine(grid);
+  for (int i : order) {
+    int best = 0;
+    for (int b = 1; b < grid; ++b)
+      if (load[b] < load[best]) best = b;
+    load[best] += us[i].cost;
+    mine[best].push_back(i);
+  }
+  int k = 0;
+  for (int b = 0; b < grid; ++b) {
+    std::sort(mine[b].begin(), mine[b].end());
+    p.unit_off[b] = static_cast<uint16_t>(k);
+    for (int i : mine[b]) {
+      const U& u = us[i];
+      if (u.mt > 15 || u.nt > 0xFFFF || u.pieces > 0xFF || u.c0 > 0xFFF || u.nk > 0x7FF || u.sp > 0xFF) return;
+      p.unit[k][0] = static_cast<uint32_t>(u.j) | static_cast<uint32_t>(u.mt) << 4 |
+                     static_cast<uint32_t>(u.nt) << 8 | static_cast<uint32_t>(u.pieces) << 24;
+      p.unit[k][1] = static_cast<uint32_t>(u.c0) | static_cast<uint32_t>(u.nk) << 12 |
+                     static_cast<uint32_t>(u.sp) << 23 | static_cast<uint32_t>(u.nl) << 31;
+      ++k;
+    }
+  }
+  p.unit_off[grid] = static_cast<uint16_t>(k);
+  p.total_units = n;
+  p.table_grid = grid;
+  p.use_table = 1;
 }
 
 int w4_bn_for(int64_t M) {
@@ -981,6 +1069,15 @@ int w4_bk_for(int64_t M) { return M <= 64 ? 256 : 64; }
 // after_prologue: the previous kernel in the stream is the prologue that
 // writes x16 / pexp / t'; this launch may then start before it completes.
 cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, bool pair, bool after_prologue, cudaStream_t stream) {
+  if (p.use_table) {
+    // decode with the unit table the caller built for its grid
+    if (p.total_units == 0) return cudaSuccess;
+    switch (bn) {
+      case 16: return launch_bn<16, 256, true, kDecodeGroups>(p, p.table_grid, after_prologue, stream);
+      case 32: return launch_bn<32, 256, true, kDecodeGroups>(p, p.table_grid, after_prologue, stream);
+      default: return launch_bn<64, 256, true, kDecodeGroups>(p, p.table_grid, after_prologue, stream);
+    }
+  }
   int units = 0;
   for (int j = 0; j < p.count; ++j) {
     p.layer[j].first_unit = units;
@@ -991,8 +1088,6 @@ cudaError_t launch_w4a16_tc(W4Params& p, int bn, bool f16, bool pair, bool after
   int dev = 0, sms = kSMs;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = units < sms ? units : sms;
-  p.use_sched = 0;
-  if (!pair && units <= kMaxSchedUnits && grid <= kMaxSchedCtas) build_schedule(p, grid, f16 ? 256 : 64);
   if (f16) {
     switch (bn) {
       case 16: return launch_bn<16, 256, true, kDecodeGroups>(p, grid, after_prologue, stream);
