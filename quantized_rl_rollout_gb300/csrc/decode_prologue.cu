@@ -169,26 +169,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_prologue_kernel(const __gr
       if (mma) (void)mbar_wait(&sh.round_done, (round - 1) & 1, abort, b.status);
       __syncthreads();
     }
-    for (int i = tid; i < n * rows_step * 8; i += kThreads) {
-      const int st = i / (rows_step * 8), rem = i - st * rows_step * 8;
-      const int row = rem >> 3, pc = rem & 7;
-      const int kcol = (k0 + c0 + st) * 64 + pc * 8;
-      uint8_t* dst;
-      const uint16_t* src;
-      bool valid;
-      if (row < XR) {
-        dst = xs + st * XR * 128 + row * 128 + ((pc ^ (row & 7)) << 4);
-        valid = row < M;
-        src = xg + static_cast<int64_t>(valid ? row : 0) * K + kcol;
-      } else {
-        const int ar = row - XR;
-        dst = as + st * R * 128 + ar * 128 + ((pc ^ (ar & 7)) << 4);
-        valid = ar < r;
-        src = ag + static_cast<int64_t>(valid ? ar : 0) * K + kcol;
+    {
+      // thread: 16-byte piece tid % 8 of rows tid / 8, tid / 8 + 24, ...
+      const int pc = tid & 7;
+      for (int row = tid >> 3; row < rows_step; row += kThreads / 8) {
+        const bool is_x = row < XR;
+        const int rr = is_x ? row : row - XR;
+        const bool valid = is_x ? rr < M : rr < r;
+        const uint16_t* src = (is_x ? xg : ag) + static_cast<int64_t>(valid ? rr : 0) * K + (k0 + c0) * 64 + pc * 8;
+        uint8_t* dst = (is_x ? xs : as) + rr * 128 + ((pc ^ (rr & 7)) << 4);
+        const int dstep = is_x ? XR * 128 : R * 128;
+        for (int st = 0; st < n; ++st)
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst + st * dstep)),
+                       "l"(src + st * 64), "r"(valid ? 16 : 0)
+                       : "memory");
       }
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-                   "r"(valid ? 16 : 0)
-                   : "memory");
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     // the copies were made through the generic proxy; the MMA reads through
@@ -289,9 +284,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_prologue_kernel(const __gr
     const int nvec = steps * 8;  // 16-byte vectors per token row of the slice
     const bool resident = steps <= S;  // one round: step c still sits in slot c
     __half* const x16 = L.x16;
-    const uint16_t* const xg = L.x;
-    for (int i = tid; i < M * nvec; i += kThreads) {
-      const int m = i / nvec, v = i - m * nvec;
+    // element i = m nvec + v, stepped by kThreads without a division per step
+    const int dm = nvec > 0 ? kThreads / nvec : 0, dv = kThreads - dm * nvec;
+    int m = nvec > 0 ? tid / nvec : M, v = tid - m * nvec;
+    for (; m < M; m += dm, v += dv) {
+      if (v >= nvec) {
+        v -= nvec;
+        ++m;
+        if (m >= M) break;
+      }
       const int c = v >> 3, pc = v & 7;
       uint4 xv;
       if (resident)
