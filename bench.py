@@ -584,10 +584,14 @@ def run_phase(w, name):
 
 
 def timed_steps(w, steps, phases):
-    """Per-phase device ms (lists over steps) and kernel launches in the timed region."""
+    """Per-phase device ms (lists over steps) and kernel launches in the timed region.
+    The region is an NVTX range "timed" (free without a tool attached), so a
+    profiler can be limited to the timed launches (ncu --nvtx --nvtx-include
+    "timed/")."""
     stream = torch.cuda.current_stream()
     times = {p: [] for p in phases}
     launches = 0
+    torch.cuda.nvtx.range_push("timed")
     for _ in range(steps):
         w.next_step()
         for p in phases:
@@ -598,6 +602,7 @@ def timed_steps(w, steps, phases):
             launches += run_phase(w, p)
             e1.record(stream)
             times[p].append((e0, e1))
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     out = {p: [a.elapsed_time(b) for a, b in times[p]] for p in phases}
     return out, launches
