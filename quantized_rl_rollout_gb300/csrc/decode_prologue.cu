@@ -17,8 +17,8 @@
 //               the 128-row x operand reads past the XR staged rows into
 //               whatever follows in shared memory, which only reaches
 //               accumulator rows that are never read
-//   warps 2..5  per-token max |x| over the staged tiles; then t_c from TMEM
-//               into shared memory
+//   warps 2..5  per-token max |x| over the staged tiles; then (warps 4 and 5,
+//               TMEM lane quarters 0 and 1) t_c from TMEM into shared memory
 // and then, across the cluster through distributed shared memory, every CTA
 // takes the token maxima over all slices and writes the f16 image of its own
 // slice, and the t outputs are divided among the CTAs, each summing the ks
@@ -54,7 +54,7 @@ __device__ unsigned long long qrr_dtrace_buf[128][16];
 namespace {
 
 constexpr int kKsMax = 16;  // CTAs per cluster = K slices per layer (16: a non-portable cluster size)
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;  // 12 warps: roles in warps 0..5, all share the copies and conversions
 constexpr int kMaxXR = 64;
 constexpr int kMaxR = 64;
 constexpr int kMaxStages = 32;
@@ -137,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_prologue_kernel(const __gr
   const bool lora = r > 0;
   const bool mma = lora && steps > 0;
   volatile int* abort = &sh.abort;
+  const float st = lora ? *L.tensor_scale : 1.0f;  // read early: it is needed only at the end
 
   if (tid == 0) {
     mbar_init(&sh.round_done, 1);
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_prologue_kernel(const __gr
         mma_commit(c0 + n < steps ? &sh.round_done : &sh.d_full);
       }
       __syncwarp();
-    } else if (warp >= 2) {
+    } else if (warp >= 2 && warp < 6) {
       // per-token max |x| over the round's tiles; the swizzle only permutes
       // pieces within a row, which a maximum ignores
       for (int c = 0; c < n; ++c) {
@@ -218,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_prologue_kernel(const __gr
       }
     }
   }
-  if (warp >= 2) {
+  if (warp >= 2 && warp < 6) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       mx[i] = max(mx[i], __shfl_xor_sync(0xFFFFFFFFu, mx[i], 1));
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_prologue_kernel(const __gr
     }
     if (et == 0) QRR_DSTAMP(2);
     // t of this slice: the two warps on TMEM lane quarters 0 and 1 (tokens 0..63)
-    if (lora && (warp & 3) < 2) {
+    if (lora && warp >= 4) {
       const int q = warp & 3;
       const int m = 32 * q + lane;
       bool have = mma && mbar_wait(&sh.d_full, 0, abort, b.status);
@@ -302,10 +303,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_prologue_kernel(const __gr
       const Pow2Scaler sc(sh.pexp[m]);
       const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
       uint32_t o[4];
+      if (sc.f2 == 1.0f) {  // 2^-p a normal fp32 number: one exact multiply
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const __half2 h = __floats2half2_rn(sc(bf16_lo(w[u])), sc(bf16_hi(w[u])));
-        o[u] = *reinterpret_cast<const uint32_t*>(&h);
+        for (int u = 0; u < 4; ++u) {
+          const __half2 h = __floats2half2_rn(__fmul_rn(bf16_lo(w[u]), sc.f1), __fmul_rn(bf16_hi(w[u]), sc.f1));
+          o[u] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const __half2 h = __floats2half2_rn(sc(bf16_lo(w[u])), sc(bf16_hi(w[u])));
+          o[u] = *reinterpret_cast<const uint32_t*>(&h);
+        }
       }
       *(reinterpret_cast<uint4*>(x16 + static_cast<int64_t>(m) * K + (k0 + c) * 64) + pc) =
           make_uint4(o[0], o[1], o[2], o[3]);
@@ -316,7 +325,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_prologue_kernel(const __gr
   // t': the outputs divided among the cluster, each the slice partials
   // summed in slice order
   if (lora) {
-    const float st = *L.tensor_scale;
     const float g = st > 0.0f ? st : 1.0f;
     const float lscale = L.lora_scale;
     __nv_bfloat16* const t = L.t;
