@@ -366,6 +366,29 @@ typedef enum qrr_op {
 } qrr_op;
 size_t qrr_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t r);
 
+/* Host-only query of how a decode call (qrr_linear_nvfp4_lora_grouped at
+ * 1 <= M <= 64 tokens) divides its work among `grid` CTAs; it launches
+ * nothing and needs no GPU.  Every tile (128 weight rows of one layer, all M
+ * tokens) is a sequence of K / 256 weight stages followed, when the layer
+ * has an adapter (r > 0), by one LoRA stage.  Up to 32 tokens the stages of
+ * all tiles, layer after layer, are cut into equal contiguous ranges, one
+ * per CTA (stream-K); above, each layer's K is split into equal pieces and
+ * the pieces go to the CTAs longest first.
+ *   count        layers, 1..8; N[j] % 128 == 0, K[j] % 256 == 0, K[j] > 0,
+ *                N[j] > 0, r[j] in {0} or a multiple of 8 up to 64
+ *   grid         CTAs offered, 1..160 (fewer are used when there are fewer
+ *                stages); *grid_used receives the number used
+ *   units        host [max_units][2] uint32: word 0 = layer (bits 0-3), m tile
+ *                (4-7), n tile (8-23), the tile's piece count (24-31);
+ *                word 1 = first K stage (0-11), K stages (12-22), piece index
+ *                within the tile (23-30), LoRA stage (31)
+ *   offsets      host [grid + 1]: CTA b takes units offsets[b] .. offsets[b+1]
+ * Returns the number of units, or a negative qrr_status (invalid argument,
+ * unsupported shape, or a table larger than max_units). */
+int64_t qrr_plan_decode_units(int64_t M, int32_t count, const int64_t* N, const int64_t* K, const int32_t* r,
+                              int32_t grid, uint32_t* units, int32_t max_units, uint16_t* offsets,
+                              int32_t* grid_used);
+
 /* Probe of the bounded-wait path.  Every tensor-core pipeline wait of the
  * library gives up after a bounded time (about 2 s), raises QRR_DEV_TIMEOUT,
  * lets its CTA drain its copies, free its tensor memory and exit, so a broken

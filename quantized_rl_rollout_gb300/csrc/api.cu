@@ -796,6 +796,53 @@ size_t qrr_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int32_t 
   }
 }
 
+int64_t qrr_plan_decode_units(int64_t M, int32_t count, const int64_t* N, const int64_t* K, const int32_t* r,
+                              int32_t grid, uint32_t* units, int32_t max_units, uint16_t* offsets,
+                              int32_t* grid_used) {
+  if (!N || !K || !r || !units || !offsets || !grid_used || max_units < 0) return -QRR_ERR_INVALID_ARG;
+  if (M < 1 || M > 64 || count < 1 || count > kMaxW4Layers || grid < 1 || grid > kMaxTableCtas)
+    return -QRR_ERR_INVALID_ARG;
+  LinIn in[kMaxW4Layers];
+  for (int j = 0; j < count; ++j) {
+    if (N[j] <= 0 || K[j] <= 0 || N[j] % 128 != 0 || K[j] % 256 != 0 || N[j] > INT32_MAX || K[j] > INT32_MAX)
+      return -QRR_ERR_UNSUPPORTED_SHAPE;
+    if (r[j] < 0 || r[j] > 64 || r[j] % 8 != 0) return -QRR_ERR_UNSUPPORTED_SHAPE;
+    in[j] = LinIn{nullptr, N[j], K[j], nullptr, nullptr, nullptr, nullptr, nullptr, r[j], 0.0f, nullptr};
+  }
+  // the decode launch's own planning (run_linear): per-layer splits, then the table
+  const LinPlan pl = plan_linear(M, in, count);
+  W4Params p{};
+  p.count = count;
+  int kc[kMaxW4Layers], nl[kMaxW4Layers], nt[kMaxW4Layers], mt[kMaxW4Layers], pieces[kMaxW4Layers];
+  for (int j = 0; j < count; ++j) {
+    W4Layer& L = p.layer[j];
+    L.M = static_cast<int>(M);
+    L.N = static_cast<int>(N[j]);
+    L.K = static_cast<int>(K[j]);
+    L.r = r[j];
+    L.lora_chunks = pl.l[j].lora_chunks;
+    L.n_tiles = pl.l[j].n_tiles;
+    L.m_tiles = pl.m_tiles;
+    L.splits = pl.l[j].splits;
+    L.kcps = pl.l[j].kcps;
+    kc[j] = L.K / pl.bk;
+    nl[j] = r[j] > 0 ? 1 : 0;
+    nt[j] = L.n_tiles;
+    mt[j] = L.m_tiles;
+  }
+  if (pl.sk) {
+    if (stream_k_units(kc, nl, nt, mt, count, grid, &p, pieces) < 0) return -QRR_ERR_UNSUPPORTED_SHAPE;
+  } else {
+    lpt_units(p, pl.bk, grid);
+    if (!p.use_table) return -QRR_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (p.total_units > max_units) return -QRR_ERR_WORKSPACE;
+  memcpy(units, p.unit, sizeof(uint32_t) * 2 * static_cast<size_t>(p.total_units));
+  memcpy(offsets, p.unit_off, sizeof(uint16_t) * static_cast<size_t>(p.table_grid + 1));
+  *grid_used = p.table_grid;
+  return p.total_units;
+}
+
 qrr_status qrr_wait_probe(int64_t limit_cycles, int32_t arrive, int32_t* dev_status, int64_t* cycles, void* stream) {
   if (limit_cycles <= 0 || limit_cycles > kWaitLimitCycles || (arrive != 0 && arrive != 1)) return QRR_ERR_INVALID_ARG;
   if (!dev_status) return QRR_ERR_INVALID_ARG;

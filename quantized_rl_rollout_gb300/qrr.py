@@ -92,6 +92,7 @@ SIGNATURES = {
                                              _c_p]),
     "qrr_workspace_bytes": (_c_sz, [_c_i32, _c_i64, _c_i64, _c_i64, _c_i32]),
     "qrr_wait_probe": (ctypes.c_int, [_c_i64, _c_i32, _c_p, _c_p, _c_p]),
+    "qrr_plan_decode_units": (_c_i64, [_c_i64, _c_i32, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_p]),
 }
 
 _lib = None
@@ -341,6 +342,32 @@ def get_last_device_status(dev_status, stream=None) -> int:
 
 def workspace_bytes(op, M=0, N=0, K=0, r=0) -> int:
     return int(lib().qrr_workspace_bytes(int(op), int(M), int(N), int(K), int(r)))
+
+
+def plan_decode_units(M, shapes, grid, max_units=4096):
+    """The decode launch's unit table for layers ``shapes`` = [(N, K, r), ...]
+    at M tokens on ``grid`` CTAs (host only; see ``qrr_plan_decode_units``).
+
+    Returns ``(units, offsets)``: a list of decoded units (dicts with layer,
+    m_tile, n_tile, pieces, c0, nk, piece, lora) and the per-CTA offsets."""
+    n = len(shapes)
+    Ns = (ctypes.c_int64 * n)(*[int(s[0]) for s in shapes])
+    Ks = (ctypes.c_int64 * n)(*[int(s[1]) for s in shapes])
+    rs = (ctypes.c_int32 * n)(*[int(s[2]) for s in shapes])
+    units = (ctypes.c_uint32 * (2 * max_units))()
+    offsets = (ctypes.c_uint16 * (int(grid) + 1))()
+    used = ctypes.c_int32(0)
+    got = lib().qrr_plan_decode_units(int(M), n, ctypes.addressof(Ns), ctypes.addressof(Ks), ctypes.addressof(rs),
+                                      int(grid), ctypes.addressof(units), int(max_units), ctypes.addressof(offsets),
+                                      ctypes.addressof(used))
+    if got < 0:
+        raise QrrError(int(-got), "qrr_plan_decode_units")
+    out = []
+    for i in range(got):
+        w0, w1 = units[2 * i], units[2 * i + 1]
+        out.append(dict(layer=w0 & 0xF, m_tile=(w0 >> 4) & 0xF, n_tile=(w0 >> 8) & 0xFFFF, pieces=w0 >> 24,
+                        c0=w1 & 0xFFF, nk=(w1 >> 12) & 0x7FF, piece=(w1 >> 23) & 0xFF, lora=w1 >> 31))
+    return out, [int(offsets[b]) for b in range(used.value + 1)]
 
 
 def wait_probe(limit_cycles, arrive, dev_status, cycles=None, stream=None):
