@@ -50,7 +50,10 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <string.h>
+
 #include <algorithm>
+#include <mutex>
 #include <type_traits>
 #include <vector>
 
@@ -923,8 +926,10 @@ int decode_grid() {
   return cached[dev];
 }
 
-int stream_k_units(const int* kc, const int* nl, const int* n_tiles, const int* m_tiles, int count, int grid,
-                   W4Params* p, int* max_pieces) {
+namespace {
+
+int stream_k_units_build(const int* kc, const int* nl, const int* n_tiles, const int* m_tiles, int count, int grid,
+                         W4Params* p, int* max_pieces) {
   long long total = 0;
   for (int j = 0; j < count; ++j) {
     max_pieces[j] = 1;
@@ -999,7 +1004,7 @@ int stream_k_units(const int* kc, const int* nl, const int* n_tiles, const int* 
 // stage plus its epilogue (about half a stage, or three when it writes a
 // split-K partial and may run the reduction); each unit in turn, costliest
 // first, goes to the least loaded CTA, which takes its units in index order.
-void lpt_units(W4Params& p, int bk, int grid) {
+void lpt_units_build(W4Params& p, int bk, int grid) {
   p.use_table = 0;
   struct U {
     double cost;
@@ -1052,6 +1057,89 @@ void lpt_units(W4Params& p, int bk, int grid) {
   p.total_units = n;
   p.table_grid = grid;
   p.use_table = 1;
+}
+
+// The last few unit tables, kept while the caller repeats a launch shape
+// (decode calls cycle through a handful of token counts): building one walks
+// every stage or sorts every unit, host time that would otherwise be spent
+// on every call.
+struct TableEntry {
+  bool used = false;
+  std::vector<int> key;
+  int n = -1, grid_used = 0, use_table = 0;
+  int pieces[kMaxW4Layers];
+  uint16_t off[kMaxTableCtas + 1];
+  uint32_t unit[kMaxTableUnits][2];
+};
+std::mutex g_table_mu;
+TableEntry g_tables[4];
+int g_table_next = 0;
+W4Params g_table_scratch;  // guarded by g_table_mu
+
+TableEntry* table_find(const std::vector<int>& key) {
+  for (TableEntry& e : g_tables)
+    if (e.used && e.key == key) return &e;
+  TableEntry& e = g_tables[g_table_next];
+  g_table_next = (g_table_next + 1) % 4;
+  e.used = false;
+  e.key = key;
+  return &e;
+}
+
+void table_store(TableEntry& e, const W4Params& p, int n) {
+  e.n = n;
+  e.use_table = p.use_table;
+  e.grid_used = p.table_grid;
+  if (p.use_table) {
+    memcpy(e.off, p.unit_off, sizeof(uint16_t) * static_cast<size_t>(p.table_grid + 1));
+    memcpy(e.unit, p.unit, sizeof(uint32_t) * 2 * static_cast<size_t>(p.total_units));
+  }
+  e.used = true;
+}
+
+void table_load(const TableEntry& e, W4Params& p, int n_units) {
+  p.use_table = e.use_table;
+  if (!e.use_table) return;
+  p.table_grid = e.grid_used;
+  p.total_units = n_units;
+  memcpy(p.unit_off, e.off, sizeof(uint16_t) * static_cast<size_t>(e.grid_used + 1));
+  memcpy(p.unit, e.unit, sizeof(uint32_t) * 2 * static_cast<size_t>(n_units));
+}
+
+}  // namespace
+
+int stream_k_units(const int* kc, const int* nl, const int* n_tiles, const int* m_tiles, int count, int grid,
+                   W4Params* p, int* max_pieces) {
+  std::vector<int> key = {0, count, grid};
+  for (int j = 0; j < count; ++j) key.insert(key.end(), {kc[j], nl[j], n_tiles[j], m_tiles[j]});
+  std::lock_guard<std::mutex> lock(g_table_mu);
+  TableEntry* e = table_find(key);
+  if (!e->used) {
+    g_table_scratch.use_table = 0;
+    const int n = stream_k_units_build(kc, nl, n_tiles, m_tiles, count, grid, &g_table_scratch, e->pieces);
+    table_store(*e, g_table_scratch, n);
+  }
+  for (int j = 0; j < count; ++j) max_pieces[j] = e->pieces[j];
+  if (p != nullptr && e->n >= 0) table_load(*e, *p, e->n);
+  return e->n;
+}
+
+void lpt_units(W4Params& p, int bk, int grid) {
+  std::vector<int> key = {1, p.count, bk, grid};
+  for (int j = 0; j < p.count; ++j) {
+    const W4Layer& L = p.layer[j];
+    key.insert(key.end(), {L.n_tiles, L.m_tiles, L.splits, L.kcps, L.K, L.r, L.lora_chunks});
+  }
+  std::lock_guard<std::mutex> lock(g_table_mu);
+  TableEntry* e = table_find(key);
+  if (!e->used) {
+    g_table_scratch.count = p.count;
+    for (int j = 0; j < p.count; ++j) g_table_scratch.layer[j] = p.layer[j];
+    lpt_units_build(g_table_scratch, bk, grid);
+    table_store(*e, g_table_scratch, g_table_scratch.use_table ? g_table_scratch.total_units : -1);
+  }
+  p.use_table = 0;
+  if (e->n >= 0) table_load(*e, p, e->n);
 }
 
 int w4_bn_for(int64_t M) {
