@@ -244,6 +244,32 @@ def linear_nvfp4_lora_grouped(layers, workspace=None, dev_status=None, stream=No
     return [d["y"] for d in layers]
 
 
+class GroupedLinear:
+    """A grouped linear call prepared once, for the decode loop's case of
+    fixed buffers: the layers' tensors (x, weights, adapters, y) and the
+    workspace are bound at construction, checked once, and ``run()`` only
+    launches.  Refill x in place between runs; y is rewritten by each run.
+    The numbers are those of ``linear_nvfp4_lora_grouped`` on the same
+    tensors, bit for bit (it is the same C call)."""
+
+    def __init__(self, layers, workspace=None):
+        self.layers = layers
+        self.descs, self.m = _linear_descs(layers)
+        nbytes = int(lib().qrr_linear_nvfp4_lora_grouped_workspace_bytes(self.descs, len(layers), self.m))
+        if workspace is None:
+            workspace = _workspace(nbytes, layers[0]["x"].device)
+        elif workspace.numel() < nbytes:
+            raise ValueError(f"workspace of {workspace.numel()} bytes, the call needs {nbytes}")
+        self.workspace = workspace
+        self.outputs = [d["y"] for d in layers]
+        self._args = (self.descs, len(layers), self.m, _ptr(workspace), workspace.numel())
+        self._fn = lib().qrr_linear_nvfp4_lora_grouped
+
+    def run(self, dev_status=None, stream=None):
+        _check(self._fn(*self._args, _ptr(dev_status), _stream(stream)), "qrr_linear_nvfp4_lora_grouped")
+        return self.outputs
+
+
 def quantize_fp8_w128x128(W, mode=SCALE_FP32, q=None, scales=None, dev_status=None, stream=None):
     _need(W, torch.bfloat16, "W")
     n, k = W.shape

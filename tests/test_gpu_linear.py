@@ -370,3 +370,29 @@ def test_decode_nonfinite_x_flagged(q):
     q.linear_nvfp4_lora(x, codes, scales, ts, A, B, alpha, dev_status=st)
     torch.cuda.synchronize()
     assert q.get_last_device_status(st) & q.DEV_NONFINITE
+
+
+@pytest.mark.parametrize("m", [1, 64])
+def test_prepared_grouped_call(q, m):
+    """A GroupedLinear prepared once gives the bits of the one-shot grouped
+    call, and follows new tokens written into its x buffers in place."""
+    shapes = [(384, 1024, 32), (256, 2048, 0), (512, 768, 64)]
+    layers, ref_layers = [], []
+    for i, (n, k, r) in enumerate(shapes):
+        W, codes, scales, ts, A, B, alpha = _layer(q, n, k, r, f"prep{i}")
+        x = inputs.activations(m, k, inputs.derive_seed(0, "prep-x", i, m), device=DEV)
+        layers.append(dict(x=x, codes=codes, scales=scales, tensor_scale=ts, lora_A=A, lora_B=B, alpha=alpha))
+        ref_layers.append(dict(layers[-1]))
+    prep = q.GroupedLinear(layers)
+    for step in range(2):
+        if step:
+            for i, d in enumerate(layers):
+                d["x"].copy_(inputs.activations(m, d["x"].shape[1], inputs.derive_seed(1, "prep-x", i, m), device=DEV))
+        ys = prep.run()
+        for d, r in zip(layers, ref_layers):
+            r["x"] = d["x"].clone()
+            r["y"] = None
+        ref = q.linear_nvfp4_lora_grouped(ref_layers)
+        torch.cuda.synchronize()
+        for a, b in zip(ys, ref):
+            assert torch.equal(a, b)
