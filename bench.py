@@ -40,8 +40,10 @@ second figure, against GB300's published dense numbers (8 TB/s HBM, 2.25
 PFLOP/s bf16, 4.5 PFLOP/s FP8).
 
 Each phase is timed with CUDA events on the launching stream after an L2
-flush (a 512 MB write), so no phase reads its weights from L2 left by the
-previous one.  ``value`` is the decode phase's HBM throughput: its
+flush (a 512 MB write, then a read of the same 512 MB), so no phase reads
+its weights from L2 left by the previous one, and none starts by writing
+back a cache full of the flush's dirty lines (a cost of the flush, not of
+the phase: about 4 us of every decode phase).  ``value`` is the decode phase's HBM throughput: its
 algorithmic bytes (packed codes, block and tensor scales, LoRA factors,
 activations in, outputs out) over its device time; the other phases are
 reported in ``breakdown`` with their own roofline fractions.
@@ -381,6 +383,7 @@ class Workload:
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
         self.rq_ws = torch.empty(4096, dtype=torch.uint8, device=device)
         self.flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
+        self.flush_sum = torch.zeros((), dtype=torch.int64, device=device)
         self.launches = 0
 
     def next_step(self):
@@ -503,6 +506,7 @@ class Workload:
 
     def do_flush(self):
         self.flush.fill_(self.launches & 0xFF)
+        torch.sum(self.flush.view(torch.int32), dim=0, dtype=torch.int64, out=self.flush_sum)
 
     # -- 32B-class stack (built on first use: ~62 GB of bf16 masters) --
     def _stack32(self):
@@ -1010,7 +1014,7 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
                 "warmup": warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "nvfp4xbf16", "data": "synthetic",
-                "config": {"workload": WORKLOAD, "phases": phases, "l2": "flushed (512 MB write) before every phase",
+                "config": {"workload": WORKLOAD, "phases": phases, "l2": "flushed before every phase: a 512 MB write, then a read of it",
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                            "separately_timed": nxt + extra},
                 "roofline": roof, "breakdown": breakdown, "cpu_baseline": cpu, "e2e": e2e,

@@ -126,8 +126,13 @@ qrr_status qrr_quantize_nvfp4(const void* W, int64_t N, int64_t K, uint8_t* code
  *   workspace    qrr_linear_nvfp4_lora_workspace_bytes(M, N, K, r) bytes
  * Products are formed exactly and summed in fp32; the dequantized weight
  * e2m1 * e4m3 is exact in bf16.  A decode variant (split-K GEMV) is chosen
- * for small M and a tensor-core GEMM for large M; both give the same
- * contract. */
+ * for M <= 64 and a tensor-core GEMM for larger M; both give the same
+ * contract.  For M <= 8 the decode runs on the NVFP4 tensor-core MMA with
+ * each token's x (scaled by a power of two so its largest value lies in
+ * (3, 6]) carried as six E2M1 digit planes, sum_p d_p 6^-p: every value is
+ * represented to within 6^-5 of the token's largest one (below bf16's own
+ * half-ulp there), so outputs meet the same tolerance; powers of two are
+ * exact. */
 size_t qrr_linear_nvfp4_lora_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r);
 qrr_status qrr_linear_nvfp4_lora(const void* x, int64_t M, int64_t K, const uint8_t* codes,
                                  const uint8_t* scales, const float* tensor_scale, int64_t N,

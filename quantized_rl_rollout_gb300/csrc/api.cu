@@ -59,6 +59,7 @@ struct LinPlan {
   bool pair;  // 256-token tiles on CTA pairs (2-CTA clusters), each pair two 128-row tiles
   int bn, bk, m_tiles, count;
   bool sk;  // decode with a stream-K table (else one unit per tile)
+  bool nvf4;  // decode on the native NVFP4 MMA with x as E2M1 digit planes (the stream-K sizes)
   struct Layer {
     int n_tiles, splits, kcps, lora_chunks;
     size_t t_off, x16_off, p_off, part_off, cnt_off;
@@ -115,6 +116,7 @@ LinPlan plan_linear(int64_t M, const LinIn* in, int count) {
     p.sk = stream_k_units(skc, nl, nt, mt, n, decode_grid(), nullptr, pieces) >= 0;
     if (p.sk)
       for (int i = 0; i < n; ++i) p.l[idx[i]].splits = pieces[i];  // partial slots
+    p.nvf4 = p.sk && M <= kNvf4MaxM;
   }
   if (decode && !p.sk) {
     // Cost model in pipeline stages: a unit costs its K stages plus its
@@ -152,8 +154,12 @@ LinPlan plan_linear(int64_t M, const LinIn* in, int count) {
     LinPlan::Layer& L = p.l[j];
     L.t_off = off;
     off += round_up(static_cast<size_t>(M) * 64 * L.lora_chunks * 2);
-    L.x16_off = off;
-    if (p.f16) off += round_up(static_cast<size_t>(M) * static_cast<size_t>(in[j].K) * 2);
+    L.x16_off = off;  // the f16 image of x, or its digit planes
+    if (p.nvf4)
+      off += round_up(static_cast<size_t>(kXPlanes) * nvf4_geo(static_cast<int>(M)).ms *
+                      static_cast<size_t>(in[j].K) / 2);
+    else if (p.f16)
+      off += round_up(static_cast<size_t>(M) * static_cast<size_t>(in[j].K) * 2);
     L.p_off = off;
     if (p.f16) off += round_up(static_cast<size_t>(M) * 4);
     L.part_off = off;
@@ -219,7 +225,9 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
       DecodeProLayer& dl = db.l[db.count++];
       dl.x = static_cast<const uint16_t*>(a.x);
       dl.A = static_cast<const uint16_t*>(a.A);
-      dl.x16 = x16;
+      dl.x16 = pl.nvf4 ? nullptr : x16;
+      dl.planes = pl.nvf4 ? reinterpret_cast<uint8_t*>(x16) : nullptr;
+      dl.ms = nvf4_geo(static_cast<int>(M)).ms;
       dl.pexp = pexp;
       dl.t = tbuf;
       dl.tensor_scale = a.tensor_scale;
@@ -258,7 +266,13 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
     const void* xsrc = pl.f16 ? static_cast<const void*>(x16) : a.x;
     const CUtensorMapDataType xt = pl.f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const uint32_t box_m = pl.pair ? pl.bn / 2 : pl.bn;  // token rows one CTA loads
-    if (!make_tmap_2d(&L.tx, xsrc, xt, M, a.K, a.K * 2, box_m, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if (pl.nvf4) {
+      const Nvf4Geo geo = nvf4_geo(static_cast<int>(M));
+      if (!make_tmap_2d(&L.tp, x16, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<uint64_t>(kXPlanes) * geo.ms, a.K / 2,
+                        a.K / 2, static_cast<uint32_t>(geo.nmma), 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        return QRR_ERR_CUDA;
+    }
+    if ((!pl.nvf4 && !make_tmap_2d(&L.tx, xsrc, xt, M, a.K, a.K * 2, box_m, 64, CU_TENSOR_MAP_SWIZZLE_128B)) ||
         !make_tmap_2d(&L.tcodes, a.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.N, a.K / 2, a.K / 2, 128, pl.bk / 2,
                       pl.bk == 256 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B) ||
         !make_tmap_2d(&L.tscales, a.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.N, a.K / 16, a.K / 16, 128, 16,
@@ -313,6 +327,7 @@ qrr_status run_linear(const LinIn* in, int count, int64_t M, void* workspace, si
       db.clear_words = static_cast<int>(pl.cnt_bytes / 4);
     }
     if (launch_decode_prologue(db, s) != cudaSuccess) return QRR_ERR_CUDA;
+    if (pl.nvf4) return from_cuda(launch_w4_decode_nvf4(p, s));
     return from_cuda(launch_w4a16_tc(p, pl.bn, pl.f16, pl.pair, true, s));
   }
   if (lb.count > 0 && launch_lora_down_tc(lb, s) != cudaSuccess) return QRR_ERR_CUDA;

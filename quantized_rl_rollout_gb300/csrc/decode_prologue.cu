@@ -1,8 +1,10 @@
 // Decode prologue of the W4A16 + LoRA linear (at most 64 tokens).
 //
-// The GEMM takes x on its f16 operand path, which needs for each token m the
-// power of two p_m with max_k |x[m, k]| 2^-p_m in [2^14, 2^15) and the image
-// x16 = f16(x 2^-p_m); the adapter path needs
+// The GEMM takes an image of x: above 8 tokens its f16 operand, which needs
+// for each token m the power of two p_m with max_k |x[m, k]| 2^-p_m in
+// [2^14, 2^15) and x16 = f16(x 2^-p_m); up to 8 tokens the E2M1 digit planes
+// of x 2^-p_m with max |x| 2^-p_m in (3, 6] (write_planes8 below).  The
+// adapter path needs
 //   t'[m, 2j] = bf16(v), t'[m, 2j+1] = bf16(v - bf16(v)),
 //   v = (alpha / r) t[m, j] / g,  t = x A^T,  g = s_t (or 1 when s_t = 0)
 // ("NVIDIA and MIT Collaborate on QeRL", Key Features: the adapter runs in
@@ -20,7 +22,7 @@
 //   warps 2..5  per-token max |x| over the staged tiles; then (warps 4 and 5,
 //               TMEM lane quarters 0 and 1) t_c from TMEM into shared memory
 // and then, across the cluster through distributed shared memory, every CTA
-// takes the token maxima over all slices and writes the f16 image of its own
+// takes the token maxima over all slices and writes the image of its own
 // slice, and the t outputs are divided among the CTAs, each summing the ks
 // slice partials in slice order (the result does not depend on timing).  No
 // global partials, tickets or fences: one pass over x and A.  The launch
@@ -99,6 +101,51 @@ __device__ __forceinline__ int pexp_of(uint32_t mx) {
   int e;
   frexpf(bf16bits_to_f32(mx), &e);  // amax = f 2^e, 0.5 <= f < 1
   return e - 15;
+}
+
+// For the E2M1 digit planes: the power of two e with max |x| 2^-e in
+// (3, 6], so that every scaled value lies on or inside the E2M1 range.
+__device__ __forceinline__ int pexp_planes(uint32_t mx) {
+  if (mx == 0u) return 0;
+  int e;
+  const float f = frexpf(bf16bits_to_f32(mx), &e);  // amax = f 2^e, 0.5 <= f < 1
+  return f > 0.75f ? e - 2 : e - 3;
+}
+
+__device__ __forceinline__ int pexp_for(uint32_t mx, bool planes) { return planes ? pexp_planes(mx) : pexp_of(mx); }
+
+// The digit planes of 8 consecutive values of one token (one 16-byte bf16
+// vector): word p of plane p at dst[p * stride] (stride in words), eight
+// E2M1 codes, element i in nibble i.  r starts as x 2^-e (|r| <= 6); each
+// plane takes d = e2m1_rne(r) and leaves r = (r - d) 6, which stays within
+// [-6, 6] because |r - d| <= 1 on the E2M1 grid.
+__device__ __forceinline__ void write_planes8(uint4 xv, const Pow2Scaler& sc, uint32_t* dst, int64_t stride) {
+  float r[8];
+  const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    r[2 * u] = sc(bf16_lo(w[u]));
+    r[2 * u + 1] = sc(bf16_hi(w[u]));
+  }
+#pragma unroll
+  for (int pl = 0; pl < kXPlanes; ++pl) {
+    const uint32_t code = cvt_e2m1x8(r);
+    dst[pl * stride] = code;
+    if (pl + 1 < kXPlanes) {
+      uint32_t h2[4];  // the digits' values as f16 pairs (exact)
+      asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+          "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+          "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+          : "=r"(h2[0]), "=r"(h2[1]), "=r"(h2[2]), "=r"(h2[3])
+          : "r"(code));
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const float2 d = __half22float2(*reinterpret_cast<const __half2*>(&h2[b]));
+        r[2 * b] = __fmul_rn(__fsub_rn(r[2 * b], d.x), 6.0f);
+        r[2 * b + 1] = __fmul_rn(__fsub_rn(r[2 * b + 1], d.y), 6.0f);
+      }
+    }
+  }
 }
 
 // t'[m, 2j], t'[m, 2j+1] of one rank: v = (scale t / g) 2^-p_m as (high,
@@ -269,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_prologue_kernel(const __gr
     uint32_t mx = 0u;
 #pragma unroll
     for (int rr = 0; rr < kKsMax; ++rr) mx = max(mx, part[rr]);
-    const int pe = pexp_of(mx);
+    const int pe = pexp_for(mx, L.planes != nullptr);
     sh.pexp[m] = pe;
     if (rank == 0) {
       if (mx >= 0x7F80u) flag(b.status, QRR_DEV_NONFINITE);
@@ -279,8 +326,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_prologue_kernel(const __gr
   __syncthreads();
   if (tid == 0) QRR_DSTAMP(5);
 
-  // f16 image of this slice: from the staged tiles while the ring held the
-  // whole slice, else from x again (an L2 hit: the tiles were just loaded)
+  // f16 image (or digit planes) of this slice: from the staged tiles while
+  // the ring held the whole slice, else from x again (an L2 hit: the tiles
+  // were just loaded)
   {
     const int nvec = steps * 8;  // 16-byte vectors per token row of the slice
     const bool resident = steps <= S;  // one round: step c still sits in slot c
@@ -301,6 +349,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_prologue_kernel(const __gr
       else
         xv = __ldg(reinterpret_cast<const uint4*>(xg + static_cast<int64_t>(m) * K + (k0 + c) * 64) + pc);
       const Pow2Scaler sc(sh.pexp[m]);
+      if (L.planes != nullptr) {
+        const int64_t stride = static_cast<int64_t>(L.ms) * (K / 8);  // words per plane
+        write_planes8(xv, sc,
+                      reinterpret_cast<uint32_t*>(L.planes) + static_cast<int64_t>(m) * (K / 8) + (k0 + c) * 8 + pc,
+                      stride);
+        continue;
+      }
       const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
       uint32_t o[4];
       if (sc.f2 == 1.0f) {  // 2^-p a normal fp32 number: one exact multiply
@@ -413,12 +468,19 @@ __global__ void __launch_bounds__(kSmallThreads) decode_prologue_small_kernel(co
     mx = 0u;
 #pragma unroll
     for (int w = 0; w < kSmallThreads / 32; ++w) mx = max(mx, red_u[w]);
-    const int pe = pexp_of(mx);
+    const int pe = pexp_for(mx, L.planes != nullptr);
     if (tid == 0) {
       if (mx >= 0x7F80u) flag(b.status, QRR_DEV_NONFINITE);
       L.pexp[m] = pe;
     }
     const Pow2Scaler sc(pe);
+    if (L.planes != nullptr) {
+      uint32_t* const pw = reinterpret_cast<uint32_t*>(L.planes) + static_cast<int64_t>(m) * (K / 8);
+      const int64_t stride = static_cast<int64_t>(L.ms) * (K / 8);
+#pragma unroll 4
+      for (int v = tid; v < nv; v += kSmallThreads) write_planes8(__ldg(xr + v), sc, pw + v, stride);
+      return;
+    }
     uint4* x16 = reinterpret_cast<uint4*>(L.x16 + static_cast<int64_t>(m) * K);
 #pragma unroll 4
     for (int v = tid; v < nv; v += kSmallThreads) {
@@ -507,7 +569,7 @@ __global__ void __launch_bounds__(kSmallThreads) decode_prologue_small_kernel(co
     if (j0 + jj < r) {
       const float st = *L.tensor_scale;
       write_tprime(L.t + static_cast<int64_t>(mm) * L.t_cols, j0 + jj, L.lora_scale, t, st > 0.0f ? st : 1.0f,
-                   pexp_of(mx));
+                   pexp_for(mx, L.planes != nullptr));
     }
   }
   // the padding columns of t' past 2 r: the first t CTA of the layer

@@ -22,10 +22,11 @@ struct W4Layer {
   CUtensorMap tt;      // LoRA t' bf16 [M, 64 * lora_chunks], box as tx, 128 B swizzle
   CUtensorMap tscales;  // block scales u8 [N, K/16], box [128, 16] (256-wide K stages)
   CUtensorMap tb;       // decode: LoRA B bf16 [N, r], box [128, r], into the LoRA stage's code slot
+  CUtensorMap tp;       // decode on E2M1 planes: x planes u8 [kXPlanes * ms, K/2], box [nmma, 128], 128 B swizzle
   const uint8_t* scales;
   const float* tensor_scale;
   const uint16_t* B;  // LoRA B [N, r], r <= 64
-  const int* pexp;    // per-token power-of-two pre-scale (f16 path) or null
+  const int* pexp;    // per-token power-of-two pre-scale (decode) or null
   __nv_bfloat16* y;
   float* partial;      // [splits, M, N] when splits > 1
   uint32_t* counters;  // [m_tiles * n_tiles], zero before the launch
@@ -105,7 +106,9 @@ cudaError_t launch_lora_down_tc(LoraDownBatch& b, cudaStream_t stream);
 struct DecodeProLayer {
   const uint16_t* x;  // bf16 [M, K]
   const uint16_t* A;  // LoRA A bf16 [r, K] (r > 0)
-  __half* x16;        // f16 [M, K]
+  __half* x16;        // f16 [M, K], or null when `planes` is set
+  uint8_t* planes;    // E2M1 digit planes [kXPlanes * ms, K/2] (see kXPlanes below), or null
+  int ms;             // token rows per plane (planes only)
   int* pexp;          // [M]
   __nv_bfloat16* t;   // [M, t_cols] (r > 0)
   const float* tensor_scale;
@@ -124,6 +127,59 @@ struct DecodeProBatch {
 };
 
 cudaError_t launch_decode_prologue(DecodeProBatch& b, cudaStream_t stream);
+
+// ---- decode on the native NVFP4 MMA (w4_decode_nvf4.cu) ----
+// Each token's activations, scaled by the power of two 2^-e_m that brings
+// max_k |x[m, k]| into (3, 6], are written as kXPlanes E2M1 digit planes
+// d_0 .. d_5 with x 2^-e = sum_p d_p 6^-p + rest, |rest| <= 6^-5: d_p is the
+// round-to-nearest-even E2M1 value of the running residual, which is then
+// (residual - d_p) 6 (each step exact or within an fp32 rounding).  Plane
+// row p * ms + m holds token m's digits of plane p, packed like the weight
+// codes (element k in the low nibble of byte k / 2 when k is even).
+constexpr int kXPlanes = 6;
+
+// Launch geometry of the plane decode for M tokens, the same on host and
+// device: ms token rows per plane (1, else M rounded up to 8); rows = the
+// plane rows of a stage (kXPlanes * ms rounded up to 16, to 32 when they are
+// split), taken by nh MMAs of N = nmma each (N <= 256); bn = token rows of
+// the t' box (the LoRA MMA's N); the stage layout (x/t' slot of xb bytes,
+// then 16 KB of codes and 2 KB of block scales); and the tensor-memory map
+// (nd accumulators of `rows` columns, 64 columns of LoRA A, 16 of B scales,
+// then sf_slots groups of 16 columns of A scales).
+struct Nvf4Geo {
+  int ms, rows, nh, nmma, bn, xb, stage, stages, nd, lora0, sfb0, sf0, sf_slots;
+};
+
+__host__ __device__ inline Nvf4Geo nvf4_geo(int M) {
+  Nvf4Geo g{};
+  g.ms = M <= 1 ? 1 : (M + 7) / 8 * 8;
+  g.rows = (kXPlanes * g.ms + 15) / 16 * 16;
+  g.nh = g.rows > 256 ? 2 : 1;
+  if (g.nh == 2) g.rows = (g.rows + 31) / 32 * 32;
+  g.nmma = g.rows / g.nh;
+  g.bn = M <= 16 ? 16 : M <= 32 ? 32 : 64;
+  const int xrows = g.rows > 2 * g.bn ? g.rows : 2 * g.bn;
+  g.xb = (xrows * 128 + 1023) / 1024 * 1024;
+  g.stage = g.xb + 128 * 128 + 128 * 16;
+  g.stages = (220 * 1024) / g.stage;
+  g.stages = g.stages > 8 ? 8 : g.stages;
+  g.nd = 2 * g.rows + 64 + 16 + 2 * 16 <= 512 ? 2 : 1;
+  g.lora0 = (g.nd * g.rows + 63) / 64 * 64;
+  g.sfb0 = g.lora0 + 64;
+  g.sf0 = g.sfb0 + 16;
+  g.sf_slots = (512 - g.sf0) / 16;
+  g.sf_slots = g.sf_slots > 8 ? 8 : g.sf_slots;
+  return g;
+}
+
+// The plane decode takes at most this many tokens (above it, the dequant
+// kernel on its f16 operand path, up to 64).
+constexpr int kNvf4MaxM = 8;
+
+// Decode GEMM over the unit table in `p` (use_table set): codes and block
+// scales by TMA straight into the block-scaled MMA, x as its digit planes,
+// the LoRA stage as a kind::f16 MMA into plane 0's columns.
+cudaError_t launch_w4_decode_nvf4(const W4Params& p, cudaStream_t stream);
 
 int w4_bn_for(int64_t M);
 int w4_bk_for(int64_t M);

@@ -481,6 +481,46 @@ __device__ __forceinline__ void mma_f16kind_ts(uint32_t d_tmem, uint32_t a_tmem,
   mma_bf16_ts(d_tmem, a_tmem, b_desc, idesc, accumulate);
 }
 
+// 32 lanes x 8 columns of 32-bit.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+
+// 32 lanes x 16 columns of 32-bit from registers.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// D[tmem] (+)= A[smem] x B[smem]^T, kind::mxf4nvf4 with block scaling:
+// packed E2M1 operands (two per byte, K-major, 64 K per MMA = 32 bytes of a
+// row) and one UE4M3 scale per 16 K of every row of A and of B, the four
+// scales of a row for the MMA's 64 K in one 32-bit tensor-memory cell (byte
+// i for K [16 i, 16 i + 16)).  Cells are addressed as for kind::mxf8f6f4
+// (row m of A: lane m, column sfa + m / 32; row n of B: column sfb + n / 32).
+__device__ __forceinline__ void mma_nvf4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf4nvf4: E2M1 A and B (format 1 of the
+// fp4 kinds, bits [7,10) and [10,12)), UE4M3 scales (bit 23 clear), both
+// K-major, D fp32, shape M x N, scale ids 0 (the whole cell is used).
+__host__ __device__ constexpr uint32_t make_idesc_nvf4(uint32_t m, uint32_t n) {
+  return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
 // Named barrier over `count` threads (id 1..15; id 0 is __syncthreads).
 __device__ __forceinline__ void named_bar(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

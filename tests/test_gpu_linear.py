@@ -100,13 +100,15 @@ def test_closed_forms(q):
 
 
 @pytest.mark.parametrize("n", [384, 512])
-@pytest.mark.parametrize("m", [64, 100, 300])
+@pytest.mark.parametrize("m", [1, 8, 64, 100, 300])
 def test_one_hot_tokens_bit_exact(q, m, n):
     """Token m is +-e_{k_m}: y[m] is then +-W_hat[:, k_m] scaled once by s_t
     in fp32 and rounded to bf16, with no sum to round, so every output is
-    fixed to the bit (the f16 decode tiles at 64 tokens, the bf16 prefill
-    tiles of 128 and 256 tokens with a ragged last tile, on single CTAs for
-    an odd number of 128-row tiles and on CTA pairs for an even one)."""
+    fixed to the bit (the E2M1-plane decode at 1 and 8 tokens, where +-1
+    scales to the single digit +-4, the f16 decode tiles at 64 tokens, the
+    bf16 prefill tiles of 128 and 256 tokens with a ragged last tile, on
+    single CTAs for an odd number of 128-row tiles and on CTA pairs for an
+    even one)."""
     k = 2048
     W, codes, scales, ts, _, _, _ = _layer(q, n, k, 0, "onehot")
     g = np.random.default_rng(m)
@@ -396,3 +398,24 @@ def test_prepared_grouped_call(q, m):
         torch.cuda.synchronize()
         for a, b in zip(ys, ref):
             assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("m", [1, 3, 8])
+def test_decode_planes_wide_range(q, m):
+    """The plane decode (up to 8 tokens) on activations spanning 2^-40 to
+    2^20 within a token, with exact E2M1 values, values just off the
+    rounding midpoints of every plane and a token of subnormal-sized
+    values: the six digit planes leave less than 6^-5 of each token's
+    largest value unrepresented, so the output stays within tolerance."""
+    n, k, r = 384, 2048, 16
+    W, codes, scales, ts, A, B, alpha = _layer(q, n, k, r, "planes-wide")
+    g = np.random.default_rng(7 + m)
+    xh = g.standard_normal((m, k)).astype(np.float32)
+    xh *= np.exp2(g.integers(-40, 21, size=(m, k))).astype(np.float32)
+    xh[0, :8] = [6.0, -4.0, 0.25, 0.75, 1.25, 2.5, 5.0, -3.5]  # on the E2M1 grid and its midpoints
+    if m > 1:
+        xh[1] = (g.standard_normal(k) * 1e-39).astype(np.float32)  # bf16 subnormals
+    x = torch.from_numpy(xh).to(torch.bfloat16).to(DEV)
+    y = q.linear_nvfp4_lora(x, codes, scales, ts, A, B, alpha)
+    torch.cuda.synchronize()
+    _assert_close(y, _ref(x, codes, scales, ts, A, B, alpha), f"m={m}")
