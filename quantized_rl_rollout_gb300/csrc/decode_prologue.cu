@@ -140,9 +140,14 @@ __device__ __forceinline__ void write_planes8(uint4 xv, const Pow2Scaler& sc, ui
           : "r"(code));
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
+        // (r - d) 6 for both halves on the paired fp32 pipe (each half one
+        // correctly rounded fp32 subtraction, then one multiplication)
         const float2 d = __half22float2(*reinterpret_cast<const __half2*>(&h2[b]));
-        r[2 * b] = __fmul_rn(__fsub_rn(r[2 * b], d.x), 6.0f);
-        r[2 * b + 1] = __fmul_rn(__fsub_rn(r[2 * b + 1], d.y), 6.0f);
+        asm("{\n\t.reg .b64 rr, dd, six;\n\t"
+            "mov.b64 rr, {%0, %1};\n\tmov.b64 dd, {%2, %3};\n\tmov.b64 six, {%4, %4};\n\t"
+            "sub.rn.f32x2 rr, rr, dd;\n\tmul.rn.f32x2 rr, rr, six;\n\tmov.b64 {%0, %1}, rr;\n\t}"
+            : "+f"(r[2 * b]), "+f"(r[2 * b + 1])
+            : "f"(d.x), "f"(d.y), "f"(6.0f));
       }
     }
   }
@@ -430,6 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_prologue_kernel(const __gr
 constexpr int kSmallM = 1;
 constexpr int kSmallThreads = 512;
 constexpr int kRanksPerCta = 2;
+// x CTAs per token row: one per 4096 values of the row (each takes the whole
+// row's maximum, an L2 read, and writes the image of its own slice)
+constexpr int kSliceVecs = 512;  // 16-byte vectors of a slice
+
+__host__ __device__ constexpr int x_slices(int K) { return (K / 8 + kSliceVecs - 1) / kSliceVecs; }
 
 // bf16 bits -> 8 fp32 values
 __device__ __forceinline__ void unpack8_bf16(uint4 v, float (&f)[8]) {
@@ -447,6 +457,7 @@ __global__ void __launch_bounds__(kSmallThreads) decode_prologue_small_kernel(co
   __shared__ uint32_t red_m[kSmallThreads / 32][kSmallM];
   griddep_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) QRR_DSTAMP(10);
   int j = 0;
   while (j + 1 < b.count && b.l[j + 1].first_cta <= static_cast<int>(blockIdx.x)) ++j;
   const DecodeProLayer& L = b.l[j];
@@ -455,9 +466,11 @@ __global__ void __launch_bounds__(kSmallThreads) decode_prologue_small_kernel(co
   for (int w = static_cast<int>(blockIdx.x) * kSmallThreads + tid; w < b.clear_words;
        w += static_cast<int>(gridDim.x) * kSmallThreads)
     b.clear[w] = 0u;
-  if (local < M) {
-    // ---- x16 and p of token m ----
-    const int m = local;
+  const int xs = x_slices(K);
+  if (local < M * xs) {
+    // ---- x image and p of token m, slice sl of its row ----
+    const int m = local / xs, sl = local - m * xs;
+    const int v0 = sl * kSliceVecs, v1 = min(nv, v0 + kSliceVecs);
     const uint4* xr = reinterpret_cast<const uint4*>(L.x + static_cast<int64_t>(m) * K);
     uint32_t mx = 0u;
 #pragma unroll 8
@@ -469,7 +482,7 @@ __global__ void __launch_bounds__(kSmallThreads) decode_prologue_small_kernel(co
 #pragma unroll
     for (int w = 0; w < kSmallThreads / 32; ++w) mx = max(mx, red_u[w]);
     const int pe = pexp_for(mx, L.planes != nullptr);
-    if (tid == 0) {
+    if (tid == 0 && sl == 0) {
       if (mx >= 0x7F80u) flag(b.status, QRR_DEV_NONFINITE);
       L.pexp[m] = pe;
     }
@@ -477,13 +490,12 @@ __global__ void __launch_bounds__(kSmallThreads) decode_prologue_small_kernel(co
     if (L.planes != nullptr) {
       uint32_t* const pw = reinterpret_cast<uint32_t*>(L.planes) + static_cast<int64_t>(m) * (K / 8);
       const int64_t stride = static_cast<int64_t>(L.ms) * (K / 8);
-#pragma unroll 4
-      for (int v = tid; v < nv; v += kSmallThreads) write_planes8(__ldg(xr + v), sc, pw + v, stride);
+      for (int v = v0 + tid; v < v1; v += kSmallThreads) write_planes8(__ldg(xr + v), sc, pw + v, stride);
+      if (tid == 0) QRR_DSTAMP(11);
       return;
     }
     uint4* x16 = reinterpret_cast<uint4*>(L.x16 + static_cast<int64_t>(m) * K);
-#pragma unroll 4
-    for (int v = tid; v < nv; v += kSmallThreads) {
+    for (int v = v0 + tid; v < v1; v += kSmallThreads) {
       const uint4 xv = __ldg(xr + v);
       const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
       uint32_t o[4];
@@ -497,7 +509,7 @@ __global__ void __launch_bounds__(kSmallThreads) decode_prologue_small_kernel(co
     return;
   }
   // ---- t of kRanksPerCta ranks, all tokens ----
-  const int r = L.r, j0 = (local - M) * kRanksPerCta;
+  const int r = L.r, j0 = (local - M * xs) * kRanksPerCta;
   float acc[kSmallM][kRanksPerCta];
   uint32_t xmax[kSmallM];  // each token's max |x| (its p scales t')
 #pragma unroll
@@ -578,6 +590,7 @@ __global__ void __launch_bounds__(kSmallThreads) decode_prologue_small_kernel(co
     for (int idx = tid; idx < M * pad; idx += kSmallThreads)
       L.t[static_cast<int64_t>(idx / pad) * L.t_cols + 2 * r + idx % pad] = __float2bfloat16_rn(0.0f);
   }
+  if (tid == 0) QRR_DSTAMP(11);
 }
 
 namespace {
@@ -615,7 +628,7 @@ cudaError_t launch_decode_prologue(DecodeProBatch& b, cudaStream_t stream) {
     for (int j = 0; j < b.count; ++j) {
       DecodeProLayer& L = b.l[j];
       L.first_cta = ctas;
-      ctas += L.M + (L.r + kRanksPerCta - 1) / kRanksPerCta;
+      ctas += L.M * x_slices(L.K) + (L.r + kRanksPerCta - 1) / kRanksPerCta;
     }
     decode_prologue_small_kernel<<<ctas, kSmallThreads, 0, stream>>>(b);
     return cudaGetLastError();

@@ -43,6 +43,23 @@
 
 namespace qrr {
 
+// Development builds (-DQRR_TRACE_BUILD) record global-timer stamps per CTA:
+// start, planes released (the prologue has completed), first MMA, end.
+// Ordinary builds compile them away.
+#ifdef QRR_TRACE_BUILD
+__device__ unsigned long long qrr_ntrace_buf[256][4];
+#define QRR_NSTAMP(ev)                                               \
+  do {                                                               \
+    unsigned long long t_;                                           \
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));           \
+    if (blockIdx.x < 256) qrr_ntrace_buf[blockIdx.x][ev] = t_;       \
+  } while (0)
+#else
+#define QRR_NSTAMP(ev) \
+  do {                 \
+  } while (0)
+#endif
+
 namespace {
 
 constexpr int kThreads = 320;
@@ -85,6 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_decode_nvf4_kernel(const __gri
   Ctl& sh = *reinterpret_cast<Ctl*>(tiles + S * g.stage);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &sh.abort;
+  if (threadIdx.x == 0) QRR_NSTAMP(0);
   const int sk0 = p.unit_off[blockIdx.x];
   const int n_my = p.unit_off[blockIdx.x + 1] - sk0;
   auto wait = [&](uint64_t* bar, uint32_t parity) { return mbar_wait(bar, parity, abort, p.status); };
@@ -177,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_decode_nvf4_kernel(const __gri
         ++nw;
       }
       griddep_wait();  // the planes and t' are the prologue's
+      QRR_NSTAMP(1);
       for (uint32_t nx = 0; nx < nw; ++nx) {
         next(kx);
         issue_x(kx, static_cast<int>(nx));
@@ -227,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_decode_nvf4_kernel(const __gri
               break;
             }
             tc_fence_after();
+            if (seq == 0) QRR_NSTAMP(2);
             const uint32_t cs = xs + static_cast<uint32_t>(g.xb);
             const uint32_t sfa = tmem + static_cast<uint32_t>(g.sf0 + 16 * slot);
             // plane rows [h nmma, (h + 1) nmma) into accumulator columns alike
@@ -476,6 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_decode_nvf4_kernel(const __gri
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) QRR_NSTAMP(3);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -508,3 +529,9 @@ cudaError_t launch_w4_decode_nvf4(const W4Params& p, cudaStream_t stream) {
 }
 
 }  // namespace qrr
+
+#ifdef QRR_TRACE_BUILD
+extern "C" int qrr_ntrace_read(unsigned long long* host) {
+  return static_cast<int>(cudaMemcpyFromSymbol(host, qrr::qrr_ntrace_buf, sizeof(qrr::qrr_ntrace_buf)));
+}
+#endif
