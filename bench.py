@@ -383,7 +383,7 @@ class Workload:
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
         self.rq_ws = torch.empty(4096, dtype=torch.uint8, device=device)
         self.flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
-        self.flush_sum = torch.zeros((), dtype=torch.int64, device=device)
+        self.flush_sum = torch.zeros((), dtype=torch.float32, device=device)
         self.launches = 0
 
     def next_step(self):
@@ -506,7 +506,7 @@ class Workload:
 
     def do_flush(self):
         self.flush.fill_(self.launches & 0xFF)
-        torch.sum(self.flush.view(torch.int32), dim=0, dtype=torch.int64, out=self.flush_sum)
+        torch.sum(self.flush.view(torch.float32), dim=0, out=self.flush_sum)
 
     # -- 32B-class stack (built on first use: ~62 GB of bf16 masters) --
     def _stack32(self):

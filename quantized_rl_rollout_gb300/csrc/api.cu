@@ -382,7 +382,7 @@ struct BwdPlan {
 BwdPlan plan_backward(int64_t M, int64_t N, int64_t K, int32_t r) {
   BwdPlan p{};
   p.t_cols = r > 0 ? 64 * static_cast<int>((2 * r + 63) / 64) : 0;
-  p.slice = 1024;  // contraction slice of the rank projections (16 steps of 64)
+  p.slice = 2048;  // contraction slice of the rank projections (32 steps of 64)
   p.ks_u = static_cast<int>((N + p.slice - 1) / p.slice);
   p.ks_t = static_cast<int>((K + p.slice - 1) / p.slice);
   size_t off = 0;
@@ -464,7 +464,7 @@ qrr_status qrr_lora_backward_nvfp4(const void* dy, int64_t M, int64_t N, const v
     return QRR_ERR_CUDA;
   if (lora) {
     // u' = (alpha/r) (dY . B) / g and t' = (alpha/r) (x . A^T) / g, split over
-    // 1024-wide contraction slices with a ticket per 128-token tile
+    // 2048-wide contraction slices with a ticket per 128-token tile
     if (cudaMemsetAsync(ws + pl.tick_off, 0, pl.tick_bytes, s) != cudaSuccess) return QRR_ERR_CUDA;
     LoraDownBatch lb{};
     lb.status = dev_status;

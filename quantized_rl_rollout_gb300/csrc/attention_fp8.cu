@@ -13,7 +13,10 @@
 //
 // Decode attention reads every cached byte once and does G = Hq / Hkv
 // multiply-adds per byte, so it is HBM-bound; it runs on the CUDA cores in
-// fp32 (the E4M3 codes convert exactly).  Split over the sequence: a CTA
+// fp32 (the E4M3 codes convert exactly).  The scores take each key value as
+// f16 into mixed-precision FMAs (f16 x f16 products are exact in fp32)
+// against the query scaled by a power of two into f16, which leaves out one
+// conversion per key value, the most frequent instruction of the kernel.  Split over the sequence: a CTA
 // takes 512 tokens of one (sequence, KV head), streams their key and value
 // rows and scales through shared memory in 64-token chunks by bulk copies
 // (three in flight), and writes a partial (max, sum, unnormalized output) per
@@ -53,6 +56,23 @@ __device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float (&f)[4]) {
   f[1] = a.y;
   f[2] = b.x;
   f[3] = b.y;
+}
+
+// a += k.lo q.lo + k.hi q.hi for two f16 pairs: mixed-precision FMAs, whose
+// f16 x f16 products are exact in fp32
+__device__ __forceinline__ void fma_f16pair(float& a, uint32_t k2, uint32_t q2) {
+  asm("{\n\t.reg .b16 kl, kh, ql, qh;\n\tmov.b32 {kl, kh}, %1;\n\tmov.b32 {ql, qh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, kl, ql, %0;\n\tfma.rn.f32.f16 %0, kh, qh, %0;\n\t}"
+      : "+f"(a)
+      : "r"(k2), "r"(q2));
+}
+
+// four E4M3 bytes -> two f16 pairs (bytes 0,1 and 2,3; exact)
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 constexpr int CH = 64;      // tokens per pipeline chunk
@@ -135,11 +155,16 @@ __global__ void __launch_bounds__(kThreads) attn_decode_fp8_kernel(
     int32_t* status) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   AttnShared<G>& sh = *reinterpret_cast<AttnShared<G>*>(smem_raw);
-  // q / sqrt(d) * log2(e) as [16-value piece][value][head], each piece's row
-  // padded by 4 words: the 8 pieces that the threads of a shared-memory phase
-  // read at once (see the rotated key reads below) sit on distinct banks
-  constexpr int QROW = 16 * G + 4;
-  __shared__ __align__(16) float qs[8][QROW];
+  // q 2^-e_h in f16 (e_h: head h's power of two that brings max |q| into
+  // [2^14, 2^15), exact for bf16 values) as [16-value piece][value pair]
+  // [head] f16 pairs, each piece's row padded by 4 words: the 8 pieces that
+  // the threads of a shared-memory phase read at once (see the rotated key
+  // reads below) sit on distinct banks.  The score is then
+  // (sum_d k q 2^-e_h) 2^e_h / sqrt(128) log2(e) times the key row's scale.
+  constexpr int QROW = 8 * G + 4;
+  __shared__ __align__(16) uint32_t qs[8][QROW];
+  __shared__ uint32_t qmax[kThreads / 32][G];
+  __shared__ float qf[G];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int s = blockIdx.x % splits, bg = blockIdx.x / splits;
   const int b = bg / Hkv, g = bg % Hkv;
@@ -165,10 +190,35 @@ __global__ void __launch_bounds__(kThreads) attn_decode_fp8_kernel(
     fence_barrier_init();
   }
   const float qscale = 0.08838834764831845f * kLog2e;  // 1 / sqrt(128) * log2(e)
-  for (int i = tid; i < G * D; i += kThreads) {
-    const int h = i / D, d = i % D;
-    const uint16_t qb = __ldg(q + (static_cast<int64_t>(b) * Hkv * G + g * G + h) * D + d);
-    qs[d >> 4][(d & 15) * G + h] = bf16bits_to_f32(qb) * qscale;
+  const uint16_t* const qg = q + (static_cast<int64_t>(b) * Hkv * G + g * G) * D;
+  {
+    // each head's max |q| (thread: value pair tid of every head)
+    uint32_t mx[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const uint32_t w = tid < D / 2 ? __ldg(reinterpret_cast<const uint32_t*>(qg + h * D) + tid) : 0u;
+      mx[h] = __reduce_max_sync(0xFFFFFFFFu, max(w & 0x7FFFu, (w >> 16) & 0x7FFFu));
+      if (lane == 0) qmax[warp][h] = mx[h];
+    }
+  }
+  __syncthreads();
+  if (tid < G) {
+    uint32_t m = 0u;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) m = max(m, qmax[w][tid]);
+    int e = 0;
+    if (m != 0u) frexpf(bf16bits_to_f32(m), &e);  // max = f 2^e, 0.5 <= f < 1
+    const int eh = m != 0u ? e - 15 : 0;
+    qmax[0][tid] = static_cast<uint32_t>(eh);
+    qf[tid] = __fmul_rn(qscale, pow2_from_exp(eh));
+  }
+  __syncthreads();
+  for (int i = tid; i < G * (D / 2); i += kThreads) {
+    const int h = i / (D / 2), jp = i % (D / 2);  // value pair jp of head h
+    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(qg + h * D) + jp);
+    const Pow2Scaler sc(static_cast<int>(qmax[0][h]));
+    const __half2 h2 = __floats2half2_rn(sc(bf16_lo(w)), sc(bf16_hi(w)));
+    qs[jp >> 3][(jp & 7) * G + h] = *reinterpret_cast<const uint32_t*>(&h2);
   }
   __syncthreads();
   // chunk c: n_c tokens; scales move in multiples of 4 (16 bytes), which stay
@@ -214,13 +264,14 @@ __global__ void __launch_bounds__(kThreads) attn_decode_fp8_kernel(
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          float f[4];
-          e4m3x4_to_f32(ws[e], f);
-          const float* qp = &qs[piece][(4 * e) * G];
+          uint32_t k01, k23;
+          e4m3x4_to_f16x4(ws[e], k01, k23);
+          const uint32_t* qp = &qs[piece][(2 * e) * G];  // value pairs 2e, 2e + 1 of the piece
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-            for (int h = 0; h < G; ++h) acc[h] = fmaf(f[cc], qp[cc * G + h], acc[h]);
+          for (int h = 0; h < G; ++h) {
+            fma_f16pair(acc[h], k01, qp[h]);
+            fma_f16pair(acc[h], k23, qp[G + h]);
+          }
         }
       }
     }
@@ -228,7 +279,7 @@ __global__ void __launch_bounds__(kThreads) attn_decode_fp8_kernel(
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       acc[h] += __shfl_xor_sync(0xFFFFFFFFu, acc[h], 1);  // the two halves of the token
-      const float sc = (ok && t < nc) ? acc[h] * sh.ks[st][t] : -INFINITY;
+      const float sc = (ok && t < nc) ? acc[h] * (sh.ks[st][t] * qf[h]) : -INFINITY;
       acc[h] = sc;
       float v = sc;
       for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
