@@ -318,8 +318,15 @@ __global__ void __launch_bounds__(kThreads) attn_decode_fp8_kernel(
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           const float pw = sh.p[tt][h];
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) o[h][cc] = fmaf(pw, f[cc], o[h][cc]);
+          // two values per instruction on the paired fp32 pipe (each half an
+          // ordinary fp32 FMA)
+          asm("{\n\t.reg .b64 aa, bb, ff, gg, pp;\n\t"
+              "mov.b64 aa, {%0, %1};\n\tmov.b64 bb, {%2, %3};\n\t"
+              "mov.b64 ff, {%4, %5};\n\tmov.b64 gg, {%6, %7};\n\tmov.b64 pp, {%8, %8};\n\t"
+              "fma.rn.f32x2 aa, pp, ff, aa;\n\tfma.rn.f32x2 bb, pp, gg, bb;\n\t"
+              "mov.b64 {%0, %1}, aa;\n\tmov.b64 {%2, %3}, bb;\n\t}"
+              : "+f"(o[h][0]), "+f"(o[h][1]), "+f"(o[h][2]), "+f"(o[h][3])
+              : "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(pw));
         }
       }
     __syncthreads();  // sh.p and sh.red are rewritten by the next chunk
