@@ -92,8 +92,8 @@ SPEC_PEAKS = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0, "fp8_tflops": 4500.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 PHASE_KERNELS = {  # phase -> (kernel name prefix, template arguments as ncu prints them)
     "prefill": ("w4a16_tc_kernel", "<256, 64, 0, 3, 1>"),
-    "decode_m1": ("w4a16_tc_kernel", "<16, 256, 1, 3, 0>"),
-    "decode_m8": ("w4a16_tc_kernel", "<16, 256, 1, 3, 0>"),
+    "decode_m1": ("w4_decode_nvf4_kernel", ""),
+    "decode_m8": ("w4_decode_nvf4_kernel", ""),
     "decode_m64": ("w4a16_tc_kernel", "<64, 256, 1, 3, 0>"),
     "requant": ("nvfp4_encode_kernel", ""),
     "requant_aqn": ("nvfp4_encode_kernel", ""),
