@@ -27,8 +27,9 @@ def test_record_and_load(tmp_path, monkeypatch):
     rows = [(0, "void w4a16_tc_kernel<256, 64, 0, 3, 1>(W4Params)", 500_000_000, 300_000_000),
             (1, "void w4a16_tc_kernel<256, 64, 0, 3, 1>(W4Params)", 520_000_000, 300_000_000),
             (2, "void w4a16_tc_kernel<256, 64, 0, 3, 1>(W4Params)", 900_000_000, 300_000_000),
-            (3, "void w4a16_tc_kernel<16, 256, 1, 3, 0>(W4Params)", 126_000_000, 4_000_000),
-            (4, "nvfp4_encode_kernel(Nvfp4Batch)", 400_000_000, 140_000_000)]
+            (3, "w4_decode_nvf4_kernel(W4Params)", 126_000_000, 4_000_000),
+            (4, "nvfp4_encode_kernel(Nvfp4Batch)", 400_000_000, 140_000_000),
+            (5, "void w4a16_tc_kernel<64, 256, 1, 3, 0>(W4Params)", 131_000_000, 1_000_000)]
     src = tmp_path / "launches.csv"
     src.write_text(_csv(rows))
     bench.record_traffic(str(src))
@@ -37,6 +38,8 @@ def test_record_and_load(tmp_path, monkeypatch):
     assert d["phases"]["prefill"]["dram_bytes_per_launch"] == 820_000_000  # median of three launches
     assert d["phases"]["prefill"]["launches"] == 3
     assert d["phases"]["decode_m1"]["dram_bytes_per_launch"] == 130_000_000
+    assert d["phases"]["decode_m8"]["dram_bytes_per_launch"] == 130_000_000
+    assert d["phases"]["decode_m64"]["dram_bytes_per_launch"] == 132_000_000
     assert d["phases"]["requant"]["dram_bytes_per_launch"] == 540_000_000
     assert "fp8_gemm" not in d["phases"]
     assert bench.load_traffic("prefill") == 820_000_000
