@@ -165,6 +165,10 @@ struct SharedDivisor2 {
       q1 = __fdiv_rn(x1, d);
       return;
     }
+    fast(x0, x1, q0, q1);
+  }
+  // the same for a divisor known to lie in [1e-20, 1e20] (ok set)
+  __device__ __forceinline__ void fast(float x0, float x1, float& q0, float& q1) const {
     uint64_t x, q, r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q) : "l"(x), "l"(y2));
