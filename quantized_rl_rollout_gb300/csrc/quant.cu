@@ -310,11 +310,20 @@ __global__ void __launch_bounds__(256) fp8_a1x128_kernel(const uint16_t* __restr
         if (mode == QRR_SCALE_FP32) {
           s = v448;
           const SharedDivisor2 div(s);
+          if (div.ok) {  // one test per vector for the divisor's range
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            float a, b;
-            div(bf16_lo(w[k]), bf16_hi(w[k]), a, b);
-            out[k >> 1] |= cvt_e4m3x2(a, b) << (16 * (k & 1));
+            for (int k = 0; k < 4; ++k) {
+              float a, b;
+              div.fast(bf16_lo(w[k]), bf16_hi(w[k]), a, b);
+              out[k >> 1] |= cvt_e4m3x2(a, b) << (16 * (k & 1));
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float a, b;
+              div(bf16_lo(w[k]), bf16_hi(w[k]), a, b);
+              out[k >> 1] |= cvt_e4m3x2(a, b) << (16 * (k & 1));
+            }
           }
         } else {
           const int e = pow2_ceil_exp(v448);
