@@ -769,9 +769,8 @@ qrr_status qrr_attention_decode_fp8(const void* q, int32_t B, int32_t Hq, int32_
   float* pm = static_cast<float*>(workspace);
   float* pl = pm + rows;
   float* po = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round_up(rows * 8));
-  (void)pl;
   return from_cuda(launch_attention_decode_fp8(q, k_cache, k_scales, v_cache, v_scales, lens, B, Hq, Hkv, Lmax, out,
-                                               pm, pm + rows, po, dev_status, as_stream(stream)));
+                                               pm, pl, po, dev_status, as_stream(stream)));
 }
 
 qrr_status qrr_token_logprobs_is(const void* logits, int64_t T, int64_t V, const int32_t* tokens,

@@ -38,8 +38,6 @@ __device__ __forceinline__ float e2m1_value(uint32_t nib) {
   return (nib & 8u) ? -mag : mag;
 }
 
-constexpr int kT = 64;  // transpose tile: 64 weight rows x 64 K
-
 int grid_for_elems(int64_t n) {
   int dev = 0, sms = kSMs;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -49,34 +47,64 @@ int grid_for_elems(int64_t n) {
 
 }  // namespace
 
-// WT[k][n] = e2m1(code[n][k]) e4m3(scale[n][k / 16]) in bf16 (exact).
+// WT[k][n] = e2m1(code[n][k]) e4m3(scale[n][k / 16]) in bf16 (exact).  A CTA
+// takes 64 weight rows x kSub tiles of 128 K.  Every code and scale load of
+// its tiles is issued first (one tile alone leaves too few bytes in flight to
+// cover HBM latency); each tile then goes through shared memory as [k][n]
+// rows of 32-bit (n, n + 1) pairs, which the CTA writes out as 128-byte rows
+// of WT.  The 16-byte chunk c of row k is kept at chunk c ^ ((k / 16) mod 8):
+// a warp's pair stores (eight rows 16 apart, four pairs each) and its
+// 16-byte row reads then each touch every bank once.
+constexpr int kTN = 64, kTK = 128;
+constexpr int kSub = 1;
 __global__ void __launch_bounds__(256) nvfp4_transpose_dequant_kernel(const uint8_t* __restrict__ codes,
                                                                       const uint8_t* __restrict__ scales, int N, int K,
                                                                       __nv_bfloat16* __restrict__ wt) {
-  __shared__ __nv_bfloat16 tile[kT][kT + 8];  // [k][n], rows padded against bank conflicts
-  const int n0 = blockIdx.y * kT, k0 = blockIdx.x * kT;
-  // 64 rows x 32 code bytes: thread t takes 8 bytes (16 K values) of row t / 4
-  const int t = threadIdx.x;
-  const int rn = t >> 2, part = t & 3;
-  const int n = n0 + rn;
-  if (n < N) {
-    const uint2 cw = __ldg(reinterpret_cast<const uint2*>(codes + static_cast<int64_t>(n) * (K / 2) + k0 / 2) + part);
-    const float s = e4m3_to_f32(__ldg(scales + static_cast<int64_t>(n) * (K / 16) + k0 / 16 + part));
-    const uint32_t w[2] = {cw.x, cw.y};
+  __shared__ uint4 tile[kTK][kTN / 8];
+  const int t = threadIdx.x, lane = t & 31;
+  const int part = lane & 7;                  // K values [16 part, 16 part + 16) of a tile
+  const int pair = (t >> 5) * 4 + (lane >> 3);  // weight rows na, na + 1
+  const int n0 = blockIdx.y * kTN, kb = blockIdx.x * kTK * kSub;
+  const int na = n0 + 2 * pair;
+  const bool rows_in = na + 1 < N;
+  uint2 c0[kSub], c1[kSub];
+  float s0[kSub], s1[kSub];
+#pragma unroll
+  for (int u = 0; u < kSub; ++u) {
+    const int k0 = kb + u * kTK;
+    const bool in = rows_in && k0 < K;
+    const uint8_t* cr = codes + static_cast<int64_t>(na) * (K / 2) + k0 / 2 + 8 * part;
+    const uint8_t* sr = scales + static_cast<int64_t>(na) * (K / 16) + k0 / 16 + part;
+    c0[u] = in ? __ldg(reinterpret_cast<const uint2*>(cr)) : make_uint2(0u, 0u);
+    c1[u] = in ? __ldg(reinterpret_cast<const uint2*>(cr + K / 2)) : make_uint2(0u, 0u);
+    s0[u] = in ? e4m3_to_f32(__ldg(sr)) : 0.0f;
+    s1[u] = in ? e4m3_to_f32(__ldg(sr + K / 16)) : 0.0f;
+  }
+  uint32_t* tw = reinterpret_cast<uint32_t*>(&tile[0][0]);
+  const int col = (((pair >> 2) ^ part) << 2) | (pair & 3);  // word within a row: (k / 16) mod 8 = part
+#pragma unroll
+  for (int u = 0; u < kSub; ++u) {
+    const int k0 = kb + u * kTK;
+    if (k0 >= K) break;  // uniform over the CTA
+    if (u > 0) __syncthreads();  // the previous tile has been read out
+    const uint32_t w0[2] = {c0[u].x, c0[u].y}, w1[2] = {c1[u].x, c1[u].y};
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const uint32_t nib = (w[i >> 3] >> (4 * (i & 7))) & 0xFu;
-      tile[16 * part + i][rn] = __float2bfloat16_rn(e2m1_value(nib) * s);  // exact product
+      const int sh = 4 * (i & 7);
+      const float v0 = e2m1_value((w0[i >> 3] >> sh) & 0xFu) * s0[u];  // exact products
+      const float v1 = e2m1_value((w1[i >> 3] >> sh) & 0xFu) * s1[u];
+      const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+      tw[(16 * part + i) * (kTN / 2) + col] = *reinterpret_cast<const uint32_t*>(&h);
     }
-  }
-  __syncthreads();
-  // 64 output rows (k) of 64 bf16 (128 bytes): thread t writes 16 bytes
-  for (int idx = t; idx < kT * 8; idx += 256) {
-    const int kl = idx >> 3, seg = idx & 7;
-    const int nn = n0 + 8 * seg;
-    if (nn >= N) continue;
-    const uint4 v = *reinterpret_cast<const uint4*>(&tile[kl][8 * seg]);
-    *reinterpret_cast<uint4*>(wt + static_cast<int64_t>(k0 + kl) * N + nn) = v;
+    __syncthreads();
+    // 128 rows of 64 bf16: four 16-byte chunks per thread
+#pragma unroll
+    for (int idx = t; idx < kTK * 8; idx += 256) {
+      const int kl = idx >> 3, seg = idx & 7;
+      const int nn = n0 + 8 * seg;
+      if (nn >= N) continue;
+      *reinterpret_cast<uint4*>(wt + static_cast<int64_t>(k0 + kl) * N + nn) = tile[kl][seg ^ ((kl >> 4) & 7)];
+    }
   }
 }
 
@@ -253,7 +281,8 @@ cudaError_t launch_lora_backward_prep(const uint8_t* codes, const uint8_t* scale
                                       int N, int K, int r, int t_cols, __nv_bfloat16* wt, uint16_t* at2, uint16_t* bt,
                                       cudaStream_t stream) {
   if (N > 0 && K > 0) {
-    const dim3 grid(static_cast<unsigned>(K / kT), static_cast<unsigned>((N + kT - 1) / kT));
+    const int kc = kTK * kSub;
+    const dim3 grid(static_cast<unsigned>((K + kc - 1) / kc), static_cast<unsigned>((N + kTN - 1) / kTN));
     nvfp4_transpose_dequant_kernel<<<grid, 256, 0, stream>>>(codes, scales, N, K, wt);
   }
   if (r > 0) {
