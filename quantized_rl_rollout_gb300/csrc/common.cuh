@@ -96,6 +96,32 @@ __device__ __forceinline__ float pow2_from_exp(int e) {  // e in [-149, 127]
                    : __uint_as_float(1u << (e + 149));
 }
 
+// Eight E2M1 codes (one word, code k in nibble k) -> four f16x2 (pairs 0-1,
+// 2-3, 4-5, 6-7), one byte unpack feeding four hardware conversions.
+__device__ __forceinline__ void f16x2x4_from_e2m1x8(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// An f16x2 of E2M1 values (only the top mantissa bit can be set) re-read as
+// the bf16x2 of the same values times 2^-112: each half's exponent and
+// mantissa fields move down three bits (an f16 exponent under the bf16 bias,
+// 127 - 15 = 112; the bits shifted out are zero), the sign stays.  One bf16x2
+// multiply by s 2^112 then gives v s exactly whenever v s has at most eight
+// significant bits and both factors are normal bf16 numbers.
+__device__ __forceinline__ uint32_t e2m1_f16x2_rebias_bf16x2(uint32_t h) {
+  return ((h & 0x7FFF7FFFu) >> 3) | (h & 0x80008000u);
+}
+
 // x * 2^-e, exact for the magnitudes that reach the E4M3 grid.
 struct Pow2Scaler {
   float f1, f2;

@@ -161,25 +161,9 @@ __device__ __forceinline__ void f16x2x2_from_e4m3x4(uint32_t four, uint32_t& lo,
       : "r"(four));
 }
 
-// Eight E2M1 codes (one word, code k in nibble k) -> four f16x2 (pairs 0-1,
-// 2-3, 4-5, 6-7), one byte unpack feeding four hardware conversions.
-__device__ __forceinline__ void f16x2x4_from_e2m1x8(uint32_t w, uint32_t (&o)[4]) {
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
-      : "r"(w));
-}
-
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
 
@@ -208,14 +192,10 @@ __device__ __forceinline__ void dequant64(const uint32_t* w, uint32_t scales4, u
         for (int b = 0; b < 4; ++b) out[8 * g + 4 * q + b] = hmul2(h[b], sg[g]);
       }
   } else {
-    // The E2M1 values come out of the hardware conversion as f16, where only
-    // the top mantissa bit can be set.  Moving each half's exponent and
-    // mantissa fields down by three bits re-reads them as the bf16 of
-    // v 2^-112 (an f16 exponent field under the bf16 bias, 127 - 15 = 112;
-    // the three mantissa bits shifted out are zero, zero stays zero), and
-    // one bf16x2 multiply by s_b 2^112 returns v s_b exactly: both factors
-    // and the product are normal bf16 numbers, the product has at most six
-    // significant bits.
+    // The hardware conversion's f16 E2M1 values re-read as bf16 v 2^-112,
+    // then one bf16x2 multiply by s_b 2^112 returns v s_b exactly: both
+    // factors and the product are normal bf16 numbers, the product has at
+    // most six significant bits.
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       const float sv = e4m3_to_f32((scales4 >> (8 * g)) & 0xFFu) * 0x1p112f;
@@ -226,7 +206,7 @@ __device__ __forceinline__ void dequant64(const uint32_t* w, uint32_t scales4, u
         f16x2x4_from_e2m1x8(w[2 * g + q], h);
 #pragma unroll
         for (int b = 0; b < 4; ++b)
-          out[8 * g + 4 * q + b] = bmul2(((h[b] & 0x7FFF7FFFu) >> 3) | (h[b] & 0x80008000u), s2);
+          out[8 * g + 4 * q + b] = bmul2(e2m1_f16x2_rebias_bf16x2(h[b]), s2);
       }
     }
   }

@@ -31,13 +31,6 @@ namespace qrr {
 
 namespace {
 
-// |e2m1| values by magnitude code
-__device__ __forceinline__ float e2m1_value(uint32_t nib) {
-  const uint32_t m = nib & 7u;
-  const float mag = m < 4 ? 0.5f * static_cast<float>(m) : (m < 6 ? static_cast<float>(m - 2) : (m == 6 ? 4.0f : 6.0f));
-  return (nib & 8u) ? -mag : mag;
-}
-
 int grid_for_elems(int64_t n) {
   int dev = 0, sms = kSMs;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -87,14 +80,24 @@ __global__ void __launch_bounds__(256) nvfp4_transpose_dequant_kernel(const uint
     const int k0 = kb + u * kTK;
     if (k0 >= K) break;  // uniform over the CTA
     if (u > 0) __syncthreads();  // the previous tile has been read out
+    // the two rows' block scales times 2^112 as one bf16x2 (exact: four
+    // significant bits, at most 448 2^112)
+    uint32_t s2;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(s2) : "f"(s1[u] * 0x1p112f), "f"(s0[u] * 0x1p112f));
     const uint32_t w0[2] = {c0[u].x, c0[u].y}, w1[2] = {c1[u].x, c1[u].y};
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int sh = 4 * (i & 7);
-      const float v0 = e2m1_value((w0[i >> 3] >> sh) & 0xFu) * s0[u];  // exact products
-      const float v1 = e2m1_value((w1[i >> 3] >> sh) & 0xFu) * s1[u];
-      const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
-      tw[(16 * part + i) * (kTN / 2) + col] = *reinterpret_cast<const uint32_t*>(&h);
+    for (int h = 0; h < 2; ++h) {
+      uint32_t a[4], b[4];  // f16x2 of K (2q, 2q + 1) of rows na and na + 1
+      f16x2x4_from_e2m1x8(w0[h], a);
+      f16x2x4_from_e2m1x8(w1[h], b);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t ra = e2m1_f16x2_rebias_bf16x2(a[q]), rb = e2m1_f16x2_rebias_bf16x2(b[q]);
+        const int k = 16 * part + 8 * h + 2 * q;
+        // (row na, row na + 1) at K k and k + 1, times (s0, s1): exact products
+        tw[k * (kTN / 2) + col] = bmul2(__byte_perm(ra, rb, 0x5410), s2);
+        tw[(k + 1) * (kTN / 2) + col] = bmul2(__byte_perm(ra, rb, 0x7632), s2);
+      }
     }
     __syncthreads();
     // 128 rows of 64 bf16: four 16-byte chunks per thread
