@@ -59,6 +59,11 @@ __device__ __forceinline__ float aqn_z(uint32_t w) {
   return __fmul_rn(__fsub_rn(f, 510.0f), 1.7320508075688772f * 0x1p-8f);
 }
 
+// The largest |z| aqn_z can return, with the same rounding: fp32 of 510
+// times the same constant.  fp32(sigma) times it bounds |fp32(sigma z)|,
+// because rounding is monotone.
+__device__ __forceinline__ float aqn_zmax() { return __fmul_rn(510.0f, 1.7320508075688772f * 0x1p-8f); }
+
 // The four generator words of elements 4 c .. 4 c + 3 of tensor `tensor`.
 __device__ __forceinline__ void aqn_words(uint64_t c, uint32_t tensor, const AqnParams& a, uint32_t (&r)[4]) {
   philox4x32_10(static_cast<uint32_t>(c), static_cast<uint32_t>(c >> 32), tensor, a.step,

@@ -30,6 +30,11 @@ namespace {
 
 constexpr int kStreamChunk = 16384;  // bytes: 8192 bf16, 512 NVFP4 blocks
 constexpr int kStreamStages = 6;     // absmax: 2 CTAs per SM
+// absmax with AQN noise: its arithmetic, not HBM, bounds it, so a shallower
+// ring and more CTAs per SM (more warps to issue from: 607 -> 582 us for the
+// 8B-class set against 6 stages at 2 CTAs per SM)
+constexpr int kAqnAmaxStages = 2;
+constexpr int kAqnAmaxPerSm = 6;
 constexpr int kEncodeStages = 3;     // encode: 4 CTAs per SM (more warps for its arithmetic)
 constexpr int kEncodeThreads = 256;  // encode: threads per CTA, each kStreamChunk / 32 / kEncodeThreads blocks a chunk
 constexpr int kEncodeBlocksPerThread = kStreamChunk / 32 / kEncodeThreads;
@@ -62,18 +67,31 @@ __device__ __forceinline__ bool stream_issue(StreamRing& r, uint8_t* ring, int64
 // patterns; `amax_bits[j]` must be zero before the launch.  Each warp keeps a
 // running max over its chunks and publishes it with one atomic per tensor it
 // leaves (same-address atomics serialize in L2).
+//
+// With AQN noise only the largest |W'| of a tensor matters, W' = bf16(W + t)
+// with |t| <= T = fp32(sigma) * zmax.  Over a warp's share of a chunk, with M
+// its largest |W|: the element holding M has |W'| >= L = bf16(fp32(M - T))
+// (or 0), and an element has |W'| <= bf16(fp32(|W| + T)), both because
+// rounding is monotone.  So only 8-value vectors whose largest |W| passes
+// bf16(fp32(max + T)) >= L can hold the share's largest |W'|; the warp
+// queues those and draws noise for them alone, exactly.  Non-finite input
+// (M at or past the infinity pattern) takes every vector.
 template <bool NOISE>
-__global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __grid_constant__ Nvfp4Batch batch) {
+__global__ void __launch_bounds__(256, NOISE ? kAqnAmaxPerSm : 2) nvfp4_amax_kernel(const __grid_constant__ Nvfp4Batch batch) {
+  constexpr int S = NOISE ? kAqnAmaxStages : kStreamStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* ring = smem_raw;
-  StreamRing& r = *reinterpret_cast<StreamRing*>(smem_raw + kStreamStages * kStreamChunk);
+  StreamRing& r = *reinterpret_cast<StreamRing*>(smem_raw + S * kStreamChunk);
   __shared__ int64_t s_first[kMaxJobs + 1];
   __shared__ int64_t s_bytes[kMaxJobs];
   __shared__ const uint8_t* s_src[kMaxJobs];
   __shared__ uint32_t s_tensor[kMaxJobs];
+  constexpr int kVecPerThread = kStreamChunk / 16 / 256;
+  __shared__ uint16_t s_queue[NOISE ? 8 : 1][NOISE ? 32 * kVecPerThread : 1];  // per warp: vectors to draw noise for
   const int count = batch.count;
   const int64_t chunks = batch.total_amax_chunks;
   const AqnParams aqn = batch.aqn;
+  const float tbound = __fmul_rn(aqn.sigma, aqn_zmax());  // bounds |fp32(sigma z)|
   for (int j = threadIdx.x; j < count; j += blockDim.x) {
     s_first[j] = batch.job[j].first_amax_chunk;
     s_bytes[j] = batch.job[j].N * batch.job[j].K * 2;
@@ -82,7 +100,7 @@ __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __grid_constant__
   }
   if (threadIdx.x == 0) {
     s_first[count] = chunks;
-    for (int s = 0; s < kStreamStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&r.full[s], 1);
       mbar_init(&r.empty[s], 8);  // one arrival per warp
     }
@@ -103,7 +121,7 @@ __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __grid_constant__
     bytes = static_cast<uint32_t>(left < kStreamChunk ? left : kStreamChunk);
   };
   if (threadIdx.x == 0)
-    for (int64_t i = 0; i < kStreamStages - 1; ++i) stream_issue<kStreamStages>(r, ring, i, steps, src_of, status);
+    for (int64_t i = 0; i < S - 1; ++i) stream_issue<S>(r, ring, i, steps, src_of, status);
   int cur = -1, j = 0;
   uint32_t run = 0;
   auto publish = [&]() {
@@ -115,9 +133,9 @@ __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __grid_constant__
     run = 0;
   };
   for (int64_t i = 0; i < steps; ++i) {
-    if (threadIdx.x == 0 && !stream_issue<kStreamStages>(r, ring, i + kStreamStages - 1, steps, src_of, status)) break;
-    const int s = static_cast<int>(i % kStreamStages);
-    if (!mbar_wait(&r.full[s], (i / kStreamStages) & 1, &r.abort, status)) break;
+    if (threadIdx.x == 0 && !stream_issue<S>(r, ring, i + S - 1, steps, src_of, status)) break;
+    const int s = static_cast<int>(i % S);
+    if (!mbar_wait(&r.full[s], (i / S) & 1, &r.abort, status)) break;
     const int64_t c = blockIdx.x + i * gridDim.x;
     while (s_first[j + 1] <= c) ++j;
     if (j != cur) {
@@ -128,13 +146,40 @@ __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __grid_constant__
     const int nvec = static_cast<int>((left < kStreamChunk ? left : kStreamChunk) / 16);
     const uint4* v = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * kStreamChunk);
     const int64_t e0 = (c - s_first[j]) * (kStreamChunk / 2);  // first element of the chunk
+    if constexpr (!NOISE) {
 #pragma unroll
-    for (int u = 0; u < kStreamChunk / 16 / 256; ++u) {
-      const int e = u * 256 + threadIdx.x;
-      if (e < nvec) {
-        uint4 x = v[e];
-        if constexpr (NOISE) x = aqn_noisy8(x, e0 + 8 * e, s_tensor[j], aqn);
-        run = max(run, absmax_bits8(x));
+      for (int u = 0; u < kVecPerThread; ++u) {
+        const int e = u * 256 + threadIdx.x;
+        if (e < nvec) run = max(run, absmax_bits8(v[e]));
+      }
+    } else {
+      uint32_t vm[kVecPerThread], m = 0u;
+#pragma unroll
+      for (int u = 0; u < kVecPerThread; ++u) {
+        const int e = u * 256 + threadIdx.x;
+        vm[u] = e < nvec ? absmax_bits8(v[e]) : 0u;
+        m = max(m, vm[u]);
+      }
+      const uint32_t M = __reduce_max_sync(0xFFFFFFFFu, m);
+      const int lane = threadIdx.x & 31;
+      uint16_t* const q = s_queue[threadIdx.x >> 5];
+      int cnt = 0;
+      const float lo = __fsub_rn(bf16bits_to_f32(M), tbound);
+      const uint32_t L = lo > 0.0f ? static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) : 0u;
+#pragma unroll
+      for (int u = 0; u < kVecPerThread; ++u) {
+        const int e = u * 256 + threadIdx.x;
+        const uint32_t ub = static_cast<uint32_t>(
+            __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(bf16bits_to_f32(vm[u]), tbound))));
+        const bool cand = e < nvec && (M >= 0x7F80u || ub >= L);
+        const uint32_t mask = __ballot_sync(0xFFFFFFFFu, cand);
+        if (cand) q[cnt + __popc(mask & ((1u << lane) - 1u))] = static_cast<uint16_t>(e);
+        cnt += __popc(mask);
+      }
+      __syncwarp();
+      for (int i = lane; i < cnt; i += 32) {
+        const int e = q[i];
+        run = max(run, absmax_bits8(aqn_noisy8(v[e], e0 + 8 * e, s_tensor[j], aqn)));
       }
     }
     __syncwarp();
@@ -144,8 +189,8 @@ __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const __grid_constant__
   // every issued copy has landed before the CTA exits
   if (threadIdx.x == 0) {
     volatile int no_abort = 0;
-    for (int64_t k = steps - 1; k >= 0 && k >= steps - kStreamStages; --k)
-      mbar_wait(&r.full[k % kStreamStages], (k / kStreamStages) & 1, &no_abort, status);
+    for (int64_t k = steps - 1; k >= 0 && k >= steps - S; --k)
+      mbar_wait(&r.full[k % S], (k / S) & 1, &no_abort, status);
   }
 }
 
@@ -449,6 +494,7 @@ int grid_for(int64_t work_units, int per_sm) {
 
 constexpr int kNvfp4Chunk = kStreamChunk;
 constexpr int kNvfp4Smem = kStreamStages * kStreamChunk + static_cast<int>(sizeof(StreamRing));
+constexpr int kAqnAmaxSmem = kAqnAmaxStages * kStreamChunk + static_cast<int>(sizeof(StreamRing));
 constexpr int kEncodeSmem = kEncodeStages * kStreamChunk + static_cast<int>(sizeof(StreamRing));
 
 cudaError_t launch_nvfp4(Nvfp4Batch& batch, cudaStream_t stream) {
@@ -470,7 +516,7 @@ cudaError_t launch_nvfp4(Nvfp4Batch& batch, cudaStream_t stream) {
   if (!attr) {
     err = cudaFuncSetAttribute(nvfp4_amax_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kNvfp4Smem);
     if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(nvfp4_amax_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kNvfp4Smem);
+      err = cudaFuncSetAttribute(nvfp4_amax_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAqnAmaxSmem);
     if (err == cudaSuccess)
       err = cudaFuncSetAttribute(nvfp4_encode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kEncodeSmem);
     if (err == cudaSuccess)
@@ -480,7 +526,8 @@ cudaError_t launch_nvfp4(Nvfp4Batch& batch, cudaStream_t stream) {
   }
   // sigma 0 adds exactly nothing (W + 0 z = W), so it takes the plain kernels
   if (batch.aqn.sigma != 0.0f) {
-    if (amax_chunks > 0) nvfp4_amax_kernel<true><<<grid_for(amax_chunks, 2), 256, kNvfp4Smem, stream>>>(batch);
+    if (amax_chunks > 0)
+      nvfp4_amax_kernel<true><<<grid_for(amax_chunks, kAqnAmaxPerSm), 256, kAqnAmaxSmem, stream>>>(batch);
     nvfp4_encode_kernel<true><<<grid_for(enc_chunks, 4), kEncodeThreads, kEncodeSmem, stream>>>(batch);
   } else {
     if (amax_chunks > 0) nvfp4_amax_kernel<false><<<grid_for(amax_chunks, 2), 256, kNvfp4Smem, stream>>>(batch);

@@ -64,6 +64,32 @@ def test_nvfp4_noisy_requant(q, sigma):
         assert not np.array_equal(ref[2][0], plain)
 
 
+@pytest.mark.parametrize("sigma", [1e-4, 3e-3, 5e-2, 1.0])
+def test_nvfp4_noisy_absmax_near_ties(q, sigma):
+    """The absmax pass draws noise only for values that can still hold a
+    tensor's largest |W'| (within fp32(sigma) zmax of the largest |W| of a
+    warp's share, by a bound that rounding cannot break).  Many near-ties
+    around the maximum, in both signs, one tensor whose largest |W| sits in a
+    single 8-value vector, and one spread evenly: the tensor scales and codes
+    must still equal the oracle's for small, moderate and overwhelming noise."""
+    g = np.random.default_rng(int(sigma * 1e6) + 3)
+    a = (g.standard_normal((256, 512)) * 0.02).astype(np.float32)
+    idx = g.choice(a.size, 300, replace=False)
+    a.flat[idx] = np.where(g.random(300) < 0.5, -1.0, 1.0) * (0.5 - g.random(300) * 0.01)
+    b = (g.standard_normal((128, 1024)) * 0.02).astype(np.float32)
+    b[77, 8:16] = np.float32(0.25)
+    c = np.full((64, 256), 0.125, np.float32) * np.where(g.random((64, 256)) < 0.5, -1.0, 1.0).astype(np.float32)
+    Ws = [torch.from_numpy(x).to(torch.bfloat16).to(DEV) for x in (a, b, c)]
+    outs = [_nv_out(w.shape[0], w.shape[1]) for w in Ws]
+    s32 = np.float32(sigma)
+    q.requantize_weights_aqn(Ws, outs, float(s32), 4242, 9)
+    torch.cuda.synchronize()
+    ref = aqn.requantize_aqn([to_np(w) for w in Ws], s32, 4242, 9)
+    for (cd, sc, t), (rc, rs, rt) in zip(outs, ref):
+        assert t.item() == float(rt)
+        assert np.array_equal(sc.cpu().numpy(), rs) and np.array_equal(cd.cpu().numpy(), rc)
+
+
 @pytest.mark.parametrize("mode", [0, 1])
 def test_fp8_noisy_requant(q, mode):
     shapes = [(512, 256), (200, 1024), (1024, 128)]
