@@ -869,7 +869,7 @@ qrr_status qrr_wait_probe(int64_t limit_cycles, int32_t arrive, int32_t* dev_sta
 
 qrr_status qrr_requantize_weights(const qrr_weight_desc* descs, int32_t count, int32_t format, int32_t scale_mode,
                                   void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
-  return requantize(descs, count, format, scale_mode, AqnParams{0.0f, 0u, 0ull}, workspace, workspace_bytes,
+  return requantize(descs, count, format, scale_mode, aqn_params(0.0f, 0u, 0ull), workspace, workspace_bytes,
                     dev_status, stream);
 }
 
@@ -877,7 +877,7 @@ qrr_status qrr_requantize_weights_aqn(const qrr_weight_desc* descs, int32_t coun
                                       int32_t scale_mode, float sigma, uint64_t seed, int32_t step, void* workspace,
                                       size_t workspace_bytes, int32_t* dev_status, void* stream) {
   if (!(sigma >= 0.0f) || sigma == INFINITY || step < 0) return QRR_ERR_INVALID_ARG;
-  return requantize(descs, count, format, scale_mode, AqnParams{sigma, static_cast<uint32_t>(step), seed}, workspace,
+  return requantize(descs, count, format, scale_mode, aqn_params(sigma, static_cast<uint32_t>(step), seed), workspace,
                     workspace_bytes, dev_status, stream);
 }
 
@@ -893,7 +893,7 @@ qrr_status qrr_aqn_noise_probe(float* out, int64_t n, int64_t start, uint64_t se
   if (reinterpret_cast<uintptr_t>(out) & 3u) return QRR_ERR_MISALIGNED;
   if (injected_cuda_fault()) return QRR_ERR_CUDA;
   return from_cuda(launch_aqn_noise_probe(out, n, start, static_cast<uint32_t>(tensor),
-                                          AqnParams{1.0f, static_cast<uint32_t>(step), seed}, as_stream(stream)));
+                                          aqn_params(1.0f, static_cast<uint32_t>(step), seed), as_stream(stream)));
 }
 
 qrr_status qrr_round_probe(const float* in, int64_t n, int32_t fmt, uint8_t* out, void* stream) {

@@ -25,22 +25,36 @@ struct AqnParams {
   float sigma;    // 0: no noise
   uint32_t step;  // training step (third counter word)
   uint64_t seed;  // key
+  // the generator's round keys for this seed (round i: the seed's words
+  // plus i times the Weyl constants), set by aqn_params(); kernels read them
+  // straight from their launch parameters
+  uint32_t rk0[10], rk1[10];
 };
 
-__device__ __forceinline__ void philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
-                                              uint32_t k1, uint32_t (&r)[4]) {
+__host__ __device__ inline AqnParams aqn_params(float sigma, uint32_t step, uint64_t seed) {
+  AqnParams a{sigma, step, seed, {}, {}};
+  uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+  for (int i = 0; i < 10; ++i) {
+    a.rk0[i] = k0;
+    a.rk1[i] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return a;
+}
+
+__device__ __forceinline__ void philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, const AqnParams& a,
+                                              uint32_t (&r)[4]) {
 #pragma unroll
   for (int i = 0; i < 10; ++i) {
     const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c0, p1 = static_cast<uint64_t>(0xCD9E8D57u) * c2;
     const uint32_t hi0 = static_cast<uint32_t>(p0 >> 32), lo0 = static_cast<uint32_t>(p0);
     const uint32_t hi1 = static_cast<uint32_t>(p1 >> 32), lo1 = static_cast<uint32_t>(p1);
-    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    const uint32_t n0 = hi1 ^ c1 ^ a.rk0[i], n2 = hi0 ^ c3 ^ a.rk1[i];
     c0 = n0;
     c1 = lo1;
     c2 = n2;
     c3 = lo0;
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
   }
   r[0] = c0;
   r[1] = c1;
@@ -49,14 +63,15 @@ __device__ __forceinline__ void philox4x32_10(uint32_t c0, uint32_t c1, uint32_t
 }
 
 // The standardized sum of the four bytes of a word: one dot-product
-// instruction sums the bytes, an add to 2^23 turns the sum into an fp32
-// integer exactly, and (sum - 510) is scaled by fp32(sqrt 3) 2^-8 in one
-// correctly rounded multiply -- bit for bit fp32(sqrt 3) times the exact
-// (sum - 510) 2^-8, as scaling by a power of two commutes with rounding.
+// instruction sums the bytes, the bit pattern 2^23 + sum less 2^23 + 510
+// (both integers below 2^24, so the difference is exact) is sum - 510, and
+// one correctly rounded multiply scales it by fp32(sqrt 3) 2^-8 -- bit for
+// bit fp32(sqrt 3) times the exact (sum - 510) 2^-8, as scaling by a power
+// of two commutes with rounding.
 __device__ __forceinline__ float aqn_z(uint32_t w) {
-  const uint32_t sum = __dp4a(w, 0x01010101u, 0u);                          // 0 .. 1020
-  const float f = __fsub_rn(__uint_as_float(0x4B000000u | sum), 8388608.0f);  // = sum, exactly
-  return __fmul_rn(__fsub_rn(f, 510.0f), 1.7320508075688772f * 0x1p-8f);
+  const uint32_t sum = __dp4a(w, 0x01010101u, 0u);  // 0 .. 1020
+  const float f = __fsub_rn(__uint_as_float(0x4B000000u | sum), 8389118.0f);  // = sum - 510, exactly
+  return __fmul_rn(f, 1.7320508075688772f * 0x1p-8f);
 }
 
 // The largest |z| aqn_z can return, with the same rounding: fp32 of 510
@@ -66,14 +81,18 @@ __device__ __forceinline__ float aqn_zmax() { return __fmul_rn(510.0f, 1.7320508
 
 // The four generator words of elements 4 c .. 4 c + 3 of tensor `tensor`.
 __device__ __forceinline__ void aqn_words(uint64_t c, uint32_t tensor, const AqnParams& a, uint32_t (&r)[4]) {
-  philox4x32_10(static_cast<uint32_t>(c), static_cast<uint32_t>(c >> 32), tensor, a.step,
-                static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32), r);
+  philox4x32_10(static_cast<uint32_t>(c), static_cast<uint32_t>(c >> 32), tensor, a.step, a, r);
 }
 
-// bf16 bits of bf16_rn(fp32(w) + fp32(sigma z)).
-__device__ __forceinline__ uint32_t aqn_noisy(uint32_t wbits, float sigma, float z) {
-  const float s = __fadd_rn(__uint_as_float(wbits << 16), __fmul_rn(sigma, z));
-  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(s)));
+// bf16x2 bits of bf16_rn(fp32(w) + fp32(sigma z)) for both halves of the
+// bf16x2 w (za for the low half, zb for the high one): one paired
+// round-to-nearest-even conversion.
+__device__ __forceinline__ uint32_t aqn_noisy2(uint32_t w, float sigma, float za, float zb) {
+  const float lo = __fadd_rn(__uint_as_float(w << 16), __fmul_rn(sigma, za));
+  const float hi = __fadd_rn(__uint_as_float(w & 0xFFFF0000u), __fmul_rn(sigma, zb));
+  uint32_t o;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o) : "f"(hi), "f"(lo));
+  return o;
 }
 
 // Eight consecutive bf16 values starting at element e0 (a multiple of 8):
@@ -87,7 +106,7 @@ __device__ __forceinline__ uint4 aqn_noisy8(uint4 v, uint64_t e0, uint32_t tenso
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t za = i < 2 ? r0[2 * i] : r1[2 * i - 4], zb = i < 2 ? r0[2 * i + 1] : r1[2 * i - 3];
-    o[i] = aqn_noisy(w[i] & 0xFFFFu, a.sigma, aqn_z(za)) | (aqn_noisy(w[i] >> 16, a.sigma, aqn_z(zb)) << 16);
+    o[i] = aqn_noisy2(w[i], a.sigma, aqn_z(za), aqn_z(zb));
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }

@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(256, NOISE ? kAqnAmaxPerSm : 2) nvfp4_amax_ker
   __shared__ uint16_t s_queue[NOISE ? 8 : 1][NOISE ? 32 * kVecPerThread : 1];  // per warp: vectors to draw noise for
   const int count = batch.count;
   const int64_t chunks = batch.total_amax_chunks;
-  const AqnParams aqn = batch.aqn;
+  const AqnParams& aqn = batch.aqn;  // read from the launch parameters
   const float tbound = __fmul_rn(aqn.sigma, aqn_zmax());  // bounds |fp32(sigma z)|
   for (int j = threadIdx.x; j < count; j += blockDim.x) {
     s_first[j] = batch.job[j].first_amax_chunk;
@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(kEncodeThreads, 4) nvfp4_encode_kernel(const _
   __shared__ uint32_t s_tensor[kMaxJobs];
   const int count = batch.count;
   const int64_t chunks = batch.total_encode_chunks;
-  const AqnParams aqn = batch.aqn;
+  const AqnParams& aqn = batch.aqn;  // read from the launch parameters
   for (int j = threadIdx.x; j < count; j += blockDim.x) {
     s_tensor[j] = batch.job[j].tensor;
     s_first[j] = batch.job[j].first_encode_chunk;
@@ -561,7 +561,7 @@ cudaError_t launch_fp8_w128(Fp8WBatch& batch, cudaStream_t stream) {
 }
 
 __global__ void aqn_noise_probe_kernel(float* __restrict__ out, int64_t n, int64_t start, uint32_t tensor,
-                                       AqnParams a) {
+                                       const __grid_constant__ AqnParams a) {
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t e = start + i;
