@@ -140,7 +140,8 @@ __global__ void lora_factor_transpose_kernel(const uint16_t* __restrict__ A, con
 //   warp 1  MMA: 4 x tcgen05.mma kind::f16 (M128 N t_cols K16), A and B MN-major
 //   warps 2..5  the 128 x t_cols accumulator out of TMEM, pairs summed, stored
 namespace {
-constexpr int kGStages = 4;
+constexpr int kGStages = 3;
+constexpr int kGPerSm = 2;  // resident CTAs per SM (shared memory and TMEM allow two)
 constexpr int kGA = 2 * 64 * 128;      // X stage: 2 boxes of 64 tokens x 64 columns (bf16)
 constexpr int kGB = 2 * 64 * 128;      // tp stage: up to 2 boxes
 constexpr int kGStage = kGA + kGB;     // 32 KB
@@ -155,7 +156,7 @@ struct GradTcParams {
   int32_t* status;
 };
 
-__global__ void __launch_bounds__(192, 1) lora_grad_tc_kernel(const __grid_constant__ GradTcParams p) {
+__global__ void __launch_bounds__(192, kGPerSm) lora_grad_tc_kernel(const __grid_constant__ GradTcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   struct Ctl {
@@ -275,8 +276,14 @@ __global__ void lora_grad_reduce_kernel(const float* __restrict__ part, int slic
 
 int lora_grad_slices(int64_t M, int64_t C) {
   const int64_t col_ctas = (C + 127) / 128;
-  int64_t s = (kSMs + col_ctas - 1) / col_ctas;  // about one wave of CTAs
+  // as many token slices as keep every CTA in one wave of kGPerSm per SM
+  // (rounding up would leave a few CTAs to run their whole slice afterwards)
+  int64_t s = static_cast<int64_t>(kSMs) * kGPerSm / col_ctas;
   s = s < (M + 255) / 256 ? s : (M + 255) / 256;  // at least 256 tokens per slice
+  if (s < 1) s = 1;
+  // slices are whole 64-token stages: count only those that get tokens
+  const int64_t per = ((M + s - 1) / s + 63) / 64 * 64;
+  s = per > 0 ? (M + per - 1) / per : 1;
   return static_cast<int>(s < 1 ? 1 : s);
 }
 
