@@ -19,7 +19,7 @@
 // conversion per key value, the most frequent instruction of the kernel.  Split over the sequence: a CTA
 // takes 512 tokens of one (sequence, KV head), streams their key and value
 // rows and scales through shared memory in 64-token chunks by bulk copies
-// (three in flight), and writes a partial (max, sum, unnormalized output) per
+// (two in flight), and writes a partial (max, sum, unnormalized output) per
 // query head of the group; a second kernel merges the partials in split
 // order.
 #include <cuda_bf16.h>
@@ -76,17 +76,27 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
 }
 
 constexpr int CH = 64;      // tokens per pipeline chunk
-constexpr int NST = 3;      // chunks in flight
+// chunks in flight: two leave room for six CTAs per SM (the per-warp output
+// buffer shares the ring's space), and the warps of six CTAs cover the copy
+// latency better than a third chunk of three or four CTAs did (136 against
+// 147 and 163 us for 64 sequences)
+constexpr int NST = 2;
 constexpr int TSPLIT = 512; // tokens per CTA
 
 template <int G>
 struct AttnShared {
-  uint8_t k[NST][CH * D];  // 8 KB per chunk
-  uint8_t v[NST][CH * D];
+  union {
+    struct {
+      uint8_t k[NST][CH * D];  // 8 KB per chunk
+      uint8_t v[NST][CH * D];
+    } ring;
+    // per-warp outputs, merged at the end: written only after the last
+    // chunk's barrier, when no warp reads the ring and no copy is in flight
+    float o[4][G][D];
+  } u;
   float ks[NST][CH], vs[NST][CH];
   float p[CH][G];   // this chunk's softmax numerators times the value row scale
   float red[4][G];  // per-warp partial max / sum
-  float o[4][G][D]; // per-warp outputs, merged at the end
   uint64_t full[NST], empty[NST];
   int abort;
 };
@@ -228,8 +238,8 @@ __global__ void __launch_bounds__(kThreads) attn_decode_fp8_kernel(
     const int nc = min(CH, n - c * CH), nr = (nc + 3) & ~3;
     const int64_t r = row0 + c * CH;
     mbar_arrive_expect_tx(&sh.full[st], 2 * nc * D + 2 * nr * 4);
-    bulk_load(sh.k[st], kc + r * D, nc * D, &sh.full[st]);
-    bulk_load(sh.v[st], vc + r * D, nc * D, &sh.full[st]);
+    bulk_load(sh.u.ring.k[st], kc + r * D, nc * D, &sh.full[st]);
+    bulk_load(sh.u.ring.v[st], vc + r * D, nc * D, &sh.full[st]);
     bulk_load(sh.ks[st], ksc + r, nr * 4, &sh.full[st]);
     bulk_load(sh.vs[st], vsc + r, nr * 4, &sh.full[st]);
   };
@@ -256,7 +266,7 @@ __global__ void __launch_bounds__(kThreads) attn_decode_fp8_kernel(
 #pragma unroll
     for (int h = 0; h < G; ++h) acc[h] = 0.0f;
     if (ok && t < nc) {
-      const uint4* row = reinterpret_cast<const uint4*>(sh.k[st] + t * D);
+      const uint4* row = reinterpret_cast<const uint4*>(sh.u.ring.k[st] + t * D);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int piece = 4 * half + ((i + t) & 3);
@@ -314,7 +324,7 @@ __global__ void __launch_bounds__(kThreads) attn_decode_fp8_kernel(
     if (ok)
       for (int tt = warp; tt < nc; tt += 4) {
         float f[4];
-        e4m3x4_to_f32(reinterpret_cast<const uint32_t*>(sh.v[st] + tt * D)[lane], f);
+        e4m3x4_to_f32(reinterpret_cast<const uint32_t*>(sh.u.ring.v[st] + tt * D)[lane], f);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           const float pw = sh.p[tt][h];
@@ -340,7 +350,7 @@ __global__ void __launch_bounds__(kThreads) attn_decode_fp8_kernel(
   // ---- merge the warps' outputs and the threads' sums
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    *reinterpret_cast<float4*>(&sh.o[warp][h][4 * lane]) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+    *reinterpret_cast<float4*>(&sh.u.o[warp][h][4 * lane]) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
     float v = l_run[h];
     for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
     if (lane == 0) sh.red[warp][h] = v;
@@ -348,7 +358,7 @@ __global__ void __launch_bounds__(kThreads) attn_decode_fp8_kernel(
   __syncthreads();
   for (int i = tid; i < G * D; i += kThreads) {
     const int h = i / D, d = i % D;
-    part_o[pidx * D + i] = sh.o[0][h][d] + sh.o[1][h][d] + sh.o[2][h][d] + sh.o[3][h][d];
+    part_o[pidx * D + i] = sh.u.o[0][h][d] + sh.u.o[1][h][d] + sh.u.o[2][h][d] + sh.u.o[3][h][d];
   }
   if (tid < G) {
     part_m[pidx + tid] = ok ? m_run[tid] : -INFINITY;
