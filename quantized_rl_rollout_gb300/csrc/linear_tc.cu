@@ -578,8 +578,14 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
           for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]) * v[i];
         } else {
           tmem_ld_wait();
+          // two outputs per instruction on the paired fp32 pipe (each half
+          // one correctly rounded fp32 multiply)
 #pragma unroll
-          for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]) * g;
+          for (int i = 0; i < CW; i += 2)
+            asm("{\n\t.reg .b64 rr, gg;\n\tmov.b64 rr, {%2, %3};\n\tmov.b64 gg, {%4, %4};\n\t"
+                "mul.rn.f32x2 rr, rr, gg;\n\tmov.b64 {%0, %1}, rr;\n\t}"
+                : "=f"(v[i]), "=f"(v[i + 1])
+                : "f"(__uint_as_float(r[i])), "f"(__uint_as_float(r[i + 1])), "f"(g));
         }
         if (part != nullptr) {
           float* const dst = part + static_cast<int64_t>(mb) * N + n;
@@ -594,17 +600,19 @@ __global__ void __maxnreg__((Cfg<BN, BK, G, PAIR>::MAXNREG)) w4a16_tc_kernel(con
         } else {
           __nv_bfloat16* const dst = y + static_cast<int64_t>(mb) * N + n;
           if (cnt >= CW) {
-            // Token pairs: lanes n (even) and n + 1 swap one value, so each
-            // lane holds two adjacent outputs of one token and writes them as
-            // one word (the even lane token i, the odd lane token i + 1): one
-            // packed conversion and one store per two outputs.
+            // Token pairs: each lane rounds its tokens i, i + 1 into one
+            // bf16x2 word and swaps it with lane n ^ 1; a byte permute then
+            // forms the word of two adjacent outputs of one token (the even
+            // lane token i, the odd lane token i + 1): one conversion, one
+            // shuffle, one permute and one store per two outputs.
             const int odd = lane & 1;
+            const uint32_t sel = odd ? 0x3276u : 0x5410u;
             uint32_t* const dstw = reinterpret_cast<uint32_t*>(dst - odd);
 #pragma unroll
             for (int i = 0; i < CW; i += 2) {
-              const float recv = __shfl_xor_sync(0xFFFFFFFFu, odd ? v[i] : v[i + 1], 1);
-              const uint32_t w = odd ? pack_bf16x2(recv, v[i + 1]) : pack_bf16x2(v[i], recv);
-              dstw[static_cast<int64_t>(i + odd) * (N / 2)] = w;
+              const uint32_t own = pack_bf16x2(v[i], v[i + 1]);
+              const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, own, 1);
+              dstw[static_cast<int64_t>(i + odd) * (N / 2)] = __byte_perm(own, other, sel);
             }
           } else {
 #pragma unroll
