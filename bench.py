@@ -8,7 +8,8 @@ tokens.  One step is one pass of the whole hot path over that layer set:
 
   requant  re-quantize all 7 bf16 weights to NVFP4 (absmax sweep + encode);
            requant_aqn the same with adaptive quantization noise added to the
-           masters (Philox noise regenerated in both sweeps)
+           masters (Philox noise drawn in the encode sweep, and in the absmax
+           sweep only for values that can hold the largest |W'|)
   decode   W4A16 + LoRA linear of all 7 layers at M = 1, 8 and 64 (one
            grouped call per token count)
   prefill  the same linears at M = 4096 (activations with 1% x10 channels)
@@ -23,6 +24,10 @@ tokens.  One step is one pass of the whole hot path over that layer set:
            cached tokens, 32 query / 8 KV heads of 128 (attn_fp8)
   is       token log-probabilities and importance-sampling weights of 4096
            tokens over a 128256-entry vocabulary (rollout_is)
+  floor    the memory floor of one decode pass: the one-token decode's bytes
+           streamed through the decode kernels' TMA ring of [128 x 128 B]
+           boxes with no arithmetic (stream_floor; a reference for the decode
+           phases, not part of the hot path)
 
 Re-quantization follows a training step: the bf16 masters alternate between W
 and W' = bf16(W + N(0, 1e-4)) from step to step, so every step recalibrates
@@ -102,6 +107,7 @@ PHASE_KERNELS = {  # phase -> (kernel name prefix, template arguments as ncu pri
     "fp8_gemm": ("fp8_gemm_tc_kernel", ""),
     "fp8_gemm_pow2": ("fp8_gemm_mx_kernel", ""),
     "rollout_is": ("token_logprob_is_kernel", ""),
+    "stream_floor": ("stream_probe_kernel", ""),
     "lora_bwd": ("gemm_bf16_tc_kernel", ""),
     "attn_fp8": ("attn_decode_fp8_kernel", ""),
 }
@@ -492,6 +498,16 @@ class Workload:
                                     workspace=a["ws"])
         return 3
 
+    def stream_floor(self):
+        # the memory-system floor of one decode pass: the one-token decode's
+        # bytes as a [rows x 2048] byte matrix (the shape of a 4096-wide
+        # layer's packed codes) through the decode kernels' TMA ring, no arithmetic
+        if getattr(self, "sbuf", None) is None:
+            rows = -(-decode_bytes(self.layers, 1, R) // (2048 * 128)) * 128
+            self.sbuf = torch.zeros(rows, 2048, dtype=torch.uint8, device=self.dev)
+        self.q.stream_probe(self.sbuf)
+        return 1
+
     def rollout_is(self):
         if getattr(self, "lg", None) is None:
             # token log-probabilities / importance weights over an 8B-class vocabulary
@@ -555,7 +571,7 @@ class Workload:
 # importance weights) are timed after it, each in a region of its own
 PHASES = ["requant", "decode_m1", "decode_m8", "decode_m64", "prefill", "fp8_requant", "fp8_act_quant", "fp8_gemm",
           "fp8_gemm_pow2"]
-NEXT_PHASES = ["requant_aqn", "lora_bwd", "attn_fp8", "rollout_is"]
+NEXT_PHASES = ["requant_aqn", "lora_bwd", "attn_fp8", "rollout_is", "stream_floor"]
 EXTRA_PHASES = ["requant32b", "decode32b"]
 
 
@@ -584,6 +600,8 @@ def run_phase(w, name):
         return w.lora_bwd()
     if name == "attn_fp8":
         return w.attn_fp8()
+    if name == "stream_floor":
+        return w.stream_floor()
     return w.fp8_gemm()
 
 
@@ -956,6 +974,12 @@ def main():
                             "frac_fp8_spec": f / ms / 1e9 / SPEC_PEAKS["fp8_tflops"], "flops": f,
                             "scale_mode": "fp32 (promotion)" if p == "fp8_gemm" else
                             "pow2 (native block-scaled MMA, UE8M0)"}
+        elif p == "stream_floor":
+            breakdown[p] = hbm(ms, w.sbuf.numel())
+            breakdown[p]["workload"] = ("TMA stream of the one-token decode's bytes in [128 x 128 B] boxes, "
+                                        "no arithmetic (the memory floor of one such pass)")
+            if "decode_m1" in med:
+                breakdown[p]["decode_m1_over_floor_time"] = ms / med["decode_m1"]
         elif p == "rollout_is":
             breakdown[p] = hbm(ms, IS_TOKENS * IS_VOCAB * 2 + IS_TOKENS * 16)
             breakdown[p]["workload"] = f"{IS_TOKENS} tokens x {IS_VOCAB} vocabulary, bf16 logits"

@@ -407,6 +407,16 @@ int64_t qrr_plan_decode_units(int64_t M, int32_t count, const int64_t* N, const 
  * either way. */
 qrr_status qrr_wait_probe(int64_t limit_cycles, int32_t arrive, int32_t* dev_status, int64_t* cycles, void* stream);
 
+/* Memory-system probe: the floor of one pass over a byte matrix, to set
+ * beside the decode kernels, which read a weight's packed codes the same way.
+ * `data` u8 [rows][row_bytes] (device, 16-byte aligned, rows and row_bytes
+ * multiples of 128) goes through an 8-stage shared-memory ring of
+ * [128 x 128 B] TMA boxes, one CTA per SM, each a contiguous range of boxes
+ * (row tiles outer, 128-byte column tiles inner), with no arithmetic on the
+ * bytes.  Nothing is written.  A bounded wait that runs out sets
+ * QRR_DEV_TIMEOUT in *dev_status (nullable). */
+qrr_status qrr_stream_probe(const void* data, int64_t rows, int64_t row_bytes, int32_t* dev_status, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Re-quantization with adaptive quantization noise ("QeRL: Beyond Efficiency
  * -- Quantization-enhanced Reinforcement Learning for LLMs", Abstract: noise

@@ -867,6 +867,16 @@ qrr_status qrr_wait_probe(int64_t limit_cycles, int32_t arrive, int32_t* dev_sta
                                      as_stream(stream)));
 }
 
+qrr_status qrr_stream_probe(const void* data, int64_t rows, int64_t row_bytes, int32_t* dev_status, void* stream) {
+  if (rows < 0 || row_bytes < 0 || (rows * row_bytes > 0 && !data)) return QRR_ERR_INVALID_ARG;
+  if (rows % 128 != 0 || row_bytes % 128 != 0 || rows > INT32_MAX || row_bytes > INT32_MAX)
+    return QRR_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(data) || (reinterpret_cast<uintptr_t>(dev_status) & 3u)) return QRR_ERR_MISALIGNED;
+  if (injected_cuda_fault()) return QRR_ERR_CUDA;
+  if (rows == 0 || row_bytes == 0) return QRR_OK;
+  return from_cuda(launch_stream_probe(data, rows, row_bytes, dev_status, as_stream(stream)));
+}
+
 qrr_status qrr_requantize_weights(const qrr_weight_desc* descs, int32_t count, int32_t format, int32_t scale_mode,
                                   void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
   return requantize(descs, count, format, scale_mode, aqn_params(0.0f, 0u, 0ull), workspace, workspace_bytes,

@@ -242,5 +242,8 @@ cudaError_t launch_token_logprob_is(const void* logits, int64_t T, int64_t V, co
 // limit: give-up time of the wait in SM clock cycles; arrive: complete the
 // barrier before waiting; cycles (nullable, device): the wait's duration.
 cudaError_t launch_wait_probe(long long limit, int arrive, int32_t* status, long long* cycles, cudaStream_t stream);
+// A TMA stream of [128 x 128 B] boxes over a byte matrix with no arithmetic (probe.cu).
+cudaError_t launch_stream_probe(const void* data, int64_t rows, int64_t row_bytes, int32_t* status,
+                                cudaStream_t stream);
 
 }  // namespace qrr

@@ -92,6 +92,7 @@ SIGNATURES = {
                                              _c_p]),
     "qrr_workspace_bytes": (_c_sz, [_c_i32, _c_i64, _c_i64, _c_i64, _c_i32]),
     "qrr_wait_probe": (ctypes.c_int, [_c_i64, _c_i32, _c_p, _c_p, _c_p]),
+    "qrr_stream_probe": (ctypes.c_int, [_c_p, _c_i64, _c_i64, _c_p, _c_p]),
     "qrr_plan_decode_units": (_c_i64, [_c_i64, _c_i32, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_p]),
 }
 
@@ -403,6 +404,18 @@ def wait_probe(limit_cycles, arrive, dev_status, cycles=None, stream=None):
         _need(cycles, torch.int64, "cycles")
     _check(lib().qrr_wait_probe(int(limit_cycles), int(arrive), _ptr(dev_status), _ptr(cycles), _stream(stream)),
            "qrr_wait_probe")
+
+
+def stream_probe(data, dev_status=None, stream=None):
+    """Stream a uint8 [rows, row_bytes] matrix through the TMA ring of the
+    decode kernels with no arithmetic (see ``qrr_stream_probe``)."""
+    _need(data, torch.uint8, "data")
+    if data.dim() != 2:
+        raise ValueError("stream_probe: data must be a 2-D uint8 tensor")
+    if dev_status is not None:
+        _need(dev_status, torch.int32, "dev_status")
+    _check(lib().qrr_stream_probe(_ptr(data), data.shape[0], data.shape[1], _ptr(dev_status), _stream(stream)),
+           "qrr_stream_probe")
 
 
 def token_logprobs_is(logits, tokens, rollout_logp=None, cap=0.0, logp=None, w=None, dev_status=None, stream=None):

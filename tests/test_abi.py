@@ -136,6 +136,14 @@ def test_status_sync_and_probe_validation(lib):
     assert lib.qrr_wait_probe(1000, 2, FAKE, None, None) == 1
     assert lib.qrr_wait_probe(1000, 0, None, None, None) == 1
     assert lib.qrr_wait_probe(1000, 0, FAKE, FAKE + 4, None) == 3
+    # the stream probe: shapes in whole 128-row, 128-byte boxes, aligned data
+    assert lib.qrr_stream_probe(None, 128, 128, None, None) == 1
+    assert lib.qrr_stream_probe(FAKE, -128, 128, None, None) == 1
+    assert lib.qrr_stream_probe(FAKE, 130, 128, None, None) == 2
+    assert lib.qrr_stream_probe(FAKE, 128, 100, None, None) == 2
+    assert lib.qrr_stream_probe(FAKE + 8, 128, 128, None, None) == 3
+    assert lib.qrr_stream_probe(FAKE, 128, 128, FAKE + 2, None) == 3
+    assert lib.qrr_stream_probe(FAKE, 0, 128, None, None) == 0  # nothing to stream, nothing launched
 
 
 def test_generic_workspace_query_matches_per_call_queries(lib):

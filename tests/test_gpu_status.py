@@ -79,3 +79,15 @@ def test_context_usable_after_timeout(q):
     y_ref = oracle.linear.linear_nvfp4_lora(to_np(x), rc, rs, rt, to_np(A), to_np(B), c["alpha"])
     ok, nerr, worst = oracle.linear.within_tolerance(to_np(y), y_ref)
     assert ok, f"normwise {nerr:.3e}, worst {worst:.3f}"
+
+
+def test_stream_probe_runs_clean(q):
+    """The memory-floor probe streams a byte matrix through the decode
+    kernels' TMA ring and finishes without flagging anything: a few boxes,
+    a ragged share per CTA, and the one-token decode's size."""
+    for rows, cols in [(128, 128), (384, 640), (62592, 2048)]:
+        data = torch.zeros(rows, cols, dtype=torch.uint8, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        q.stream_probe(data, dev_status=st)
+        torch.cuda.synchronize()
+        assert q.get_last_device_status(st) == 0
