@@ -157,3 +157,22 @@ def _noisy_at(flat, i, sigma, seed, j, step):
     x = np.float32(flat[i].float().item())
     z = aqn.noise(1, seed, j, step, start=i)[0]
     return oracle.formats.bf16_rne(np.array([x + np.float32(np.float32(sigma) * z)], np.float32))[0]
+
+
+@pytest.mark.parametrize("bad", [float("inf"), float("-inf"), float("nan")])
+def test_nvfp4_noisy_absmax_flags_nonfinite(q, bad):
+    """A non-finite master takes the noisy absmax sweep's fallback (every
+    vector drawn): the device status still reports it, and a clean tensor
+    in the same call raises nothing on its own."""
+    W = (torch.randn(256, 512, device=DEV) * 0.02).to(torch.bfloat16)
+    W[100, 37] = bad
+    outs = [_nv_out(256, 512)]
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    q.requantize_weights_aqn([W], outs, 1e-3, 7, 3, dev_status=st)
+    torch.cuda.synchronize()
+    assert q.get_last_device_status(st) & q.DEV_NONFINITE
+    ok = torch.zeros(1, dtype=torch.int32, device=DEV)
+    clean = (torch.randn(256, 512, device=DEV) * 0.02).to(torch.bfloat16)
+    q.requantize_weights_aqn([clean], [_nv_out(256, 512)], 1e-3, 7, 3, dev_status=ok)
+    torch.cuda.synchronize()
+    assert q.get_last_device_status(ok) == 0
